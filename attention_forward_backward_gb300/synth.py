@@ -1,0 +1,157 @@
+"""Seeded synthetic inputs shared by the CUDA path's tests/bench and the oracle.
+
+This module holds no attention arithmetic: it only draws numbers. Both sides
+receive the SAME arrays from here, so neither depends on the other.
+
+Generator (a counter-based stream, written from its published definitions):
+
+* SplitMix64 (Steele, Lea, Flood, "Fast splittable pseudorandom number
+  generators", OOPSLA 2014): output n of the stream with state ``seed`` is
+  ``mix(seed + (n + 1) * 0x9E3779B97F4A7C15)`` with the Stafford "Mix13"
+  finaliser (shifts 30/27/31, multipliers 0xBF58476D1CE4E5B9 and
+  0x94D049BB133111EB).
+* A uniform double in [0, 1) is the top 53 bits of an output times 2^-53.
+* Element n of a tensor is one Box-Muller normal (Box & Muller 1958) from the
+  outputs 2n and 2n+1: ``sqrt(-2 ln(1 - u0)) * cos(2 pi u1)``, computed in
+  float64 and rounded once to float32 (round to nearest even).
+* Flat element order is the row-major order of [B, H, L, D].
+* Seeds: ``1000 * cfg + tensor_id`` with Q = 0, K = 1, V = 2, dO = 3.
+
+bf16 inputs (the accelerated contract) are the float32 values rounded to
+bfloat16 with IEEE round-to-nearest-even on the bit pattern, done here so that
+the GPU and the oracle get bit-identical operands.
+"""
+from __future__ import annotations
+
+import math
+from dataclasses import dataclass
+
+import numpy as np
+
+_GAMMA = np.uint64(0x9E3779B97F4A7C15)
+_M1 = np.uint64(0xBF58476D1CE4E5B9)
+_M2 = np.uint64(0x94D049BB133111EB)
+
+TENSOR_IDS = {"Q": 0, "K": 1, "V": 2, "dO": 3}
+
+
+def _mix(z: np.ndarray) -> np.ndarray:
+    z = (z ^ (z >> np.uint64(30))) * _M1
+    z = (z ^ (z >> np.uint64(27))) * _M2
+    return z ^ (z >> np.uint64(31))
+
+
+def splitmix64(seed: int, start: int, count: int) -> np.ndarray:
+    """Outputs ``start .. start+count-1`` of the SplitMix64 stream for ``seed``."""
+    n = np.arange(start + 1, start + count + 1, dtype=np.uint64)
+    with np.errstate(over="ignore"):
+        z = np.uint64(seed & 0xFFFFFFFFFFFFFFFF) + n * _GAMMA
+        return _mix(z)
+
+
+def normal_f32(seed: int, count: int, chunk: int = 1 << 22) -> np.ndarray:
+    """``count`` standard normals as float32, element n from outputs 2n, 2n+1."""
+    out = np.empty(count, dtype=np.float32)
+    two_pi = 2.0 * math.pi
+    for s in range(0, count, chunk):
+        c = min(chunk, count - s)
+        r = splitmix64(seed, 2 * s, 2 * c).reshape(c, 2)
+        u = (r >> np.uint64(11)).astype(np.float64) * (1.0 / 9007199254740992.0)
+        rad = np.sqrt(-2.0 * np.log1p(-u[:, 0]))
+        out[s:s + c] = (rad * np.cos(two_pi * u[:, 1])).astype(np.float32)
+    return out
+
+
+def round_to_bf16(x: np.ndarray) -> np.ndarray:
+    """Round float32 to the nearest bfloat16 (ties to even); returns the uint16
+    bit patterns. Inputs here are finite normals, so no NaN handling is needed."""
+    b = np.ascontiguousarray(x, dtype=np.float32).view(np.uint32)
+    lsb = (b >> np.uint32(16)) & np.uint32(1)
+    r = (b + np.uint32(0x7FFF) + lsb) >> np.uint32(16)
+    return r.astype(np.uint16)
+
+
+def bf16_bits_to_f32(bits: np.ndarray) -> np.ndarray:
+    return (np.asarray(bits, dtype=np.uint16).astype(np.uint32) << np.uint32(16)).view(np.float32)
+
+
+@dataclass(frozen=True)
+class Workload:
+    """One seeded attention workload. Shapes are [B, H, L, D] row-major."""
+    cfg: int
+    B: int
+    H: int
+    L: int
+    D: int
+    causal: bool
+    contracts: tuple
+    qk_gain: float = 1.0
+    name: str = ""
+
+    @property
+    def scale(self) -> float:
+        return 1.0 / math.sqrt(self.D)
+
+    @property
+    def shape(self):
+        return (self.B, self.H, self.L, self.D)
+
+    @property
+    def numel(self) -> int:
+        return self.B * self.H * self.L * self.D
+
+    def flops_fwd(self) -> float:
+        """4 B H L^2 D, halved when causal (the convention the throughput
+        numbers are quoted in; not L(L+1)/2)."""
+        f = 4.0 * self.B * self.H * self.L * self.L * self.D
+        return f / 2 if self.causal else f
+
+    def flops_bwd(self) -> float:
+        return 2.5 * self.flops_fwd()
+
+
+# The five workloads. Scale is 1/sqrt(D) everywhere; cfg 4 multiplies the Q
+# and K draws by 4 so that logits have standard deviation 16.
+WORKLOADS = {
+    1: Workload(1, 1, 2, 64, 32, True, ("strict",), name="tiny causal B1 H2 L64 D32"),
+    2: Workload(2, 4, 8, 512, 64, True, ("strict", "accel"), name="decoder causal B4 H8 L512 D64"),
+    3: Workload(3, 32, 12, 197, 64, False, ("accel",), name="encoder full B32 H12 L197 D64"),
+    4: Workload(4, 8, 16, 2048, 64, True, ("strict", "accel"), qk_gain=4.0,
+                name="large-logit causal B8 H16 L2048 D64 (Q,K x4)"),
+    5: Workload(5, 2, 32, 8192, 128, True, ("strict", "accel"),
+                name="long-sequence causal B2 H32 L8192 D128"),
+}
+
+
+def tensor_f32(w: Workload, which: str) -> np.ndarray:
+    """Seeded float32 tensor ``which`` in {Q, K, V, dO} of workload ``w``."""
+    seed = 1000 * w.cfg + TENSOR_IDS[which]
+    x = normal_f32(seed, w.numel).reshape(w.shape)
+    if which in ("Q", "K") and w.qk_gain != 1.0:
+        x *= np.float32(w.qk_gain)
+    return x
+
+
+def inputs(w: Workload, contract: str):
+    """Dict of host inputs for a contract.
+
+    strict -> float32 arrays. accel -> uint16 bf16 bit patterns (key "bits")
+    plus their exact float32 values (key "values"), which the oracle consumes.
+    """
+    out = {}
+    for t in ("Q", "K", "V", "dO"):
+        x = tensor_f32(w, t)
+        if contract == "strict":
+            out[t] = x
+        elif contract == "accel":
+            bits = round_to_bf16(x)
+            out[t] = {"bits": bits, "values": bf16_bits_to_f32(bits)}
+        else:
+            raise ValueError(contract)
+    return out
+
+
+def custom_workload(B, H, L, D, causal, seed_cfg=900, qk_gain=1.0) -> Workload:
+    """An ad-hoc workload (edge cases in tests) with its own seed block."""
+    return Workload(seed_cfg, B, H, L, D, bool(causal), ("strict", "accel"), qk_gain,
+                    name=f"custom B{B} H{H} L{L} D{D} {'causal' if causal else 'full'}")
