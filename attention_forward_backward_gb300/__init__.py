@@ -1,0 +1,190 @@
+"""Python binding of libmgattn.so (ctypes): multi-head scaled-dot-product
+attention forward + backward on one GB300 GPU.
+
+Argument marshalling only. Every step of the computation runs in the CUDA
+library; there is no Python, PyTorch or CPU fallback. If the library has not
+been built, or the CUDA device is missing, the calls raise.
+
+The function names mirror the C ABI in ``include/mg_attn.h``:
+
+* ``mg_attn_fwd(Q, K, V, O, LSE, causal, scale, contract, stream=None)``
+* ``mg_attn_bwd_workspace_bytes(B, H, L, D, contract)``
+* ``mg_attn_bwd(Q, K, V, O, dO, LSE, dQ, dK, dV, causal, scale, contract,
+  workspace, stream=None)``
+* ``mg_status_string(status)``, ``mg_get_device_error(stream=None)``
+* ``mg_attn_profile_enable``, ``mg_attn_profile_read``, ``mg_attn_kernel_name``
+
+Tensors are PyTorch CUDA tensors, contiguous [B, H, L, D] (LSE [B, H, L]); the
+shape is read from Q. ``contract`` is ``STRICT_F32`` (0) or ``ACCEL_BF16`` (1).
+``attention_fwd`` / ``attention_bwd`` are conveniences that allocate the
+outputs with PyTorch and call the above.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+
+STRICT_F32 = 0
+ACCEL_BF16 = 1
+CONTRACTS = {"strict": STRICT_F32, "accel": ACCEL_BF16}
+
+MG_OK, MG_ERR_INVALID_ARG, MG_ERR_UNSUPPORTED, MG_ERR_WORKSPACE, MG_ERR_CUDA, MG_ERR_TIMEOUT = range(6)
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "libmgattn.so")
+_lock = threading.Lock()
+_lib = None
+
+
+class MgError(RuntimeError):
+    def __init__(self, status: int, what: str):
+        self.status = status
+        super().__init__(f"{what}: {mg_status_string(status)} ({status})")
+
+
+def load_library(path: str | None = None):
+    """Load libmgattn.so (raises if it has not been built)."""
+    global _lib
+    with _lock:
+        if _lib is not None:
+            return _lib
+        p = path or LIB_PATH
+        if not os.path.exists(p):
+            raise RuntimeError(
+                f"{p} is missing: build the CUDA library first "
+                "(python -c 'import __graft_entry__ as g; g.build()')")
+        lib = ctypes.CDLL(p)
+        vp, i, f, sz = ctypes.c_void_p, ctypes.c_int, ctypes.c_float, ctypes.c_size_t
+        lib.mg_attn_fwd.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, i, f, i, vp]
+        lib.mg_attn_fwd.restype = i
+        lib.mg_attn_bwd_workspace_bytes.argtypes = [i, i, i, i, i]
+        lib.mg_attn_bwd_workspace_bytes.restype = sz
+        lib.mg_attn_bwd.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, i, i, i, i, i, f, i,
+                                    vp, sz, vp]
+        lib.mg_attn_bwd.restype = i
+        lib.mg_status_string.argtypes = [i]
+        lib.mg_status_string.restype = ctypes.c_char_p
+        lib.mg_get_device_error.argtypes = [vp]
+        lib.mg_get_device_error.restype = i
+        lib.mg_attn_profile_enable.argtypes = [i, i]
+        lib.mg_attn_profile_enable.restype = i
+        lib.mg_attn_profile_read.argtypes = [i, ctypes.POINTER(i), ctypes.POINTER(ctypes.c_double)]
+        lib.mg_attn_profile_read.restype = i
+        lib.mg_attn_kernel_count.argtypes = []
+        lib.mg_attn_kernel_count.restype = i
+        lib.mg_attn_kernel_name.argtypes = [i]
+        lib.mg_attn_kernel_name.restype = ctypes.c_char_p
+        _lib = lib
+        return lib
+
+
+def _ptr(t) -> int | None:
+    if t is None:
+        return None
+    if isinstance(t, int):
+        return t
+    return t.data_ptr()
+
+
+def _stream(stream) -> int | None:
+    if stream is None:
+        import torch
+        return torch.cuda.current_stream().cuda_stream
+    if isinstance(stream, int):
+        return stream
+    return stream.cuda_stream
+
+
+def _dims(Q):
+    if Q.dim() != 4:
+        raise ValueError("expected a [B, H, L, D] tensor")
+    return tuple(int(x) for x in Q.shape)
+
+
+def _contract(c) -> int:
+    return CONTRACTS[c] if isinstance(c, str) else int(c)
+
+
+def mg_status_string(status: int) -> str:
+    return load_library().mg_status_string(int(status)).decode()
+
+
+def mg_attn_fwd(Q, K, V, O, LSE, causal, scale, contract, stream=None) -> int:
+    B, H, L, D = _dims(Q)
+    rc = load_library().mg_attn_fwd(_ptr(Q), _ptr(K), _ptr(V), _ptr(O), _ptr(LSE), B, H, L, D,
+                                    int(bool(causal)), float(scale), _contract(contract),
+                                    _stream(stream))
+    if rc != MG_OK:
+        raise MgError(rc, "mg_attn_fwd")
+    return rc
+
+
+def mg_attn_bwd_workspace_bytes(B, H, L, D, contract) -> int:
+    return int(load_library().mg_attn_bwd_workspace_bytes(B, H, L, D, _contract(contract)))
+
+
+def mg_attn_bwd(Q, K, V, O, dO, LSE, dQ, dK, dV, causal, scale, contract, workspace,
+                stream=None) -> int:
+    B, H, L, D = _dims(Q)
+    ws_bytes = workspace.numel() * workspace.element_size() if workspace is not None else 0
+    rc = load_library().mg_attn_bwd(_ptr(Q), _ptr(K), _ptr(V), _ptr(O), _ptr(dO), _ptr(LSE),
+                                    _ptr(dQ), _ptr(dK), _ptr(dV), B, H, L, D,
+                                    int(bool(causal)), float(scale), _contract(contract),
+                                    _ptr(workspace), ws_bytes, _stream(stream))
+    if rc != MG_OK:
+        raise MgError(rc, "mg_attn_bwd")
+    return rc
+
+
+def mg_get_device_error(stream=None) -> int:
+    return int(load_library().mg_get_device_error(_stream(stream)))
+
+
+def mg_attn_profile_enable(enable: bool, capacity: int = 4096) -> None:
+    rc = load_library().mg_attn_profile_enable(int(bool(enable)), int(capacity))
+    if rc != MG_OK:
+        raise MgError(rc, "mg_attn_profile_enable")
+
+
+def mg_attn_profile_read(kernel: int):
+    n = ctypes.c_int(0)
+    ms = ctypes.c_double(0.0)
+    rc = load_library().mg_attn_profile_read(int(kernel), ctypes.byref(n), ctypes.byref(ms))
+    if rc != MG_OK:
+        raise MgError(rc, "mg_attn_profile_read")
+    return n.value, ms.value
+
+
+def mg_attn_kernel_count() -> int:
+    return int(load_library().mg_attn_kernel_count())
+
+
+def mg_attn_kernel_name(kernel: int) -> str:
+    return load_library().mg_attn_kernel_name(int(kernel)).decode()
+
+
+# ------------------------------------------------------------ conveniences
+def attention_fwd(Q, K, V, causal: bool, scale: float, contract, stream=None):
+    """Allocate O (f32) and LSE (f32) with PyTorch and run mg_attn_fwd."""
+    import torch
+    B, H, L, D = _dims(Q)
+    O = torch.empty((B, H, L, D), dtype=torch.float32, device=Q.device)
+    LSE = torch.empty((B, H, L), dtype=torch.float32, device=Q.device)
+    mg_attn_fwd(Q, K, V, O, LSE, causal, scale, contract, stream)
+    return O, LSE
+
+
+def attention_bwd(Q, K, V, O, dO, LSE, causal: bool, scale: float, contract, stream=None,
+                  workspace=None):
+    """Allocate dQ, dK, dV (f32) and the workspace with PyTorch; run mg_attn_bwd."""
+    import torch
+    B, H, L, D = _dims(Q)
+    dQ = torch.empty((B, H, L, D), dtype=torch.float32, device=Q.device)
+    dK = torch.empty_like(dQ)
+    dV = torch.empty_like(dQ)
+    if workspace is None:
+        nbytes = mg_attn_bwd_workspace_bytes(B, H, L, D, contract)
+        workspace = torch.empty(nbytes, dtype=torch.uint8, device=Q.device)
+    mg_attn_bwd(Q, K, V, O, dO, LSE, dQ, dK, dV, causal, scale, contract, workspace, stream)
+    return dQ, dK, dV

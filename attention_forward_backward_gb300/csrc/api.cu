@@ -1,0 +1,326 @@
+// api.cu -- the C ABI of libmgattn.so (declared in include/mg_attn.h):
+// argument validation, dispatch on (contract, D), the per-device error word
+// and the optional per-kernel event timing used by benchmarks.
+//
+// The pages ("Meganeura: Portable GPU Training and Inference through Vulkan and
+// Metal", Sections 3.5 and 5.6) keep every buffer owned by a static plan and
+// allocate nothing while a step runs; the calls here follow the same rule:
+// they validate, then enqueue kernels on the caller's stream.
+#include <math.h>
+#include <string.h>
+
+#include <mutex>
+
+#include "../../include/mg_attn.h"
+#include "internal.h"
+
+namespace {
+
+constexpr int kMaxDevices = 64;
+constexpr int kMaxSlots = 32;
+
+// Device error word: bounded waits in the ACCEL kernels write a code here
+// instead of trapping. One copy per device (module globals are per context).
+__device__ unsigned int g_mg_device_error;
+
+std::mutex g_mu;
+unsigned int *g_err_ptr[kMaxDevices] = {};
+bool g_smem_done[kMaxDevices][kMaxSlots] = {};
+
+int current_device() {
+  int dev = -1;
+  if (cudaGetDevice(&dev) != cudaSuccess) return -1;
+  return dev;
+}
+
+// Device address of the error word for the current device (looked up once).
+unsigned int *device_error_word() {
+  const int dev = current_device();
+  if (dev < 0 || dev >= kMaxDevices) return nullptr;
+  std::lock_guard<std::mutex> lk(g_mu);
+  if (!g_err_ptr[dev]) {
+    void *p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_mg_device_error) != cudaSuccess) return nullptr;
+    g_err_ptr[dev] = static_cast<unsigned int *>(p);
+  }
+  return g_err_ptr[dev];
+}
+
+// ---------------------------------------------------------------- profiling
+struct ProfState {
+  bool enabled = false;
+  int capacity = 0;
+  int used = 0;
+  cudaEvent_t *ev = nullptr;  // 2 * capacity
+  int *kid = nullptr;         // kernel id of each pair
+};
+ProfState g_prof;
+
+struct ProfScope {
+  int pair = -1;
+  cudaStream_t st;
+  ProfScope(int kernel, cudaStream_t s) : st(s) {
+    std::lock_guard<std::mutex> lk(g_mu);
+    if (!g_prof.enabled || g_prof.used >= g_prof.capacity) return;
+    pair = g_prof.used++;
+    g_prof.kid[pair] = kernel;
+    cudaEventRecord(g_prof.ev[2 * pair], st);
+  }
+  ~ProfScope() {
+    if (pair >= 0) cudaEventRecord(g_prof.ev[2 * pair + 1], st);
+  }
+};
+
+void prof_free() {
+  if (g_prof.ev) {
+    for (int i = 0; i < 2 * g_prof.capacity; ++i) cudaEventDestroy(g_prof.ev[i]);
+    delete[] g_prof.ev;
+    delete[] g_prof.kid;
+  }
+  g_prof = ProfState();
+}
+
+const char *const kKernelNames[MGK_COUNT] = {
+    "strict_fwd", "strict_dvec", "strict_dkdv_dq", "accel_fwd",
+    "accel_dvec", "accel_dkdv_dq", "dq_zero"};
+
+// ---------------------------------------------------------------- validation
+bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+struct Range {
+  uintptr_t lo, hi;
+};
+bool overlap(Range a, Range b) { return a.lo < b.hi && b.lo < a.hi; }
+
+int check_common(int B, int H, int L, int D, int causal, float scale, int contract) {
+  if (B < 1 || H < 1 || L < 1) return MG_ERR_INVALID_ARG;
+  if (static_cast<long long>(B) * H > (1LL << 24) || L > (1 << 20)) return MG_ERR_INVALID_ARG;
+  if (causal != 0 && causal != 1) return MG_ERR_INVALID_ARG;
+  if (!(scale > 0.f) || !isfinite(scale)) return MG_ERR_INVALID_ARG;
+  if (contract != MG_CONTRACT_STRICT_F32 && contract != MG_CONTRACT_ACCEL_BF16)
+    return MG_ERR_INVALID_ARG;
+  if (D != 32 && D != 64 && D != 128) return MG_ERR_UNSUPPORTED;
+  return MG_OK;
+}
+
+int check_ptrs(const void *const *ptrs, int n) {
+  for (int i = 0; i < n; ++i)
+    if (!ptrs[i] || !aligned16(ptrs[i])) return MG_ERR_INVALID_ARG;
+  return MG_OK;
+}
+
+// Outputs must not overlap inputs or each other.
+int check_alias(const Range *in, int nin, const Range *out, int nout) {
+  for (int o = 0; o < nout; ++o) {
+    for (int i = 0; i < nin; ++i)
+      if (overlap(out[o], in[i])) return MG_ERR_INVALID_ARG;
+    for (int p = o + 1; p < nout; ++p)
+      if (overlap(out[o], out[p])) return MG_ERR_INVALID_ARG;
+  }
+  return MG_OK;
+}
+
+Range rng(const void *p, size_t bytes) {
+  const uintptr_t a = reinterpret_cast<uintptr_t>(p);
+  return Range{a, a + bytes};
+}
+
+int map_cuda(cudaError_t e) { return e == cudaSuccess ? MG_OK : MG_ERR_CUDA; }
+
+size_t ws_bytes(int B, int H, int L) {
+  const size_t dvec = static_cast<size_t>(B) * H * L * sizeof(float);
+  return (dvec + 255) & ~static_cast<size_t>(255);
+}
+
+}  // namespace
+
+cudaError_t mg_set_smem_attr(const void *func, int bytes, int slot) {
+  const int dev = current_device();
+  if (dev < 0) return cudaErrorNoDevice;
+  if (dev >= kMaxDevices || slot < 0 || slot >= kMaxSlots)
+    return cudaFuncSetAttribute(func, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+  {
+    std::lock_guard<std::mutex> lk(g_mu);
+    if (g_smem_done[dev][slot]) return cudaSuccess;
+  }
+  cudaError_t e = cudaFuncSetAttribute(func, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+  if (e == cudaSuccess) {
+    std::lock_guard<std::mutex> lk(g_mu);
+    g_smem_done[dev][slot] = true;
+  }
+  return e;
+}
+
+extern "C" {
+
+const char *mg_status_string(int status) {
+  switch (status) {
+    case MG_OK: return "MG_OK";
+    case MG_ERR_INVALID_ARG: return "MG_ERR_INVALID_ARG: invalid argument";
+    case MG_ERR_UNSUPPORTED: return "MG_ERR_UNSUPPORTED: head dim must be 32, 64 or 128";
+    case MG_ERR_WORKSPACE: return "MG_ERR_WORKSPACE: workspace missing or too small";
+    case MG_ERR_CUDA: return "MG_ERR_CUDA: CUDA runtime error";
+    case MG_ERR_TIMEOUT: return "MG_ERR_TIMEOUT: a kernel gave up on a bounded wait";
+    default: return "unknown mg_status_t";
+  }
+}
+
+int mg_attn_fwd(const void *Q, const void *K, const void *V, void *O, float *LSE, int B, int H,
+                int L, int D, int causal, float scale, int contract, void *stream) {
+  int rc = check_common(B, H, L, D, causal, scale, contract);
+  if (rc) return rc;
+  const void *ptrs[] = {Q, K, V, O, LSE};
+  if ((rc = check_ptrs(ptrs, 5))) return rc;
+  const size_t n = static_cast<size_t>(B) * H * L * D;
+  const size_t in_el = contract == MG_CONTRACT_STRICT_F32 ? 4 : 2;
+  const Range in[] = {rng(Q, n * in_el), rng(K, n * in_el), rng(V, n * in_el)};
+  const Range out[] = {rng(O, n * 4), rng(LSE, static_cast<size_t>(B) * H * L * 4)};
+  if ((rc = check_alias(in, 3, out, 2))) return rc;
+
+  const MgProblem p{B, H, L, D, causal, scale};
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  cudaError_t e;
+  if (contract == MG_CONTRACT_STRICT_F32) {
+    ProfScope ps(MGK_STRICT_FWD, st);
+    e = mg_launch_strict_fwd(static_cast<const float *>(Q), static_cast<const float *>(K),
+                             static_cast<const float *>(V), static_cast<float *>(O), LSE, p, st);
+  } else {
+    unsigned int *err = device_error_word();
+    if (!err) return MG_ERR_CUDA;
+    ProfScope ps(MGK_ACCEL_FWD, st);
+    e = mg_launch_accel_fwd(static_cast<const __nv_bfloat16 *>(Q),
+                            static_cast<const __nv_bfloat16 *>(K),
+                            static_cast<const __nv_bfloat16 *>(V), static_cast<float *>(O), LSE,
+                            p, err, st);
+  }
+  return map_cuda(e);
+}
+
+size_t mg_attn_bwd_workspace_bytes(int B, int H, int L, int D, int contract) {
+  if (check_common(B, H, L, D, 0, 1.f, contract) != MG_OK) return 0;
+  return ws_bytes(B, H, L);
+}
+
+int mg_attn_bwd(const void *Q, const void *K, const void *V, const void *O, const void *dO,
+                const float *LSE, void *dQ, void *dK, void *dV, int B, int H, int L, int D,
+                int causal, float scale, int contract, void *workspace, size_t workspace_bytes,
+                void *stream) {
+  int rc = check_common(B, H, L, D, causal, scale, contract);
+  if (rc) return rc;
+  const void *ptrs[] = {Q, K, V, O, dO, LSE, dQ, dK, dV};
+  if ((rc = check_ptrs(ptrs, 9))) return rc;
+  if (!workspace || !aligned16(workspace) || workspace_bytes < ws_bytes(B, H, L))
+    return MG_ERR_WORKSPACE;
+  const size_t n = static_cast<size_t>(B) * H * L * D;
+  const size_t rows = static_cast<size_t>(B) * H * L;
+  const size_t in_el = contract == MG_CONTRACT_STRICT_F32 ? 4 : 2;
+  const Range in[] = {rng(Q, n * in_el), rng(K, n * in_el), rng(V, n * in_el),
+                      rng(dO, n * in_el), rng(O, n * 4),      rng(LSE, rows * 4)};
+  const Range out[] = {rng(dQ, n * 4), rng(dK, n * 4), rng(dV, n * 4),
+                       rng(workspace, ws_bytes(B, H, L))};
+  if ((rc = check_alias(in, 6, out, 4))) return rc;
+
+  const MgProblem p{B, H, L, D, causal, scale};
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  float *Dvec = static_cast<float *>(workspace);
+  cudaError_t e;
+  if (contract == MG_CONTRACT_STRICT_F32) {
+    {
+      ProfScope ps(MGK_STRICT_DVEC, st);
+      e = mg_launch_dvec_f32(static_cast<const float *>(O), static_cast<const float *>(dO), Dvec,
+                             p, st);
+    }
+    if (e != cudaSuccess) return MG_ERR_CUDA;
+    {
+      ProfScope ps(MGK_DQ_ZERO, st);
+      e = cudaMemsetAsync(dQ, 0, n * 4, st);
+    }
+    if (e != cudaSuccess) return MG_ERR_CUDA;
+    ProfScope ps(MGK_STRICT_DKDV, st);
+    e = mg_launch_strict_dkdv(static_cast<const float *>(Q), static_cast<const float *>(K),
+                              static_cast<const float *>(V), static_cast<const float *>(dO), LSE,
+                              Dvec, static_cast<float *>(dQ), static_cast<float *>(dK),
+                              static_cast<float *>(dV), p, st);
+  } else {
+    unsigned int *err = device_error_word();
+    if (!err) return MG_ERR_CUDA;
+    {
+      ProfScope ps(MGK_ACCEL_DVEC, st);
+      e = mg_launch_dvec_bf16(static_cast<const float *>(O),
+                              static_cast<const __nv_bfloat16 *>(dO), Dvec, p, st);
+    }
+    if (e != cudaSuccess) return MG_ERR_CUDA;
+    {
+      ProfScope ps(MGK_DQ_ZERO, st);
+      e = cudaMemsetAsync(dQ, 0, n * 4, st);
+    }
+    if (e != cudaSuccess) return MG_ERR_CUDA;
+    ProfScope ps(MGK_ACCEL_DKDV, st);
+    e = mg_launch_accel_dkdv(
+        static_cast<const __nv_bfloat16 *>(Q), static_cast<const __nv_bfloat16 *>(K),
+        static_cast<const __nv_bfloat16 *>(V), static_cast<const __nv_bfloat16 *>(dO), LSE, Dvec,
+        static_cast<float *>(dQ), static_cast<float *>(dK), static_cast<float *>(dV), p, err, st);
+  }
+  return map_cuda(e);
+}
+
+int mg_get_device_error(void *stream) {
+  unsigned int *err = device_error_word();
+  if (!err) return MG_ERR_CUDA;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  unsigned int h = 0;
+  if (cudaMemcpyAsync(&h, err, sizeof(h), cudaMemcpyDeviceToHost, st) != cudaSuccess)
+    return MG_ERR_CUDA;
+  if (cudaMemsetAsync(err, 0, sizeof(h), st) != cudaSuccess) return MG_ERR_CUDA;
+  if (cudaStreamSynchronize(st) != cudaSuccess) return MG_ERR_CUDA;
+  return h == MG_DEVERR_NONE ? MG_OK : MG_ERR_TIMEOUT;
+}
+
+int mg_attn_profile_enable(int enable, int capacity) {
+  std::lock_guard<std::mutex> lk(g_mu);
+  prof_free();
+  if (!enable) return MG_OK;
+  if (capacity < 1 || capacity > (1 << 20)) return MG_ERR_INVALID_ARG;
+  g_prof.ev = new cudaEvent_t[2 * static_cast<size_t>(capacity)];
+  g_prof.kid = new int[capacity];
+  for (int i = 0; i < 2 * capacity; ++i) {
+    if (cudaEventCreate(&g_prof.ev[i]) != cudaSuccess) {
+      for (int j = 0; j < i; ++j) cudaEventDestroy(g_prof.ev[j]);
+      delete[] g_prof.ev;
+      delete[] g_prof.kid;
+      g_prof = ProfState();
+      return MG_ERR_CUDA;
+    }
+  }
+  g_prof.capacity = capacity;
+  g_prof.enabled = true;
+  return MG_OK;
+}
+
+int mg_attn_profile_read(int kernel, int *launches, double *total_ms) {
+  if (kernel < 0 || kernel >= MGK_COUNT || !launches || !total_ms) return MG_ERR_INVALID_ARG;
+  std::lock_guard<std::mutex> lk(g_mu);
+  int cnt = 0;
+  double ms = 0.0;
+  for (int i = 0; i < g_prof.used; ++i) {
+    if (g_prof.kid[i] != kernel) continue;
+    if (cudaEventSynchronize(g_prof.ev[2 * i + 1]) != cudaSuccess) return MG_ERR_CUDA;
+    float t = 0.f;
+    if (cudaEventElapsedTime(&t, g_prof.ev[2 * i], g_prof.ev[2 * i + 1]) != cudaSuccess)
+      return MG_ERR_CUDA;
+    ++cnt;
+    ms += t;
+  }
+  *launches = cnt;
+  *total_ms = ms;
+  return MG_OK;
+}
+
+int mg_attn_kernel_count(void) { return MGK_COUNT; }
+
+const char *mg_attn_kernel_name(int kernel) {
+  if (kernel < 0 || kernel >= MGK_COUNT) return "unknown";
+  return kKernelNames[kernel];
+}
+
+}  // extern "C"

@@ -1,0 +1,58 @@
+// internal.h -- host-side declarations shared by the library's translation
+// units (launchers of each kernel family). Not part of the public ABI.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <cuda_bf16.h>
+#include <stdint.h>
+
+struct MgProblem {
+  int B, H, L, D;
+  int causal;
+  float scale;
+};
+
+// Kernel ids, in the order mg_attn_kernel_name() reports them.
+enum MgKernelId {
+  MGK_STRICT_FWD = 0,
+  MGK_STRICT_DVEC = 1,
+  MGK_STRICT_DKDV = 2,
+  MGK_ACCEL_FWD = 3,
+  MGK_ACCEL_DVEC = 4,
+  MGK_ACCEL_DKDV = 5,
+  MGK_DQ_ZERO = 6,
+  MGK_COUNT = 7
+};
+
+// Device error codes written into the device error word by bounded waits.
+enum MgDeviceError : unsigned int {
+  MG_DEVERR_NONE = 0,
+  MG_DEVERR_TIMEOUT = 1
+};
+
+// STRICT_F32 (FFMA) kernels.
+cudaError_t mg_launch_strict_fwd(const float *Q, const float *K, const float *V, float *O,
+                                 float *LSE, const MgProblem &p, cudaStream_t st);
+cudaError_t mg_launch_strict_dkdv(const float *Q, const float *K, const float *V,
+                                  const float *dO, const float *LSE, const float *Dvec,
+                                  float *dQ, float *dK, float *dV, const MgProblem &p,
+                                  cudaStream_t st);
+
+// Dvec = rowsum(dO * O), dO in f32 or bf16.
+cudaError_t mg_launch_dvec_f32(const float *O, const float *dO, float *Dvec, const MgProblem &p,
+                               cudaStream_t st);
+cudaError_t mg_launch_dvec_bf16(const float *O, const __nv_bfloat16 *dO, float *Dvec,
+                                const MgProblem &p, cudaStream_t st);
+
+// ACCEL_BF16 (tcgen05 / TMEM / TMA) kernels. `err` is the device error word.
+cudaError_t mg_launch_accel_fwd(const __nv_bfloat16 *Q, const __nv_bfloat16 *K,
+                                const __nv_bfloat16 *V, float *O, float *LSE,
+                                const MgProblem &p, unsigned int *err, cudaStream_t st);
+cudaError_t mg_launch_accel_dkdv(const __nv_bfloat16 *Q, const __nv_bfloat16 *K,
+                                 const __nv_bfloat16 *V, const __nv_bfloat16 *dO,
+                                 const float *LSE, const float *Dvec, float *dQ, float *dK,
+                                 float *dV, const MgProblem &p, unsigned int *err,
+                                 cudaStream_t st);
+
+// Opt a kernel into more than 48 KB of dynamic shared memory once per device.
+cudaError_t mg_set_smem_attr(const void *func, int bytes, int slot);

@@ -1,0 +1,447 @@
+#!/usr/bin/env python3
+"""Attention forward + backward throughput on GB300 through libmgattn's C ABI.
+
+One step = mg_attn_fwd + mg_attn_bwd (Dvec pre-pass, dQ zeroing, fused dK+dV
+kernel with its dQ reductions) over one batch of the seeded long-sequence
+workload: B=2, H=32, L=8192, D=128, causal, scale = 1/sqrt(D).
+
+Throughput counts 4 B H L^2 D flops for the forward and 2.5x that for the
+backward, halved for causal attention. The headline value is the ACCEL_BF16
+(tcgen05) fwd+bwd TFLOP/s; the STRICT_F32 (FFMA) path is measured on the same
+workload and reported in the same line under "contracts".
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+                  [--contract both|accel|strict] [--cfg 5]
+
+Under torchrun (N > 1) every rank runs the same per-GPU workload on its own
+GPU (heads are independent, there is no exchange: weak scaling); the timed
+region is bracketed by a barrier and a synchronize and rank 0 reports the
+maximum over ranks. ``--impl reference`` times the fp64 CPU oracle on a bounded
+sample of the same workload on the host cores (rank 0 only).
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import numpy as np  # noqa: E402
+
+from attention_forward_backward_gb300 import synth  # noqa: E402
+
+METRIC = "attention fwd+bwd TFLOP/s on 1 GB300 (strict f32 & bf16) and % of peak"
+UNIT = "TFLOP/s"
+L2_FLUSH_BYTES = 512 << 20  # > 129 MB L2
+
+# dram__bytes_read.sum + dram__bytes_write.sum per launch of the dominant
+# kernel, from the ncu capture summarised in profiles/ (None once the kernel
+# changed since the capture).
+NCU_TRAFFIC_BYTES = {}
+
+
+def parse():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=10)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--contract", choices=["both", "accel", "strict"], default="both")
+    ap.add_argument("--cfg", type=int, default=5)
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-seconds", type=float, default=15.0,
+                    help="target CPU seconds for the oracle sample")
+    return ap.parse_args()
+
+
+def load_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            d = json.load(f)
+        return {"bf16_tflops": d.get("bf16_tflops", 1900.0),
+                "bf16_tflops_sustained": d.get("bf16_tflops_sustained", 1700.0),
+                "hbm_gbs": d.get("hbm_gbs", 6800.0),
+                "sm_max_mhz": d.get("sm_max_mhz", 2070.0), "source": "measured"}
+    return {"bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0, "hbm_gbs": 6800.0,
+            "sm_max_mhz": 2070.0, "source": "fallback"}
+
+
+def fp32_simt_peak_tflops(sm_count: int, mhz: float) -> float:
+    """FP32 CUDA-core peak: SMs x 128 FP32 lanes x 2 flops (FFMA) x clock."""
+    return sm_count * 128 * 2 * mhz * 1e6 / 1e12
+
+
+# ------------------------------------------------------------------ clocks
+class ClockSampler:
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.idx = gpu_index
+        self.proc = None
+        self.path = os.path.join("/tmp", f"mg_clocks_{os.getpid()}.csv")
+
+    def start(self):
+        try:
+            self.f = open(self.path, "w")
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.idx), f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "200"],
+                stdout=self.f, stderr=subprocess.DEVNULL)
+        except Exception:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        self.f.close()
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        with open(self.path) as f:
+            for line in f:
+                parts = [p.strip() for p in line.split(",")]
+                if len(parts) < 9:
+                    continue
+                try:
+                    sm.append(float(parts[1]))
+                    mx.append(float(parts[2]))
+                except ValueError:
+                    continue
+                for n, v in zip(names, parts[5:9]):
+                    if v.lower() == "active":
+                        reasons.add(n)
+        os.unlink(self.path)
+        if not sm:
+            return None
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx),
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+# ------------------------------------------------------------------ ours
+def make_inputs(w, contract, torch, device):
+    host = {}
+    dev = {}
+    for t in ("Q", "K", "V", "dO"):
+        x = synth.tensor_f32(w, t)
+        if contract == "strict":
+            h = torch.from_numpy(x)
+        else:
+            bits = synth.round_to_bf16(x).view(np.int16)
+            h = torch.from_numpy(bits).view(torch.bfloat16)
+        host[t] = h.pin_memory()
+        dev[t] = host[t].to(device, non_blocking=False)
+    return host, dev
+
+
+def run_contract(mg, torch, w, contract, args, device, stream, peaks, sm_count, clocks):
+    host, dev = make_inputs(w, contract, torch, device)
+    B, H, L, D = w.shape
+    f32 = torch.float32
+    O = torch.empty((B, H, L, D), dtype=f32, device=device)
+    LSE = torch.empty((B, H, L), dtype=f32, device=device)
+    dQ, dK, dV = (torch.empty_like(O) for _ in range(3))
+    ws = torch.empty(mg.mg_attn_bwd_workspace_bytes(B, H, L, D, contract), dtype=torch.uint8,
+                     device=device)
+    flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=f32, device=device)
+    s = stream.cuda_stream
+
+    def step():
+        mg.mg_attn_fwd(dev["Q"], dev["K"], dev["V"], O, LSE, w.causal, w.scale, contract, s)
+        mg.mg_attn_bwd(dev["Q"], dev["K"], dev["V"], O, dev["dO"], LSE, dQ, dK, dV, w.causal,
+                       w.scale, contract, ws, s)
+
+    with torch.cuda.stream(stream):
+        for _ in range(args.warmup):
+            step()
+        torch.cuda.synchronize()
+        if mg.mg_get_device_error(s) != mg.MG_OK:
+            raise RuntimeError(f"{contract}: device error word set during warm-up")
+
+        ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True),
+               torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
+        mg.mg_attn_profile_enable(True, 16 * args.steps + 64)
+        barrier()
+        torch.cuda.synchronize()
+        if clocks is not None:
+            clocks.start()
+        for i in range(args.steps):
+            flush.fill_(float(i))  # evict L2 between timed steps (outside the events)
+            a, b, c = ev[i]
+            a.record(stream)
+            mg.mg_attn_fwd(dev["Q"], dev["K"], dev["V"], O, LSE, w.causal, w.scale, contract, s)
+            b.record(stream)
+            mg.mg_attn_bwd(dev["Q"], dev["K"], dev["V"], O, dev["dO"], LSE, dQ, dK, dV,
+                           w.causal, w.scale, contract, ws, s)
+            c.record(stream)
+        torch.cuda.synchronize()
+        barrier()
+        clk = clocks.stop() if clocks is not None else None
+        if mg.mg_get_device_error(s) != mg.MG_OK:
+            raise RuntimeError(f"{contract}: device error word set during the timed region")
+        fwd_ms = [a.elapsed_time(b) for a, b, _ in ev]
+        tot_ms = [a.elapsed_time(c) for a, _, c in ev]
+        per_kernel = {}
+        for k in range(mg.mg_attn_kernel_count()):
+            n, ms = mg.mg_attn_profile_read(k)
+            if n:
+                per_kernel[mg.mg_attn_kernel_name(k)] = {"launches": n, "avg_ms": ms / n}
+        mg.mg_attn_profile_enable(False)
+
+    total_ms = max_over_ranks(sum(tot_ms))
+    fwd_total_ms = max_over_ranks(sum(fwd_ms))
+    ws_n = world()
+    flops_step = w.flops_fwd() + w.flops_bwd()
+    res = {
+        "fwd_bwd_tflops": ws_n * flops_step * args.steps / (total_ms * 1e-3) / 1e12,
+        "fwd_tflops": ws_n * w.flops_fwd() * args.steps / (fwd_total_ms * 1e-3) / 1e12,
+        "ms_per_step": total_ms / args.steps,
+        "fwd_ms_median": statistics.median(fwd_ms),
+        "step_ms_median": statistics.median(tot_ms),
+        "step_ms_iqr": (float(np.percentile(tot_ms, 75) - np.percentile(tot_ms, 25))
+                        if len(tot_ms) > 1 else 0.0),
+        "step_ms_min": min(tot_ms), "step_ms_max": max(tot_ms),
+        "step_ms_raw": [round(x, 4) for x in tot_ms],
+        "kernels": per_kernel,
+        "clocks": clk,
+    }
+
+    # roofline of the dominant kernel (largest total time)
+    dom = max(per_kernel.items(), key=lambda kv: kv[1]["launches"] * kv[1]["avg_ms"])
+    name, st = dom
+    if name.endswith("fwd"):
+        alg = w.flops_fwd()
+    elif "dkdv" in name:
+        alg = w.flops_bwd()
+    else:
+        alg = None
+    if contract == "accel":
+        peak = peaks["bf16_tflops"]
+        bound, peak_note = "tensor", f"bf16 dense, {peaks['source']} (cuBLAS burst)"
+    else:
+        mhz = peaks["sm_max_mhz"]
+        peak = fp32_simt_peak_tflops(sm_count, mhz)
+        bound, peak_note = "alu", f"FP32 FFMA: {sm_count} SMs x 128 lanes x 2 x {mhz:.0f} MHz"
+    ach = alg / (st["avg_ms"] * 1e-3) / 1e12 if alg else None
+    res["roofline"] = {"bound": bound, "kernel": name, "achieved": ach, "peak": peak,
+                       "unit": "TFLOP/s", "frac": (ach / peak) if ach else None,
+                       "traffic": NCU_TRAFFIC_BYTES.get((name, w.cfg)),
+                       "peak_source": peak_note,
+                       "algorithmic_flops_per_launch": alg}
+    res["frac_of_peak_fwd_bwd"] = res["fwd_bwd_tflops"] / ws_n / peak
+    res["gpu_launches_per_step"] = 3  # fwd, Dvec, dK/dV/dQ (+ one cudaMemsetAsync of dQ)
+
+    if not args.no_e2e:
+        res["e2e"] = run_e2e(mg, torch, w, contract, args, host, device, stream, flops_step)
+    del flush
+    return res
+
+
+def run_e2e(mg, torch, w, contract, args, host, device, stream, flops_step):
+    """Same metric through the C ABI with host buffers: every step copies its
+    inputs from pinned host memory and reads every output back."""
+    B, H, L, D = w.shape
+    f32 = torch.float32
+    dev = {k: torch.empty_like(v, device=device) for k, v in host.items()}
+    O = torch.empty((B, H, L, D), dtype=f32, device=device)
+    LSE = torch.empty((B, H, L), dtype=f32, device=device)
+    dQ, dK, dV = (torch.empty_like(O) for _ in range(3))
+    ws = torch.empty(mg.mg_attn_bwd_workspace_bytes(B, H, L, D, contract), dtype=torch.uint8,
+                     device=device)
+    outs = {"O": O, "LSE": LSE, "dQ": dQ, "dK": dK, "dV": dV}
+    hout = {k: torch.empty(v.shape, dtype=v.dtype).pin_memory() for k, v in outs.items()}
+    s = stream.cuda_stream
+    h2d = sum(v.numel() * v.element_size() for v in host.values())
+    d2h = sum(v.numel() * v.element_size() for v in outs.values())
+
+    def step():
+        for k in host:
+            dev[k].copy_(host[k], non_blocking=True)
+        mg.mg_attn_fwd(dev["Q"], dev["K"], dev["V"], O, LSE, w.causal, w.scale, contract, s)
+        mg.mg_attn_bwd(dev["Q"], dev["K"], dev["V"], O, dev["dO"], LSE, dQ, dK, dV, w.causal,
+                       w.scale, contract, ws, s)
+        for k in outs:
+            hout[k].copy_(outs[k], non_blocking=True)
+
+    with torch.cuda.stream(stream):
+        for _ in range(args.warmup):
+            step()
+        torch.cuda.synchronize()
+        barrier()
+        a = torch.cuda.Event(enable_timing=True)
+        b = torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        for _ in range(args.steps):
+            step()
+        b.record(stream)
+        torch.cuda.synchronize()
+        barrier()
+    ms = max_over_ranks(a.elapsed_time(b))
+    return {"value": world() * flops_step * args.steps / (ms * 1e-3) / 1e12, "unit": UNIT,
+            "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+            "ms_per_step": ms / args.steps}
+
+
+# ------------------------------------------------------------------ distributed
+_DIST = {"on": False}
+
+
+def world() -> int:
+    return int(os.environ.get("WORLD_SIZE", "1"))
+
+
+def rank() -> int:
+    return int(os.environ.get("RANK", "0"))
+
+
+def barrier():
+    if _DIST["on"]:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def max_over_ranks(x: float) -> float:
+    if not _DIST["on"]:
+        return x
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([x], dtype=torch.float64, device="cuda")
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+# ------------------------------------------------------------------ oracle (CPU)
+def oracle_sample(w, contract: str, target_s: float):
+    """Time the fp64 oracle (as it stands) on whole heads of the workload until
+    about ``target_s`` seconds of CPU work; returns (TFLOP/s, cores, sample)."""
+    import oracle
+    host = synth.inputs(w, contract)
+    vals = {k: (v if contract == "strict" else v["values"]).reshape(w.B * w.H, w.L, w.D)
+            for k, v in host.items()}
+    cores = oracle.max_threads()
+    per_head = (w.flops_fwd() + w.flops_bwd()) / (w.B * w.H)
+    heads, elapsed = 0, 0.0
+    while heads < w.B * w.H and (heads == 0 or elapsed < target_s):
+        h = heads
+        t0 = time.perf_counter()
+        oracle.attn_bwd(vals["Q"][h], vals["K"][h], vals["V"][h], vals["dO"][h], w.causal,
+                        w.scale)
+        elapsed += time.perf_counter() - t0
+        heads += 1
+    tflops = per_head * heads / elapsed / 1e12
+    sample = (f"{heads} of {w.B * w.H} heads of the workload (fwd+bwd per head, fp64, "
+              f"OpenMP over rows), {elapsed:.1f} s; throughput scaled per head")
+    return tflops, cores, sample, elapsed
+
+
+# ------------------------------------------------------------------ main
+def main():
+    args = parse()
+    w = synth.WORKLOADS[args.cfg]
+    if args.impl == "reference":
+        return main_reference(args, w)
+
+    import torch
+    import attention_forward_backward_gb300 as mg
+
+    if world() > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl")
+        _DIST["on"] = True
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    torch.cuda.set_device(local)
+    device = torch.device("cuda", local)
+    mg.load_library()
+    props = torch.cuda.get_device_properties(device)
+    sm_count = props.multi_processor_count
+    peaks = load_peaks()
+    stream = torch.cuda.Stream(device)
+
+    contracts = ["accel", "strict"] if args.contract == "both" else [args.contract]
+    results = {}
+    for c in contracts:
+        if c not in w.contracts:
+            continue
+        clocks = ClockSampler(local) if rank() == 0 else None
+        results[c] = run_contract(mg, torch, w, c, args, device, stream, peaks, sm_count, clocks)
+
+    head = "accel" if "accel" in results else "strict"
+    r = results[head]
+    line = {
+        "metric": METRIC, "value": r["fwd_bwd_tflops"], "unit": UNIT, "n_gpus": world(),
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": r["ms_per_step"],
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "bf16" if head == "accel" else "f32", "data": "synthetic",
+        "impl": "ours",
+        "config": {"workload": w.name, "cfg": w.cfg, "B": w.B, "H": w.H, "L": w.L, "D": w.D,
+                   "causal": w.causal, "scale": "1/sqrt(D)",
+                   "contract": "ACCEL_BF16" if head == "accel" else "STRICT_F32",
+                   "flops_convention": "fwd 4BHL^2D, bwd 2.5x fwd, causal x1/2",
+                   "l2": "flushed between timed steps (512 MiB write outside the events)",
+                   "parallelism": f"replica per GPU x{world()} (heads independent)"},
+        "roofline": r["roofline"],
+        "clocks": r["clocks"],
+        "e2e": r.get("e2e"),
+        "gpu_launches": r["gpu_launches_per_step"] * args.steps,
+        "contracts": {},
+    }
+    for c, rr in results.items():
+        key = "accel_bf16" if c == "accel" else "strict_f32"
+        line["contracts"][key] = {k: rr[k] for k in (
+            "fwd_bwd_tflops", "fwd_tflops", "frac_of_peak_fwd_bwd", "ms_per_step",
+            "fwd_ms_median", "step_ms_median", "step_ms_iqr", "step_ms_min", "step_ms_max",
+            "step_ms_raw", "kernels", "roofline", "clocks")}
+        if "e2e" in rr:
+            line["contracts"][key]["e2e"] = rr["e2e"]
+    if rank() == 0 and not args.no_cpu_baseline and world() == 1:
+        tf, cores, sample, _ = oracle_sample(w, head, args.cpu_seconds)
+        line["cpu_baseline"] = {"value": tf, "unit": UNIT, "cores": cores, "kind": "oracle",
+                                "sample": sample}
+    if rank() == 0:
+        print(json.dumps(line))
+    if _DIST["on"]:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+def main_reference(args, w):
+    """The oracle as the reference arm: CPU fp64, rank 0 only."""
+    if rank() != 0:
+        return
+    contract = "accel" if args.contract in ("both", "accel") else "strict"
+    per_step_s = max(1.0, min(args.cpu_seconds, 120.0 / max(1, args.steps + args.warmup)))
+    vals = []
+    sample = ""
+    cores = 0
+    for i in range(args.warmup + args.steps):
+        tf, cores, sample, _ = oracle_sample(w, contract, per_step_s)
+        if i >= args.warmup:
+            vals.append(tf)
+    v = statistics.median(vals)
+    line = {"metric": METRIC, "value": v, "unit": UNIT, "n_gpus": world(), "steps": args.steps,
+            "warmup": args.warmup, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "f64", "data": "synthetic", "impl": "reference",
+            "config": {"workload": w.name, "cfg": w.cfg, "B": w.B, "H": w.H, "L": w.L,
+                       "D": w.D, "causal": w.causal,
+                       "contract": "ACCEL_BF16 inputs" if contract == "accel" else "STRICT_F32 inputs"},
+            "cpu_baseline": {"value": v, "unit": UNIT, "cores": cores, "kind": "oracle",
+                             "sample": sample},
+            "e2e": {"value": v, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line))
+
+
+if __name__ == "__main__":
+    main()

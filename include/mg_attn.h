@@ -1,0 +1,139 @@
+/*
+ * mg_attn.h -- C ABI of libmgattn.so: multi-head scaled-dot-product attention,
+ * forward and backward, as one training step on one GB300 GPU (sm_103a).
+ *
+ * The operation. "Meganeura: Portable GPU Training and Inference through Vulkan
+ * and Metal" treats attention as one graph node with its own derivative rule
+ * (Section 3.1) and lowers it to three kernel archetypes: tiled attention
+ * forward, dQ, and fused dK+dV (Section 3.3; Section 8 makes the fused dK+dV
+ * kernel an invariant). The pages print no formula; the functions below compute
+ * the textbook definition, per (batch b, head h):
+ *
+ *   s_ij = scale * Q_i . K_j,  allowed(i,j) = (j <= i) when causal (top-left)
+ *   LSE_i = ln sum_{allowed j} exp(s_ij)          (natural log, scaled logits)
+ *   P_ij = exp(s_ij - LSE_i) on allowed pairs, else 0;   O_i = sum_j P_ij V_j
+ *   Dvec_i = dO_i . O_i;  dS_ij = P_ij (dO_i . V_j - Dvec_i)
+ *   dV_j = sum_i P_ij dO_i;  dQ_i = scale sum_j dS_ij K_j;  dK_j = scale sum_i dS_ij Q_i
+ *
+ * No L x L matrix is ever stored: the kernels tile the key axis and keep a
+ * running max and sum (forward) or recompute P from LSE (backward).
+ *
+ * Arithmetic contracts (Section 4.2 separates a strict-f32 contract from an
+ * accelerated one whose forward inputs are rounded to a 16-bit format with f32
+ * accumulation and f32 stores; Section 10: strict governs permissions, not the
+ * order of operations):
+ *   MG_CONTRACT_STRICT_F32  every tensor f32; FP32 CUDA cores only (FFMA, no
+ *                           TF32, no tensor cores). Results are not bitwise
+ *                           reproducible across runs (dQ uses f32 atomics).
+ *   MG_CONTRACT_ACCEL_BF16  Q, K, V, dO are bf16; O, dQ, dK, dV are f32; LSE f32.
+ *                           Products run on tcgen05 tensor cores with f32
+ *                           accumulation in tensor memory; P (forward and dV)
+ *                           and dS (dK, dQ) are rounded to bf16 (RNE) as MMA
+ *                           operands, everything else stays f32.
+ *
+ * Layout. Q, K, V, O, dO, dQ, dK, dV are dense row-major [B][H][L][D] (D
+ * innermost, no padding, no strides). LSE (and the workspace's Dvec) are
+ * [B][H][L] f32. Lq = Lk = L.
+ *
+ * Ownership. The caller owns every buffer (device memory, e.g. from PyTorch).
+ * The library never allocates or frees device memory on these calls; the
+ * backward's scratch is the caller-provided workspace. All compute calls are
+ * asynchronous on `stream` (a cudaStream_t; NULL is the legacy default stream)
+ * and return after the launches are queued.
+ *
+ * Errors. Every call returns an mg_status_t synchronously. Argument errors are
+ * detected on the host before anything is launched (nothing is written).
+ * A failed launch is MG_ERR_CUDA. A kernel that gives up on a bounded wait sets
+ * a device error word; mg_get_device_error() reports it as MG_ERR_TIMEOUT.
+ * Nothing aborts the process.
+ *
+ * Preconditions checked: pointers non-NULL and 16-byte aligned; B, H, L >= 1;
+ * B*H <= 2^24, L <= 2^20; D in {32, 64, 128} (else MG_ERR_UNSUPPORTED);
+ * causal in {0, 1}; scale finite and > 0; contract valid; no output buffer
+ * overlaps an input buffer or another output.
+ */
+#ifndef MG_ATTN_H
+#define MG_ATTN_H
+
+#include <stddef.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  MG_CONTRACT_STRICT_F32 = 0,
+  MG_CONTRACT_ACCEL_BF16 = 1
+} mg_contract_t;
+
+typedef enum {
+  MG_OK = 0,
+  MG_ERR_INVALID_ARG = 1, /* null/misaligned pointer, bad size, aliasing, bad scale */
+  MG_ERR_UNSUPPORTED = 2, /* D not in {32,64,128} */
+  MG_ERR_WORKSPACE = 3,   /* workspace missing or smaller than the query says */
+  MG_ERR_CUDA = 4,        /* a CUDA runtime call or launch failed */
+  MG_ERR_TIMEOUT = 5      /* a kernel gave up on a bounded wait (device error word) */
+} mg_status_t;
+
+/*
+ * Forward: O = softmax(scale * Q K^T + causal mask) V and LSE (natural log).
+ * Tiled attention forward archetype (Section 3.3 of the paper).
+ *   Q, K, V  in   [B][H][L][D]; f32 (STRICT) or bf16 (ACCEL)
+ *   O        out  [B][H][L][D] f32 (both contracts), overwritten
+ *   LSE      out  [B][H][L] f32, overwritten; the backward requires it
+ */
+int mg_attn_fwd(const void *Q, const void *K, const void *V, void *O, float *LSE,
+                int B, int H, int L, int D, int causal, float scale, int contract,
+                void *stream);
+
+/* Bytes of device workspace mg_attn_bwd needs for this shape (holds Dvec,
+ * [B][H][L] f32, rounded up to 256 bytes). 0 for invalid arguments. */
+size_t mg_attn_bwd_workspace_bytes(int B, int H, int L, int D, int contract);
+
+/*
+ * Backward: dQ, dK, dV of loss = sum(dO * O), given the forward's O and LSE.
+ * dQ and fused dK+dV archetypes (Sections 3.3 and 8 of the paper); the
+ * derivative region keeps f32 accumulation (Sections 3.1 and 4.2).
+ *   Q, K, V, dO  in   [B][H][L][D]; f32 (STRICT) or bf16 (ACCEL)
+ *   O            in   [B][H][L][D] f32, as written by mg_attn_fwd
+ *   LSE          in   [B][H][L] f32, as written by mg_attn_fwd
+ *   dQ, dK, dV   out  [B][H][L][D] f32, overwritten (never accumulated into)
+ *   workspace    scratch of at least mg_attn_bwd_workspace_bytes() bytes,
+ *                16-byte aligned; its contents on entry do not matter
+ * Steps on the stream: Dvec = rowsum(dO * O); dQ zeroed; one kernel per key
+ * block recomputes P from Q, K, LSE and accumulates dK, dV in place while
+ * adding its dQ contribution with f32 reductions.
+ */
+int mg_attn_bwd(const void *Q, const void *K, const void *V, const void *O,
+                const void *dO, const float *LSE, void *dQ, void *dK, void *dV,
+                int B, int H, int L, int D, int causal, float scale, int contract,
+                void *workspace, size_t workspace_bytes, void *stream);
+
+/* Static, human-readable name of a status code. Never NULL. */
+const char *mg_status_string(int status);
+
+/* Synchronises `stream`, then reads and clears the current device's error word.
+ * MG_OK if no kernel has reported a give-up since the last call, MG_ERR_TIMEOUT
+ * if one has, MG_ERR_CUDA if the synchronisation itself failed. */
+int mg_get_device_error(void *stream);
+
+/*
+ * Kernel timing for benchmarks. While enabled, every kernel launch made by the
+ * calls above is bracketed by two CUDA events recorded on the call's stream.
+ * mg_attn_profile_enable(1) (re)creates the event pool (capacity launches) and
+ * zeroes the counters; (0) stops recording and frees the events. These are the
+ * only entry points that create CUDA objects.
+ * mg_attn_profile_read() synchronises on the recorded events and returns, for
+ * kernel id `kernel` (0 <= kernel < mg_attn_kernel_count()), the number of
+ * recorded launches and their summed device time in milliseconds.
+ */
+int mg_attn_profile_enable(int enable, int capacity);
+int mg_attn_profile_read(int kernel, int *launches, double *total_ms);
+int mg_attn_kernel_count(void);
+const char *mg_attn_kernel_name(int kernel);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* MG_ATTN_H */

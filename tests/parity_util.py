@@ -1,0 +1,89 @@
+"""Shared helpers of the parity tests: run the CUDA path through the C ABI on
+seeded inputs and compare element by element with the fp64 oracle.
+
+Error metric (per output tensor X in O, dQ, dK, dV):
+    err(X) = max |X_gpu - X_ref| / max |X_ref|
+Gates: STRICT_F32 <= 1e-4, ACCEL_BF16 <= 2e-2. LSE is compared by
+max |LSE_gpu - LSE_ref| / max(1, max |LSE_ref|) with the same gates.
+"""
+from __future__ import annotations
+
+import numpy as np
+
+import attention_forward_backward_gb300 as mg
+from attention_forward_backward_gb300 import synth
+
+TOL = {"strict": 1e-4, "accel": 2e-2}
+
+
+def rel_err(got, ref) -> float:
+    got = np.asarray(got, dtype=np.float64)
+    ref = np.asarray(ref, dtype=np.float64)
+    denom = float(np.max(np.abs(ref))) if ref.size else 1.0
+    if not np.all(np.isfinite(got)):
+        return float("inf")
+    return float(np.max(np.abs(got - ref))) / max(denom, 1e-30) if ref.size else 0.0
+
+
+def lse_err(got, ref) -> float:
+    got = np.asarray(got, dtype=np.float64)
+    ref = np.asarray(ref, dtype=np.float64)
+    if not np.all(np.isfinite(got)):
+        return float("inf")
+    return float(np.max(np.abs(got - ref))) / max(1.0, float(np.max(np.abs(ref))))
+
+
+def device_inputs(host: dict, contract: str, device="cuda"):
+    """Torch device tensors for the CUDA path and the f64-exact values the
+    oracle consumes (bf16 values for ACCEL, f32 values for STRICT)."""
+    import torch
+    dev, vals = {}, {}
+    for k, x in host.items():
+        if contract == "strict":
+            dev[k] = torch.from_numpy(x).to(device)
+            vals[k] = x
+        else:
+            bits = np.ascontiguousarray(x["bits"]).view(np.int16)
+            dev[k] = torch.from_numpy(bits).view(torch.bfloat16).to(device)
+            vals[k] = x["values"]
+    return dev, vals
+
+
+def run_gpu(dev: dict, causal: bool, scale: float, contract: str, bwd: bool = True,
+            poison: bool = True):
+    """Forward (+ backward) through the C ABI. Output buffers start as NaN so
+    that an element the kernels fail to write shows up as an error."""
+    import torch
+    Q, K, V, dO = dev["Q"], dev["K"], dev["V"], dev["dO"]
+    B, H, L, D = Q.shape
+    O = torch.full((B, H, L, D), float("nan") if poison else 0.0, device=Q.device)
+    LSE = torch.full((B, H, L), float("nan") if poison else 0.0, device=Q.device)
+    mg.mg_attn_fwd(Q, K, V, O, LSE, causal, scale, contract)
+    out = {"O": O, "LSE": LSE}
+    if bwd:
+        dQ = torch.full_like(O, float("nan") if poison else 0.0)
+        dK = torch.full_like(O, float("nan") if poison else 0.0)
+        dV = torch.full_like(O, float("nan") if poison else 0.0)
+        nbytes = mg.mg_attn_bwd_workspace_bytes(B, H, L, D, contract)
+        ws = torch.full((nbytes // 4,), float("nan"), device=Q.device)
+        mg.mg_attn_bwd(Q, K, V, O, dO, LSE, dQ, dK, dV, causal, scale, contract, ws)
+        out.update(dQ=dQ, dK=dK, dV=dV)
+    torch.cuda.synchronize()
+    assert mg.mg_get_device_error() == mg.MG_OK
+    return {k: v.cpu().numpy() for k, v in out.items()}
+
+
+def compare(got: dict, ref: dict, contract: str, keys=("O", "dQ", "dK", "dV")):
+    tol = TOL[contract]
+    errs = {}
+    for k in keys:
+        if k in got:
+            errs[k] = rel_err(got[k], ref[k])
+    if "LSE" in got and "LSE" in ref:
+        errs["LSE"] = lse_err(got["LSE"], ref["LSE"])
+    bad = {k: e for k, e in errs.items() if not (e <= tol)}
+    return errs, bad
+
+
+def workload_inputs(w: synth.Workload, contract: str):
+    return synth.inputs(w, contract)

@@ -1,0 +1,142 @@
+"""The C ABI without a GPU: the library builds and loads, exports every function
+include/mg_attn.h declares, and rejects bad arguments on the host before any
+CUDA call (the fake pointers below are never dereferenced)."""
+import ctypes
+import os
+import re
+
+import pytest
+
+import attention_forward_backward_gb300 as mg
+from attention_forward_backward_gb300 import build as mgbuild
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "mg_attn.h")
+
+
+@pytest.fixture(scope="module")
+def lib():
+    mgbuild.build()
+    return mg.load_library()
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    names = re.findall(r"\b(mg_[a-z0-9_]+)\s*\(", text)
+    return sorted(set(names))
+
+
+def test_header_declares_the_abi():
+    names = declared_functions()
+    for n in ("mg_attn_fwd", "mg_attn_bwd", "mg_attn_bwd_workspace_bytes", "mg_status_string",
+              "mg_get_device_error"):
+        assert n in names
+
+
+def test_library_exports_every_declared_symbol(lib):
+    raw = ctypes.CDLL(mg.LIB_PATH)
+    for name in declared_functions():
+        assert hasattr(raw, name), name
+
+
+# Fake, 16-byte aligned, distinct, non-overlapping "device" addresses.
+BASE = 1 << 40
+STEP = 1 << 36
+
+
+def P(i):
+    return BASE + i * STEP
+
+
+def fwd(lib, Q=P(0), K=P(1), V=P(2), O=P(3), LSE=P(4), B=1, H=2, L=64, D=64, causal=1,
+        scale=0.125, contract=0):
+    return lib.mg_attn_fwd(Q, K, V, O, LSE, B, H, L, D, causal, scale, contract, None)
+
+
+def bwd(lib, Q=P(0), K=P(1), V=P(2), O=P(3), dO=P(4), LSE=P(5), dQ=P(6), dK=P(7), dV=P(8),
+        B=1, H=2, L=64, D=64, causal=1, scale=0.125, contract=0, ws=P(9), ws_bytes=1 << 20):
+    return lib.mg_attn_bwd(Q, K, V, O, dO, LSE, dQ, dK, dV, B, H, L, D, causal, scale, contract,
+                           ws, ws_bytes, None)
+
+
+@pytest.mark.parametrize("kw,code", [
+    (dict(Q=None), mg.MG_ERR_INVALID_ARG),
+    (dict(O=None), mg.MG_ERR_INVALID_ARG),
+    (dict(LSE=None), mg.MG_ERR_INVALID_ARG),
+    (dict(K=P(1) + 4), mg.MG_ERR_INVALID_ARG),      # misaligned
+    (dict(B=0), mg.MG_ERR_INVALID_ARG),
+    (dict(H=-1), mg.MG_ERR_INVALID_ARG),
+    (dict(L=0), mg.MG_ERR_INVALID_ARG),
+    (dict(L=(1 << 20) + 1), mg.MG_ERR_INVALID_ARG),
+    (dict(D=48), mg.MG_ERR_UNSUPPORTED),
+    (dict(D=256), mg.MG_ERR_UNSUPPORTED),
+    (dict(causal=2), mg.MG_ERR_INVALID_ARG),
+    (dict(scale=0.0), mg.MG_ERR_INVALID_ARG),
+    (dict(scale=-1.0), mg.MG_ERR_INVALID_ARG),
+    (dict(scale=float("nan")), mg.MG_ERR_INVALID_ARG),
+    (dict(scale=float("inf")), mg.MG_ERR_INVALID_ARG),
+    (dict(contract=2), mg.MG_ERR_INVALID_ARG),
+    (dict(O=P(0)), mg.MG_ERR_INVALID_ARG),          # output aliases Q
+    (dict(LSE=P(3) + 1024), mg.MG_ERR_INVALID_ARG),  # LSE inside O
+])
+def test_fwd_rejects(lib, kw, code):
+    assert fwd(lib, **kw) == code
+
+
+@pytest.mark.parametrize("kw,code", [
+    (dict(dO=None), mg.MG_ERR_INVALID_ARG),
+    (dict(dV=P(8) + 8), mg.MG_ERR_INVALID_ARG),
+    (dict(D=16), mg.MG_ERR_UNSUPPORTED),
+    (dict(ws=None), mg.MG_ERR_WORKSPACE),
+    (dict(ws_bytes=16), mg.MG_ERR_WORKSPACE),
+    (dict(ws=P(9) + 4), mg.MG_ERR_WORKSPACE),
+    (dict(dQ=P(0)), mg.MG_ERR_INVALID_ARG),          # dQ aliases Q
+    (dict(dK=P(6)), mg.MG_ERR_INVALID_ARG),          # dK aliases dQ
+    (dict(ws=P(8)), mg.MG_ERR_INVALID_ARG),          # workspace aliases dV
+    (dict(contract=1, ws=P(4)), mg.MG_ERR_INVALID_ARG),  # workspace aliases dO
+])
+def test_bwd_rejects(lib, kw, code):
+    assert bwd(lib, **kw) == code
+
+
+def test_workspace_bytes(lib):
+    for contract in (0, 1):
+        n = lib.mg_attn_bwd_workspace_bytes(2, 32, 8192, 128, contract)
+        assert n >= 2 * 32 * 8192 * 4 and n % 256 == 0
+        assert lib.mg_attn_bwd_workspace_bytes(1, 1, 1, 32, contract) == 256
+    assert lib.mg_attn_bwd_workspace_bytes(1, 1, 1, 48, 0) == 0
+    assert lib.mg_attn_bwd_workspace_bytes(0, 1, 1, 64, 0) == 0
+    assert lib.mg_attn_bwd_workspace_bytes(1, 1, 1, 64, 5) == 0
+
+
+def test_status_strings(lib):
+    for code in range(6):
+        s = lib.mg_status_string(code).decode()
+        assert s.startswith("MG_")
+    assert lib.mg_status_string(99).decode() == "unknown mg_status_t"
+
+
+def test_kernel_names(lib):
+    n = lib.mg_attn_kernel_count()
+    names = [lib.mg_attn_kernel_name(i).decode() for i in range(n)]
+    assert len(set(names)) == n and "accel_dkdv_dq" in names and "strict_fwd" in names
+    assert lib.mg_attn_kernel_name(n).decode() == "unknown"
+
+
+def test_binding_raises_on_error(lib):
+    class FakeT:
+        def __init__(self, p, shape):
+            self.p, self.shape = p, shape
+
+        def dim(self):
+            return len(self.shape)
+
+        def data_ptr(self):
+            return self.p
+
+    q = FakeT(P(0), (1, 2, 8, 48))
+    with pytest.raises(mg.MgError) as ei:
+        mg.mg_attn_fwd(q, FakeT(P(1), q.shape), FakeT(P(2), q.shape), FakeT(P(3), q.shape),
+                       FakeT(P(4), q.shape[:3]), True, 0.1, "strict", stream=0)
+    assert ei.value.status == mg.MG_ERR_UNSUPPORTED

@@ -1,0 +1,100 @@
+"""STRICT_F32 parity: the FFMA kernels against the fp64 oracle, element by
+element, through the C ABI (gate 1e-4, max-abs error over max-abs reference)."""
+import numpy as np
+import pytest
+
+import oracle
+from attention_forward_backward_gb300 import synth
+from parity_util import compare, device_inputs, run_gpu
+
+pytestmark = pytest.mark.gpu
+
+
+def _full_check(w: synth.Workload, contract="strict", bwd=True):
+    host = synth.inputs(w, contract)
+    dev, vals = device_inputs(host, contract)
+    got = run_gpu(dev, w.causal, w.scale, contract, bwd=bwd)
+    if bwd:
+        ref = oracle.attn_bwd(vals["Q"], vals["K"], vals["V"], vals["dO"], w.causal, w.scale)
+    else:
+        O, LSE = oracle.attn_fwd(vals["Q"], vals["K"], vals["V"], w.causal, w.scale)
+        ref = {"O": O, "LSE": LSE}
+    errs, bad = compare(got, ref, contract)
+    assert not bad, (w.name, errs)
+    return errs
+
+
+@pytest.mark.parametrize("cfg", [1, 2, 4])
+def test_strict_configs(cfg):
+    _full_check(synth.WORKLOADS[cfg])
+
+
+@pytest.mark.parametrize("D", [32, 64, 128])
+@pytest.mark.parametrize("L", [1, 7, 64, 65, 130, 197])
+@pytest.mark.parametrize("causal", [True, False])
+def test_strict_edge_shapes(D, L, causal):
+    """Sub-tile, exactly-one-tile and ragged sequence lengths for every head dim."""
+    _full_check(synth.custom_workload(1, 2, L, D, causal, seed_cfg=910 + D))
+
+
+def test_strict_large_logits_noncausal():
+    _full_check(synth.custom_workload(2, 3, 300, 64, False, seed_cfg=920, qk_gain=4.0))
+
+
+def test_strict_cfg5_sampled():
+    """Config 5 (B=2, H=32, L=8192, D=128, causal) in the launch configuration
+    the benchmark times: two heads are checked in full (forward and backward)
+    and every head on sampled query rows (O and LSE)."""
+    w = synth.WORKLOADS[5]
+    host = synth.inputs(w, "strict")
+    dev, vals = device_inputs(host, "strict")
+    got = run_gpu(dev, w.causal, w.scale, "strict", bwd=True)
+    BH = w.B * w.H
+    flat = {k: v.reshape(BH, w.L, -1) if v.ndim == 4 else v.reshape(BH, w.L)
+            for k, v in got.items()}
+    vflat = {k: v.reshape(BH, w.L, w.D) for k, v in vals.items()}
+    for h in (0, BH - 1):
+        ref = oracle.attn_bwd(vflat["Q"][h], vflat["K"][h], vflat["V"][h], vflat["dO"][h],
+                              True, w.scale)
+        sub = {k: flat[k][h] for k in ("O", "LSE", "dQ", "dK", "dV")}
+        errs, bad = compare(sub, ref, "strict")
+        assert not bad, (h, errs)
+    rows = np.array([0, 1, 127, 128, 4095, 8190, 8191])
+    for h in range(0, BH, 7):
+        O, LSE = oracle.attn_fwd_rows(vflat["Q"][h], vflat["K"][h], vflat["V"][h], rows, True,
+                                      w.scale)
+        errs, bad = compare({"O": flat["O"][h][rows], "LSE": flat["LSE"][h][rows]},
+                            {"O": O, "LSE": LSE}, "strict")
+        assert not bad, (h, errs)
+
+
+def test_strict_causal_first_row_exact():
+    """Row 0 attends only key 0, so O[0] must equal V[0] exactly."""
+    import torch
+    w = synth.custom_workload(2, 2, 77, 64, True, seed_cfg=930)
+    dev, vals = device_inputs(synth.inputs(w, "strict"), "strict")
+    got = run_gpu(dev, True, w.scale, "strict", bwd=False)
+    np.testing.assert_array_equal(got["O"][:, :, 0, :], vals["V"][:, :, 0, :])
+
+
+def test_strict_guard_bands_untouched():
+    """Outputs written exactly in bounds: a canary band after each output stays intact."""
+    import torch
+    import attention_forward_backward_gb300 as mg
+    w = synth.custom_workload(1, 3, 97, 64, True, seed_cfg=940)
+    dev, _ = device_inputs(synth.inputs(w, "strict"), "strict")
+    n = w.numel
+    pad = 4096
+    bufs = {k: torch.full((n + pad,), 12345.0, device="cuda") for k in ("O", "dQ", "dK", "dV")}
+    lse = torch.full((w.B * w.H * w.L + pad,), 12345.0, device="cuda")
+    view = {k: b[:n].view(w.shape) for k, b in bufs.items()}
+    lv = lse[: w.B * w.H * w.L].view(w.B, w.H, w.L)
+    mg.mg_attn_fwd(dev["Q"], dev["K"], dev["V"], view["O"], lv, True, w.scale, "strict")
+    ws = torch.empty(mg.mg_attn_bwd_workspace_bytes(*w.shape, "strict"), dtype=torch.uint8,
+                     device="cuda")
+    mg.mg_attn_bwd(dev["Q"], dev["K"], dev["V"], view["O"], dev["dO"], lv, view["dQ"],
+                   view["dK"], view["dV"], True, w.scale, "strict", ws)
+    torch.cuda.synchronize()
+    for k, b in bufs.items():
+        assert torch.all(b[n:] == 12345.0), k
+    assert torch.all(lse[w.B * w.H * w.L:] == 12345.0)
