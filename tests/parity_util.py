@@ -2,7 +2,11 @@
 seeded inputs and compare element by element with the fp64 oracle.
 
 Error metric (per output tensor X in O, dQ, dK, dV):
-    err(X) = max |X_gpu - X_ref| / max |X_ref|
+    err(X) = max |X_gpu - X_ref| / max(max |X_ref|, 1e-3 * M)
+where M is the largest max |Y_ref| over the outputs Y of the same call. The
+floor only matters where the exact result is identically zero (L = 1 gives
+dQ = dK = 0, which f32 reaches only up to rounding); everywhere else the
+denominator is max |X_ref|.
 Gates: STRICT_F32 <= 1e-4, ACCEL_BF16 <= 2e-2. LSE is compared by
 max |LSE_gpu - LSE_ref| / max(1, max |LSE_ref|) with the same gates.
 """
@@ -16,13 +20,15 @@ from attention_forward_backward_gb300 import synth
 TOL = {"strict": 1e-4, "accel": 2e-2}
 
 
-def rel_err(got, ref) -> float:
+def rel_err(got, ref, floor: float = 0.0) -> float:
     got = np.asarray(got, dtype=np.float64)
     ref = np.asarray(ref, dtype=np.float64)
-    denom = float(np.max(np.abs(ref))) if ref.size else 1.0
+    if not ref.size:
+        return 0.0
     if not np.all(np.isfinite(got)):
         return float("inf")
-    return float(np.max(np.abs(got - ref))) / max(denom, 1e-30) if ref.size else 0.0
+    denom = max(float(np.max(np.abs(ref))), floor, 1e-300)
+    return float(np.max(np.abs(got - ref))) / denom
 
 
 def lse_err(got, ref) -> float:
@@ -76,9 +82,10 @@ def run_gpu(dev: dict, causal: bool, scale: float, contract: str, bwd: bool = Tr
 def compare(got: dict, ref: dict, contract: str, keys=("O", "dQ", "dK", "dV")):
     tol = TOL[contract]
     errs = {}
-    for k in keys:
-        if k in got:
-            errs[k] = rel_err(got[k], ref[k])
+    present = [k for k in keys if k in got]
+    scale = max((float(np.max(np.abs(ref[k]))) for k in present if ref[k].size), default=0.0)
+    for k in present:
+        errs[k] = rel_err(got[k], ref[k], floor=1e-3 * scale)
     if "LSE" in got and "LSE" in ref:
         errs["LSE"] = lse_err(got["LSE"], ref["LSE"])
     bad = {k: e for k, e in errs.items() if not (e <= tol)}
