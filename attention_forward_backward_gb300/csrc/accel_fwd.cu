@@ -1,4 +1,371 @@
-// placeholder: replaced by the tcgen05 forward
+// accel_fwd.cu -- ACCEL_BF16 tiled attention forward on tcgen05 tensor cores.
+//
+// The tiled attention forward archetype of "Meganeura: Portable GPU Training
+// and Inference through Vulkan and Metal" (Section 3.3) under its accelerated
+// contract (Section 4.2: matrix inputs rounded to a 16-bit format, f32
+// accumulation, f32 stores). The pages' kernel is a WGSL cooperative-matrix
+// shader; this one is written for sm_103a:
+//
+// * One CTA owns two 128-row query tiles (A, B) of one (b, h) head and walks
+//   the key axis in 128-key tiles. Q, K, V arrive by TMA (128-byte swizzle) into
+//   shared memory: Q once, K and V through an NSTAGE ring.
+// * Warp 9 issues every MMA from one thread: S_q = Q_q K^T (f32 in TMEM,
+//   128 x 128) and O_q += P_q V with P taken straight from TMEM (bf16, written
+//   over the first 64 columns of S_q). Issue order S_A S_B PV_A S_A' PV_B S_B'
+//   ... lets one softmax warpgroup work while the tensor core serves the other.
+// * Warps 0-3 and 4-7 are the softmax warpgroups of tiles A and B: one thread
+//   per query row (its TMEM lane). Online softmax in base 2 with log2(e) folded
+//   into the scale. The running reference max only moves when a row max grows
+//   by more than 8 (a factor 256 in P); O in TMEM is then rescaled after the
+//   previous P V finished. Any reference max gives the same exact result once
+//   O is divided by the row sum taken against that same max.
+// * Warp 8 is the TMA producer.
+// Every wait is bounded (a few seconds); a wait that gives up sets the device
+// error word and the CTA leaves through the same teardown as a normal exit.
 #include "internal.h"
-cudaError_t mg_launch_accel_fwd(const __nv_bfloat16 *, const __nv_bfloat16 *, const __nv_bfloat16 *, float *, float *, const MgProblem &, unsigned int *, cudaStream_t) { return cudaErrorNotSupported; }
-cudaError_t mg_launch_accel_dkdv(const __nv_bfloat16 *, const __nv_bfloat16 *, const __nv_bfloat16 *, const __nv_bfloat16 *, const float *, const float *, float *, float *, float *, const MgProblem &, unsigned int *, cudaStream_t) { return cudaErrorNotSupported; }
+#include "tc_common.cuh"
+#include "tmap.h"
+
+namespace {
+
+using namespace mg_tc;
+
+template <int DP>
+struct FwdCfg {
+  static constexpr int BM = 128;  // query rows per tile (TMEM lanes)
+  static constexpr int NQ = 2;    // query tiles per CTA
+  static constexpr int BN = 128;  // keys per tile
+  static constexpr int NSTAGE = DP == 128 ? 2 : 3;
+  static constexpr int NCHUNK = DP / 64;  // 64-column boxes per row
+  static constexpr int Q_TILE = BM * DP * 2;
+  static constexpr int KV_TILE = BN * DP * 2;
+  static constexpr int BOX_Q = BM * 128;
+  static constexpr int BOX_KV = BN * 128;
+  static constexpr int OFF_Q = 0;
+  static constexpr int OFF_K = OFF_Q + NQ * Q_TILE;
+  static constexpr int OFF_V = OFF_K + NSTAGE * KV_TILE;
+  static constexpr int OFF_BAR = OFF_V + NSTAGE * KV_TILE;
+  // barriers
+  static constexpr int B_QFULL = 0;
+  static constexpr int B_KFULL = 1;
+  static constexpr int B_VFULL = B_KFULL + NSTAGE;
+  static constexpr int B_KVEMPTY = B_VFULL + NSTAGE;
+  static constexpr int B_SFULL = B_KVEMPTY + NSTAGE;
+  static constexpr int B_PREADY = B_SFULL + NQ;
+  static constexpr int B_ODONE = B_PREADY + NQ;
+  static constexpr int B_DRAIN = B_ODONE + NQ;
+  static constexpr int NBAR = B_DRAIN + 1;
+  static constexpr int OFF_MISC = OFF_BAR + NBAR * 8;
+  static constexpr int SMEM_BYTES = OFF_MISC + 16 + 1024;  // + slack to align the base
+  static constexpr int NTHREADS = 320;
+  static constexpr int TMEM_COLS = 512;
+  static constexpr int T_S = 0;     // S_q at q * 128
+  static constexpr int T_O = 256;   // O_q at 256 + q * DP
+  static_assert(T_O + NQ * DP <= TMEM_COLS, "TMEM column budget");
+  static_assert(SMEM_BYTES <= 227 * 1024, "shared memory budget");
+};
+
+__device__ __forceinline__ bool drain_wait(uint32_t bar, uint32_t parity, uint64_t limit_ns) {
+  // Teardown wait for our own copies / MMAs in flight; ignores the abort flag.
+  const uint64_t t0 = globaltimer();
+  while (!mbar_try_wait(bar, parity)) {
+    if (globaltimer() - t0 > limit_ns) return false;
+  }
+  return true;
+}
+
+template <int DP>
+__global__ void __launch_bounds__(320, 1)
+    accel_fwd_kernel(const __grid_constant__ CUtensorMap tmQ,
+                     const __grid_constant__ CUtensorMap tmK,
+                     const __grid_constant__ CUtensorMap tmV, float *__restrict__ O,
+                     float *__restrict__ LSE, int BH, int L, int D, int causal, float scale_log2,
+                     unsigned int *err, unsigned long long timeout_ns) {
+  using C = FwdCfg<DP>;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                              ~static_cast<uintptr_t>(1023));
+  const uint32_t sbase = smem_u32(smem);
+  const uint32_t bar0 = sbase + C::OFF_BAR;
+  auto bar = [&](int i) { return bar0 + 8u * static_cast<uint32_t>(i); };
+  uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + C::OFF_MISC);
+  volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + C::OFF_MISC + 4);
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int nqb = (L + 255) / 256;
+  const int qb = nqb - 1 - static_cast<int>(blockIdx.x / BH);
+  const int bh = static_cast<int>(blockIdx.x % BH);
+  const int q0 = qb * 256;
+  const int nkt = (L + C::BN - 1) / C::BN;
+  int nT[2];
+  nT[0] = causal ? min(nkt, (q0 + 128) / C::BN) : nkt;
+  nT[1] = causal ? min(nkt, (q0 + 256) / C::BN) : nkt;
+  const int nmax = nT[1];
+
+  if (warp == 0) {
+    tmem_alloc(smem_u32(tmem_slot), C::TMEM_COLS);
+    tmem_relinquish();
+  }
+  if (threadIdx.x == 256) {
+    for (int i = 0; i < C::NBAR; ++i) {
+      uint32_t cnt = 1;
+      if (i >= C::B_PREADY && i < C::B_PREADY + C::NQ) cnt = 128;
+      mbar_init(bar(i), cnt);
+    }
+    *abort_flag = 0;
+    fence_barrier_init();
+    tma_prefetch_desc(&tmQ);
+    tma_prefetch_desc(&tmK);
+    tma_prefetch_desc(&tmV);
+  }
+  fence_proxy_async_smem();
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+  const Abort ab{abort_flag, err, timeout_ns};
+
+  if (warp == 8) {
+    // ------------------------------------------------------------ TMA producer
+    if (lane == 0) {
+      int issued = 0;
+      mbar_arrive_expect_tx(bar(C::B_QFULL), C::NQ * C::Q_TILE);
+      for (int q = 0; q < C::NQ; ++q)
+        for (int c = 0; c < C::NCHUNK; ++c)
+          tma_load_3d(sbase + C::OFF_Q + q * C::Q_TILE + c * C::BOX_Q, &tmQ, c * 64,
+                      q0 + q * C::BM, bh, bar(C::B_QFULL));
+      for (int j = 0; j < nmax; ++j) {
+        const int s = j % C::NSTAGE;
+        if (j >= C::NSTAGE &&
+            !mbar_wait(bar(C::B_KVEMPTY + s), ((j / C::NSTAGE) - 1) & 1, ab))
+          break;
+        mbar_arrive_expect_tx(bar(C::B_KFULL + s), C::KV_TILE);
+        for (int c = 0; c < C::NCHUNK; ++c)
+          tma_load_3d(sbase + C::OFF_K + s * C::KV_TILE + c * C::BOX_KV, &tmK, c * 64,
+                      j * C::BN, bh, bar(C::B_KFULL + s));
+        mbar_arrive_expect_tx(bar(C::B_VFULL + s), C::KV_TILE);
+        for (int c = 0; c < C::NCHUNK; ++c)
+          tma_load_3d(sbase + C::OFF_V + s * C::KV_TILE + c * C::BOX_KV, &tmV, c * 64,
+                      j * C::BN, bh, bar(C::B_VFULL + s));
+        issued = j + 1;
+      }
+      // Wait for our own copies in flight before the CTA can exit.
+      drain_wait(bar(C::B_QFULL), 0, 2000000000ull);
+      for (int j = max(0, issued - C::NSTAGE); j < issued; ++j) {
+        const int s = j % C::NSTAGE;
+        drain_wait(bar(C::B_KFULL + s), (j / C::NSTAGE) & 1, 2000000000ull);
+        drain_wait(bar(C::B_VFULL + s), (j / C::NSTAGE) & 1, 2000000000ull);
+      }
+    }
+  } else if (warp == 9) {
+    // ------------------------------------------------------------ MMA issuer
+    if (lane == 0) {
+      constexpr uint32_t idS = idesc_bf16_f32(128, C::BN, false, false);
+      constexpr uint32_t idO = idesc_bf16_f32(128, DP, false, true);
+      bool ok = mbar_wait(bar(C::B_QFULL), 0, ab);
+      int kwaited = -1;
+      auto wait_k = [&](int j) -> bool {
+        if (kwaited >= j) return true;
+        kwaited = j;
+        return mbar_wait(bar(C::B_KFULL + j % C::NSTAGE), (j / C::NSTAGE) & 1, ab);
+      };
+      auto issue_S = [&](int q, int j) -> bool {
+        if (!wait_k(j)) return false;
+        tc_fence_after();
+        const uint32_t sq = sbase + C::OFF_Q + q * C::Q_TILE;
+        const uint32_t sk = sbase + C::OFF_K + (j % C::NSTAGE) * C::KV_TILE;
+#pragma unroll
+        for (int kk = 0; kk < DP / 16; ++kk) {
+          const uint32_t off = (kk >> 2) * C::BOX_Q + (kk & 3) * 32;
+          const uint32_t offk = (kk >> 2) * C::BOX_KV + (kk & 3) * 32;
+          mma_ss(tmem + C::T_S + q * 128, sdesc_sw128(sq + off, 0, 1024),
+                 sdesc_sw128(sk + offk, 0, 1024), idS, kk > 0 ? 1u : 0u);
+        }
+        mma_commit(bar(C::B_SFULL + q));
+        return true;
+      };
+      auto issue_PV = [&](int q, int j) -> bool {
+        if (!mbar_wait(bar(C::B_PREADY + q), j & 1, ab)) return false;
+        if (!mbar_wait(bar(C::B_VFULL + j % C::NSTAGE), (j / C::NSTAGE) & 1, ab)) return false;
+        tc_fence_after();
+        const uint32_t sv = sbase + C::OFF_V + (j % C::NSTAGE) * C::KV_TILE;
+#pragma unroll
+        for (int kk = 0; kk < C::BN / 16; ++kk) {
+          mma_ts(tmem + C::T_O + q * DP, tmem + C::T_S + q * 128 + kk * 8,
+                 sdesc_sw128(sv + kk * 2048, C::BOX_KV, 1024), idO,
+                 (j > 0 || kk > 0) ? 1u : 0u);
+        }
+        mma_commit(bar(C::B_ODONE + q));
+        return true;
+      };
+      if (ok) ok = issue_S(0, 0);
+      if (ok) ok = issue_S(1, 0);
+      for (int j = 0; ok && j < nmax; ++j) {
+        if (j < nT[0]) {
+          ok = issue_PV(0, j);
+          if (ok && j + 1 < nT[0]) ok = issue_S(0, j + 1);
+        }
+        if (ok) ok = issue_PV(1, j);
+        if (ok) mma_commit(bar(C::B_KVEMPTY + j % C::NSTAGE));
+        if (ok && j + 1 < nT[1]) ok = issue_S(1, j + 1);
+      }
+      // Drain every MMA this thread issued before TMEM and smem are released.
+      mma_commit(bar(C::B_DRAIN));
+      drain_wait(bar(C::B_DRAIN), 0, 2000000000ull);
+    }
+  } else {
+    // ------------------------------------------------------------ softmax warpgroups
+    const int q = warp >> 2;
+    const int rl = 32 * (warp & 3) + lane;  // row within the query tile = TMEM lane
+    const int qrow = q0 + q * C::BM + rl;
+    const uint32_t lane_off = static_cast<uint32_t>(32 * (warp & 3)) << 16;
+    const uint32_t tS = tmem + lane_off + C::T_S + q * 128;
+    const uint32_t tO = tmem + lane_off + C::T_O + q * DP;
+    const int n = nT[q];
+    float m_ref = -INFINITY, l = 0.f;
+    bool ok = true;
+    for (int j = 0; j < n; ++j) {
+      ok = mbar_wait_warp(bar(C::B_SFULL + q), j & 1, ab);
+      if (!ok) break;
+      tc_fence_after();
+      const int k0 = j * C::BN;
+      const bool need_mask = (k0 + C::BN > L) || (causal && k0 + C::BN - 1 > q0 + q * C::BM);
+      const int lim = causal ? min(L - 1, qrow) : (L - 1);  // last allowed key of this row
+      // pass 1: row max of the raw scores
+      float mx = -INFINITY;
+#pragma unroll
+      for (int c = 0; c < 4; ++c) {
+        uint32_t r[32];
+        tmem_ld32(tS + 32 * c, r);
+        tmem_wait_ld();
+#pragma unroll
+        for (int e = 0; e < 32; ++e) {
+          const float v = (need_mask && k0 + 32 * c + e > lim) ? -INFINITY : __uint_as_float(r[e]);
+          mx = fmaxf(mx, v);
+        }
+      }
+      const float mx2 = mx * scale_log2;
+      const bool need = mx2 > m_ref + 8.f;
+      if (__any_sync(0xffffffffu, need)) {
+        const float m_new = fmaxf(m_ref, mx2);
+        const float alpha = ex2(m_ref - m_new);
+        if (j > 0) {
+          // O holds the sum up to tile j-1: wait for that P V, then rescale.
+          ok = mbar_wait_warp(bar(C::B_ODONE + q), (j - 1) & 1, ab);
+          if (!ok) break;
+          tc_fence_after();
+#pragma unroll
+          for (int c = 0; c < DP / 32; ++c) {
+            uint32_t r[32];
+            tmem_ld32(tO + 32 * c, r);
+            tmem_wait_ld();
+#pragma unroll
+            for (int e = 0; e < 32; ++e) r[e] = __float_as_uint(__uint_as_float(r[e]) * alpha);
+            tmem_st32(tO + 32 * c, r);
+          }
+        }
+        l *= alpha;
+        m_ref = m_new;
+      }
+      // pass 2: P = exp2(s * scale * log2e - m_ref), packed to bf16 in place over
+      // the first 64 columns of S (chunk c only overwrites columns already read).
+      float rs = 0.f;
+#pragma unroll
+      for (int c = 0; c < 4; ++c) {
+        uint32_t r[32];
+        tmem_ld32(tS + 32 * c, r);
+        tmem_wait_ld();
+        uint32_t pk[16];
+#pragma unroll
+        for (int e = 0; e < 16; ++e) {
+          const int kc = k0 + 32 * c + 2 * e;
+          float p0 = ex2(fmaf(__uint_as_float(r[2 * e]), scale_log2, -m_ref));
+          float p1 = ex2(fmaf(__uint_as_float(r[2 * e + 1]), scale_log2, -m_ref));
+          if (need_mask) {
+            if (kc > lim) p0 = 0.f;
+            if (kc + 1 > lim) p1 = 0.f;
+          }
+          rs += p0 + p1;
+          pk[e] = pack_bf16(p0, p1);
+        }
+        tmem_st16(tS + 16 * c, pk);
+      }
+      l += rs;
+      tmem_wait_st();
+      tc_fence_before();
+      mbar_arrive(bar(C::B_PREADY + q));
+    }
+    if (ok && n > 0) ok = mbar_wait_warp(bar(C::B_ODONE + q), (n - 1) & 1, ab);
+    if (ok && n > 0) {
+      tc_fence_after();
+      const float inv = 1.f / l;
+      const bool valid = qrow < L;
+      float *orow = O + (static_cast<size_t>(bh) * L + (valid ? qrow : 0)) * D;
+#pragma unroll
+      for (int c = 0; c < DP / 32; ++c) {
+        uint32_t r[32];
+        tmem_ld32(tO + 32 * c, r);
+        tmem_wait_ld();
+        if (valid && 32 * c < D) {
+#pragma unroll
+          for (int e = 0; e < 32; e += 4) {
+            float4 v = make_float4(__uint_as_float(r[e]) * inv, __uint_as_float(r[e + 1]) * inv,
+                                   __uint_as_float(r[e + 2]) * inv,
+                                   __uint_as_float(r[e + 3]) * inv);
+            *reinterpret_cast<float4 *>(orow + 32 * c + e) = v;
+          }
+        }
+      }
+      if (valid) LSE[static_cast<size_t>(bh) * L + qrow] = (m_ref + log2f(l)) * kLn2;
+    }
+  }
+
+  // ------------------------------------------------------------ teardown
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 0) {
+    tc_fence_after();
+    tmem_dealloc(tmem, C::TMEM_COLS);
+  }
+}
+
+uint64_t wait_limit_ns() {
+  static uint64_t v = [] {
+    const char *e = getenv("MG_WAIT_TIMEOUT_MS");
+    long long ms = e ? atoll(e) : 4000;
+    if (ms < 1) ms = 1;
+    return static_cast<uint64_t>(ms) * 1000000ull;
+  }();
+  return v;
+}
+
+template <int DP>
+cudaError_t launch(const __nv_bfloat16 *Q, const __nv_bfloat16 *K, const __nv_bfloat16 *V,
+                   float *O, float *LSE, const MgProblem &p, unsigned int *err,
+                   cudaStream_t st) {
+  using C = FwdCfg<DP>;
+  const int BH = p.B * p.H;
+  CUtensorMap tq, tk, tv;
+  cudaError_t e;
+  if ((e = mg_tmap_bf16(&tq, Q, p.D, p.L, BH, C::BM)) != cudaSuccess) return e;
+  if ((e = mg_tmap_bf16(&tk, K, p.D, p.L, BH, C::BN)) != cudaSuccess) return e;
+  if ((e = mg_tmap_bf16(&tv, V, p.D, p.L, BH, C::BN)) != cudaSuccess) return e;
+  auto kern = accel_fwd_kernel<DP>;
+  if ((e = mg_set_smem_attr(reinterpret_cast<const void *>(kern), C::SMEM_BYTES,
+                            DP == 64 ? 6 : 7)) != cudaSuccess)
+    return e;
+  const int nqb = (p.L + 255) / 256;
+  const long long grid = static_cast<long long>(nqb) * BH;
+  kern<<<static_cast<unsigned>(grid), C::NTHREADS, C::SMEM_BYTES, st>>>(
+      tq, tk, tv, O, LSE, BH, p.L, p.D, p.causal, p.scale * kLog2e, err, wait_limit_ns());
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t mg_launch_accel_fwd(const __nv_bfloat16 *Q, const __nv_bfloat16 *K,
+                                const __nv_bfloat16 *V, float *O, float *LSE,
+                                const MgProblem &p, unsigned int *err, cudaStream_t st) {
+  if (p.D <= 64) return launch<64>(Q, K, V, O, LSE, p, err, st);
+  return launch<128>(Q, K, V, O, LSE, p, err, st);
+}

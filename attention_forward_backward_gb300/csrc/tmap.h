@@ -1,0 +1,16 @@
+// tmap.h -- host-side TMA tensor-map encoding for the ACCEL kernels.
+//
+// Every [B][H][L][D] tensor is described as a 3-D tensor (D, L, B*H) so that
+// rows at or past L of one head read as zeros instead of the next head's rows.
+// cuTensorMapEncodeTiled is reached through the runtime's driver entry-point
+// query, so the library does not link libcuda directly. Encoding is host-only
+// work on a caller-owned struct: no device allocation.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+// bf16 tensor, boxes of 64 columns x box_rows rows, 128-byte swizzle.
+cudaError_t mg_tmap_bf16(CUtensorMap *m, const void *ptr, int D, int L, int BH, int box_rows);
+// f32 tensor, boxes of 32 columns x box_rows rows, 128-byte swizzle (dQ reduce).
+cudaError_t mg_tmap_f32(CUtensorMap *m, const void *ptr, int D, int L, int BH, int box_rows);

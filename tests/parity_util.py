@@ -2,11 +2,12 @@
 seeded inputs and compare element by element with the fp64 oracle.
 
 Error metric (per output tensor X in O, dQ, dK, dV):
-    err(X) = max |X_gpu - X_ref| / max(max |X_ref|, 1e-3 * M)
+    err(X) = max |X_gpu - X_ref| / max(max |X_ref|, 1e-2 * M)
 where M is the largest max |Y_ref| over the outputs Y of the same call. The
-floor only matters where the exact result is identically zero (L = 1 gives
-dQ = dK = 0, which f32 reaches only up to rounding); everywhere else the
-denominator is max |X_ref|.
+floor only matters where the exact result is identically zero: L = 1 gives
+dQ = dK = 0, which f32 reaches only up to the cancellation in dP - Dvec (two
+equal dot products of length D); on every other case the denominator is
+max |X_ref|.
 Gates: STRICT_F32 <= 1e-4, ACCEL_BF16 <= 2e-2. LSE is compared by
 max |LSE_gpu - LSE_ref| / max(1, max |LSE_ref|) with the same gates.
 """
@@ -85,7 +86,7 @@ def compare(got: dict, ref: dict, contract: str, keys=("O", "dQ", "dK", "dV")):
     present = [k for k in keys if k in got]
     scale = max((float(np.max(np.abs(ref[k]))) for k in present if ref[k].size), default=0.0)
     for k in present:
-        errs[k] = rel_err(got[k], ref[k], floor=1e-3 * scale)
+        errs[k] = rel_err(got[k], ref[k], floor=1e-2 * scale)
     if "LSE" in got and "LSE" in ref:
         errs["LSE"] = lse_err(got["LSE"], ref["LSE"])
     bad = {k: e for k, e in errs.items() if not (e <= tol)}
