@@ -54,6 +54,9 @@ def parse():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--contract", choices=["both", "accel", "strict"], default="both")
     ap.add_argument("--cfg", type=int, default=5)
+    ap.add_argument("--shape", default=None,
+                    help="B,H,L,D,causal: a custom seeded workload instead of --cfg "
+                         "(used for small profiling captures)")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=15.0,
@@ -206,8 +209,8 @@ def run_contract(mg, torch, w, contract, args, device, stream, peaks, sm_count, 
     ws_n = world()
     flops_step = w.flops_fwd() + w.flops_bwd()
     res = {
-        "fwd_bwd_tflops": ws_n * flops_step * args.steps / (total_ms * 1e-3) / 1e12,
-        "fwd_tflops": ws_n * w.flops_fwd() * args.steps / (fwd_total_ms * 1e-3) / 1e12,
+        "fwd_bwd_tflops": job_tflops(flops_step, args.steps, total_ms, ws_n),
+        "fwd_tflops": job_tflops(w.flops_fwd(), args.steps, fwd_total_ms, ws_n),
         "ms_per_step": total_ms / args.steps,
         "fwd_ms_median": statistics.median(fwd_ms),
         "step_ms_median": statistics.median(tot_ms),
@@ -290,7 +293,7 @@ def run_e2e(mg, torch, w, contract, args, host, device, stream, flops_step):
         torch.cuda.synchronize()
         barrier()
     ms = max_over_ranks(a.elapsed_time(b))
-    return {"value": world() * flops_step * args.steps / (ms * 1e-3) / 1e12, "unit": UNIT,
+    return {"value": job_tflops(flops_step, args.steps, ms, world()), "unit": UNIT,
             "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
             "ms_per_step": ms / args.steps}
 
@@ -314,13 +317,23 @@ def barrier():
 
 
 def max_over_ranks(x: float) -> float:
+    """Maximum of a per-rank scalar over all ranks (a time: the job is as slow
+    as its slowest rank). NCCL needs a CUDA tensor, gloo a CPU one."""
     if not _DIST["on"]:
         return x
     import torch
     import torch.distributed as dist
-    t = torch.tensor([x], dtype=torch.float64, device="cuda")
+    dev = "cuda" if dist.get_backend() == "nccl" else "cpu"
+    t = torch.tensor([x], dtype=torch.float64, device=dev)
     dist.all_reduce(t, op=dist.ReduceOp.MAX)
     return float(t.item())
+
+
+def job_tflops(flops_per_rank_step: float, steps: int, max_ms: float, n_ranks: int) -> float:
+    """Whole-job throughput: every rank runs the same per-GPU workload (heads
+    are independent, no exchange), so the job did n_ranks x the work of one
+    rank in the slowest rank's time."""
+    return n_ranks * flops_per_rank_step * steps / (max_ms * 1e-3) / 1e12
 
 
 # ------------------------------------------------------------------ oracle (CPU)
@@ -350,7 +363,11 @@ def oracle_sample(w, contract: str, target_s: float):
 # ------------------------------------------------------------------ main
 def main():
     args = parse()
-    w = synth.WORKLOADS[args.cfg]
+    if args.shape:
+        B, H, L, D, causal = (int(x) for x in args.shape.split(","))
+        w = synth.custom_workload(B, H, L, D, bool(causal), seed_cfg=800)
+    else:
+        w = synth.WORKLOADS[args.cfg]
     if args.impl == "reference":
         return main_reference(args, w)
 
@@ -373,7 +390,7 @@ def main():
     contracts = ["accel", "strict"] if args.contract == "both" else [args.contract]
     results = {}
     for c in contracts:
-        if c not in w.contracts:
+        if c not in w.contracts and not args.shape:
             continue
         clocks = ClockSampler(local) if rank() == 0 else None
         results[c] = run_contract(mg, torch, w, c, args, device, stream, peaks, sm_count, clocks)
