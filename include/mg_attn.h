@@ -109,6 +109,27 @@ int mg_attn_bwd(const void *Q, const void *K, const void *V, const void *O,
                 int B, int H, int L, int D, int causal, float scale, int contract,
                 void *workspace, size_t workspace_bytes, void *stream);
 
+/*
+ * mg_attn_bwd without a workspace, for callers that cannot allocate device
+ * memory at all (a plugin whose host runtime owns every device allocation and
+ * offers no scratch, a service that fixes its memory budget at start-up, a
+ * caller that cannot afford cudaMalloc's implicit synchronisation). The paper
+ * has no counterpart: its runtime plans every buffer itself.
+ * Same arguments, results and errors as mg_attn_bwd minus the workspace. The
+ * Dvec scratch is a fixed device array inside the library (4 MiB, held by every
+ * GPU that loads the library until the process exits), so B*H*L must not
+ * exceed 1,048,576 rows; larger problems return MG_ERR_WORKSPACE before
+ * anything is launched. Nothing is allocated or freed.
+ * The first call on each device looks up the array's device address (make it
+ * before any stream capture). All calls on a device share the array: calls
+ * whose kernels overlap on the GPU race, calls ordered on one stream do not.
+ * No part of the array needs to start at zero.
+ */
+int mg_attn_bwd_noalloc(const void *Q, const void *K, const void *V, const void *O,
+                        const void *dO, const float *LSE, void *dQ, void *dK, void *dV,
+                        int B, int H, int L, int D, int causal, float scale, int contract,
+                        void *stream);
+
 /* Static, human-readable name of a status code. Never NULL. */
 const char *mg_status_string(int status);
 
