@@ -22,6 +22,12 @@
 //                              computes dQ_i^T = K^T dS^T so that M = 128)
 // dQ_i leaves TMEM through a swizzled f32 staging tile and a TMA tensor
 // add-reduction into dQ (zeroed by the host call beforehand).
+// MMA issue order per block: dV(i), S(i+1), dP(i+1), dK(i), dQ(i), so that the
+// tensor core computes the next block's scores while the softmax warps turn
+// dP(i) into dS(i), and dK/dQ run while they turn S(i+1) into P(i+1). dP^T is
+// double-buffered in TMEM for D = 128 (for D = 64 it goes after dQ(i)); Q and
+// dO stream through a 3-stage ring so that a tile's load has two blocks of
+// lead time.
 // Warp roles: 0-3 dQ epilogue, 4 TMA producer (plus LSE/Dvec staging), 5 MMA
 // issuer, 8-15 two softmax warpgroups splitting the query columns.
 // Every wait is bounded; on a give-up the CTA sets the device error word and
@@ -39,7 +45,7 @@ struct BwdCfg {
   static constexpr int BN = 128;                    // keys per CTA
   static constexpr int BQ = DP == 128 ? 64 : 128;   // queries per block
   static constexpr int QPW = BQ / 2;                // query columns per softmax warpgroup
-  static constexpr int NS = DP == 128 ? 2 : 1;      // S^T buffers in TMEM
+  static constexpr int ND = DP == 128 ? 2 : 1;      // dP^T buffers in TMEM
   static constexpr int NCHUNK = DP / 64;
   static constexpr int KV_TILE = BN * DP * 2;
   static constexpr int BOX_KV = BN * 128;
@@ -47,38 +53,41 @@ struct BwdCfg {
   static constexpr int BOX_Q = BQ * 128;
   static constexpr int DS_CHUNK = BN * 128;         // [128 keys][64 q] bf16
   static constexpr int NQC = BQ / 64;               // dS^T chunks
+  static constexpr int DS_BUF = NQC * DS_CHUNK;
+  static constexpr int NQS = 3;                     // Q/dO ring stages
   static constexpr int DQ_BOX = BQ * 128;           // [BQ][32] f32
   // shared memory
   static constexpr int OFF_K = 0;
   static constexpr int OFF_V = OFF_K + KV_TILE;
-  static constexpr int OFF_Q = OFF_V + KV_TILE;             // 2 stages
-  static constexpr int OFF_DO = OFF_Q + 2 * Q_TILE;         // 2 stages
-  static constexpr int OFF_DS = OFF_DO + 2 * Q_TILE;        // NQC chunks
-  static constexpr int OFF_DQ = OFF_DS + NQC * DS_CHUNK;    // DP/32 boxes
-  static constexpr int OFF_LSE = OFF_DQ + (DP / 32) * DQ_BOX;  // 2 stages x BQ f32
-  static constexpr int OFF_DV = OFF_LSE + 2 * BQ * 4;          // 2 stages x BQ f32
-  static constexpr int OFF_BAR = OFF_DV + 2 * BQ * 4;
+  static constexpr int OFF_Q = OFF_V + KV_TILE;             // NQS stages
+  static constexpr int OFF_DO = OFF_Q + NQS * Q_TILE;       // NQS stages
+  static constexpr int OFF_DS = OFF_DO + NQS * Q_TILE;      // one dS^T tile
+  static constexpr int OFF_DQ = OFF_DS + DS_BUF;            // DP/32 boxes
+  static constexpr int OFF_LSE = OFF_DQ + (DP / 32) * DQ_BOX;  // NQS stages x BQ f32
+  static constexpr int OFF_DV = OFF_LSE + NQS * BQ * 4;        // NQS stages x BQ f32
+  static constexpr int OFF_BAR = OFF_DV + NQS * BQ * 4;
   static constexpr int B_KVFULL = 0;
-  static constexpr int B_QFULL = 1;      // 2
-  static constexpr int B_QEMPTY = 3;     // 2
-  static constexpr int B_SFULL = 5;      // NS (<= 2)
-  static constexpr int B_PREADY = 7;     // NS
-  static constexpr int B_DPFULL = 9;
-  static constexpr int B_DSREADY = 10;
-  static constexpr int B_DQFULL = 11;
-  static constexpr int B_DQEMPTY = 12;
-  static constexpr int B_ACCDONE = 13;
-  static constexpr int B_DRAIN = 14;
-  static constexpr int NBAR = 15;
+  static constexpr int B_QFULL = 1;      // NQS (Q/dO stage)
+  static constexpr int B_QEMPTY = 4;     // NQS
+  static constexpr int B_SFULL = 7;
+  static constexpr int B_PREADY = 8;
+  static constexpr int B_DPFULL = 9;     // 2 (dP buffer)
+  static constexpr int B_DSREADY = 11;   // 2 (block parity)
+  static constexpr int B_DSMFREE = 13;
+  static constexpr int B_DQFULL = 14;
+  static constexpr int B_DQEMPTY = 15;
+  static constexpr int B_ACCDONE = 16;
+  static constexpr int B_DRAIN = 17;
+  static constexpr int NBAR = 18;
   static constexpr int OFF_MISC = OFF_BAR + NBAR * 8;
   static constexpr int SMEM_BYTES = OFF_MISC + 16 + 1024;
   static constexpr int NTHREADS = 512;
   static constexpr int TMEM_COLS = 512;
   static constexpr int T_DV = 0;
   static constexpr int T_DK = DP;
-  static constexpr int T_S = 2 * DP;                  // NS x BQ
-  static constexpr int T_DP = T_S + NS * BQ;          // BQ
-  static constexpr int T_DQ = T_DP + BQ;              // 64
+  static constexpr int T_S = 2 * DP;                  // BQ
+  static constexpr int T_DP = T_S + BQ;               // ND x BQ
+  static constexpr int T_DQ = T_DP + ND * BQ;         // 64
   static_assert(T_DQ + 64 <= TMEM_COLS, "TMEM column budget");
   static_assert(SMEM_BYTES <= 227 * 1024, "shared memory budget");
 };
@@ -136,8 +145,11 @@ __global__ void __launch_bounds__(512, 1)
   float *sDv = reinterpret_cast<float *>(smem + C::OFF_DV);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int kb = static_cast<int>(blockIdx.x / BH);  // causal: kb = 0 has the most work
-  const int bh = static_cast<int>(blockIdx.x % BH);
+  // Head-major order: CTAs that run together share a few heads' Q/dO in L2;
+  // within a head the heaviest causal key block (kb = 0) goes first.
+  const int nkb = (L + C::BN - 1) / C::BN;
+  const int bh = static_cast<int>(blockIdx.x / nkb);
+  const int kb = static_cast<int>(blockIdx.x % nkb);
   const int k0 = kb * C::BN;
   const int nqb = (L + C::BQ - 1) / C::BQ;
   const int qb0 = causal ? (k0 / C::BQ) : 0;
@@ -150,8 +162,8 @@ __global__ void __launch_bounds__(512, 1)
   if (threadIdx.x == 128) {
     for (int i = 0; i < C::NBAR; ++i) {
       uint32_t cnt = 1;
-      if (i == C::B_QEMPTY || i == C::B_QEMPTY + 1) cnt = 1 + 8;
-      if (i == C::B_PREADY || i == C::B_PREADY + 1 || i == C::B_DSREADY) cnt = 8;
+      if (i >= C::B_QEMPTY && i < C::B_QEMPTY + C::NQS) cnt = 1 + 8;
+      if (i == C::B_PREADY || i == C::B_DSREADY || i == C::B_DSREADY + 1) cnt = 8;
       if (i == C::B_DQEMPTY) cnt = 4;
       mbar_init(bar(i), cnt);
     }
@@ -181,8 +193,9 @@ __global__ void __launch_bounds__(512, 1)
     }
     int issued = 0;
     for (int i = 0; i < n; ++i) {
-      const int st = i & 1;
-      if (i >= 2 && !mbar_wait_warp(bar(C::B_QEMPTY + st), ((i >> 1) - 1) & 1, ab)) break;
+      const int st = i % C::NQS;
+      if (i >= C::NQS && !mbar_wait_warp(bar(C::B_QEMPTY + st), ((i / C::NQS) - 1) & 1, ab))
+        break;
       const int q0 = (qb0 + i) * C::BQ;
       // LSE (pre-scaled to base 2; +inf past L so that P = 0 there) and Dvec.
       for (int r = lane; r < C::BQ; r += 32) {
@@ -205,8 +218,8 @@ __global__ void __launch_bounds__(512, 1)
     }
     if (lane == 0) {
       drain_wait(bar(C::B_KVFULL), 0, 2000000000ull);
-      for (int i = max(0, issued - 2); i < issued; ++i)
-        drain_wait(bar(C::B_QFULL + (i & 1)), (i >> 1) & 1, 2000000000ull);
+      for (int i = max(0, issued - C::NQS); i < issued; ++i)
+        drain_wait(bar(C::B_QFULL + i % C::NQS), (i / C::NQS) & 1, 2000000000ull);
     }
   } else if (warp == 5) {
     // ------------------------------------------------------------ MMA issuer
@@ -221,7 +234,7 @@ __global__ void __launch_bounds__(512, 1)
       auto wait_q = [&](int i) -> bool {
         if (qwaited >= i) return true;
         qwaited = i;
-        return mbar_wait(bar(C::B_QFULL + (i & 1)), (i >> 1) & 1, ab);
+        return mbar_wait(bar(C::B_QFULL + i % C::NQS), (i / C::NQS) & 1, ab);
       };
       // X^T = A_tile * B_i^T with A in {K, V}, B_i in {Q_i, dO_i}; both K-major.
       auto issue_T = [&](uint32_t sA, uint32_t sB, uint32_t d) {
@@ -236,16 +249,16 @@ __global__ void __launch_bounds__(512, 1)
       auto issue_S = [&](int i) -> bool {
         if (!wait_q(i)) return false;
         tc_fence_after();
-        issue_T(sK, sbase + C::OFF_Q + (i & 1) * C::Q_TILE,
-                tmem + C::T_S + (C::NS == 2 ? (i & 1) : 0) * C::BQ);
-        mma_commit(bar(C::B_SFULL + (C::NS == 2 ? (i & 1) : 0)));
+        issue_T(sK, sbase + C::OFF_Q + (i % C::NQS) * C::Q_TILE, tmem + C::T_S);
+        mma_commit(bar(C::B_SFULL));
         return true;
       };
       auto issue_dP = [&](int i) -> bool {
         if (!wait_q(i)) return false;
         tc_fence_after();
-        issue_T(sV, sbase + C::OFF_DO + (i & 1) * C::Q_TILE, tmem + C::T_DP);
-        mma_commit(bar(C::B_DPFULL));
+        const int db = C::ND == 2 ? (i & 1) : 0;
+        issue_T(sV, sbase + C::OFF_DO + (i % C::NQS) * C::Q_TILE, tmem + C::T_DP + db * C::BQ);
+        mma_commit(bar(C::B_DPFULL + db));
         return true;
       };
       // acc (+)= X^T(tmem, bf16) * Y_i (MN-major smem), K = BQ queries.
@@ -260,43 +273,37 @@ __global__ void __launch_bounds__(512, 1)
       };
       if (ok) ok = issue_S(0);
       if (ok) ok = issue_dP(0);
-      if (ok && C::NS == 2 && n > 1) ok = issue_S(1);
       for (int i = 0; ok && i < n; ++i) {
-        const int st = i & 1;
-        const int b = C::NS == 2 ? (i & 1) : 0;
-        const uint32_t pph = C::NS == 2 ? ((i >> 1) & 1) : (i & 1);
-        if (!(ok = mbar_wait(bar(C::B_PREADY + b), pph, ab))) break;
+        const int st = i % C::NQS;
+        const int db = C::ND == 2 ? (i & 1) : 0;
+        if (!(ok = mbar_wait(bar(C::B_PREADY), i & 1, ab))) break;
         tc_fence_after();
-        issue_acc(tmem + C::T_S + b * C::BQ, sbase + C::OFF_DO + st * C::Q_TILE,
-                  tmem + C::T_DV, i == 0);
-        if (!(ok = mbar_wait(bar(C::B_DSREADY), i & 1, ab))) break;
+        issue_acc(tmem + C::T_S, sbase + C::OFF_DO + st * C::Q_TILE, tmem + C::T_DV, i == 0);
+        if (i + 1 < n && !(ok = issue_S(i + 1))) break;
+        if (C::ND == 2 && i + 1 < n && !(ok = issue_dP(i + 1))) break;
+        if (!(ok = mbar_wait(bar(C::B_DSREADY + (i & 1)), (i >> 1) & 1, ab))) break;
         tc_fence_after();
-        issue_acc(tmem + C::T_DP, sbase + C::OFF_Q + st * C::Q_TILE, tmem + C::T_DK, i == 0);
+        issue_acc(tmem + C::T_DP + db * C::BQ, sbase + C::OFF_Q + st * C::Q_TILE,
+                  tmem + C::T_DK, i == 0);
         mma_commit(bar(C::B_QEMPTY + st));
         if (i > 0 && !(ok = mbar_wait(bar(C::B_DQEMPTY), (i - 1) & 1, ab))) break;
         tc_fence_after();
+        const uint32_t sDSi = sDS;
 #pragma unroll
         for (int kk = 0; kk < C::BN / 16; ++kk) {
           if (DP == 128) {
             // dQ^T [d][q] = K^T [d][key] * dS^T [key][q]
             mma_ss(tmem + C::T_DQ, sdesc_sw128(sK + kk * 2048, C::BOX_KV, 1024),
-                   sdesc_sw128(sDS + kk * 2048, C::DS_CHUNK, 1024), idDQ, kk > 0 ? 1u : 0u);
+                   sdesc_sw128(sDSi + kk * 2048, C::DS_CHUNK, 1024), idDQ, kk > 0 ? 1u : 0u);
           } else {
             // dQ [q][d] = dS [q][key] * K [key][d]
-            mma_ss(tmem + C::T_DQ, sdesc_sw128(sDS + kk * 2048, C::DS_CHUNK, 1024),
+            mma_ss(tmem + C::T_DQ, sdesc_sw128(sDSi + kk * 2048, C::DS_CHUNK, 1024),
                    sdesc_sw128(sK + kk * 2048, C::BOX_KV, 1024), idDQ, kk > 0 ? 1u : 0u);
           }
         }
         mma_commit(bar(C::B_DQFULL));
-        if (i + 1 < n) {
-          if (C::NS == 1) {
-            if (!(ok = issue_S(i + 1))) break;
-          }
-          if (!(ok = issue_dP(i + 1))) break;
-          if (C::NS == 2 && i + 2 < n) {
-            if (!(ok = issue_S(i + 2))) break;
-          }
-        }
+        mma_commit(bar(C::B_DSMFREE));
+        if (C::ND == 1 && i + 1 < n && !(ok = issue_dP(i + 1))) break;
       }
       mma_commit(bar(C::B_ACCDONE));
       mma_commit(bar(C::B_DRAIN));
@@ -364,18 +371,17 @@ __global__ void __launch_bounds__(512, 1)
     const uint32_t sDS = sbase + C::OFF_DS;
     bool ok = true;
     for (int i = 0; i < n; ++i) {
-      const int st = i & 1;
-      const int b = C::NS == 2 ? (i & 1) : 0;
-      const uint32_t sph = C::NS == 2 ? ((i >> 1) & 1) : (i & 1);
+      const int st = i % C::NQS;
+      const int db = C::ND == 2 ? (i & 1) : 0;
       const int q0 = (qb0 + i) * C::BQ;
-      if (!(ok = mbar_wait_warp(bar(C::B_QFULL + st), (i >> 1) & 1, ab))) break;
-      if (!(ok = mbar_wait_warp(bar(C::B_SFULL + b), sph, ab))) break;
+      if (!(ok = mbar_wait_warp(bar(C::B_QFULL + st), (i / C::NQS) & 1, ab))) break;
+      if (!(ok = mbar_wait_warp(bar(C::B_SFULL), i & 1, ab))) break;
       tc_fence_after();
       const bool need_mask = (kg >= L) || (causal && k0 + C::BN - 1 > q0);
       const float *lse = sLse + st * C::BQ + g * C::QPW;
       const float *dvq = sDv + st * C::BQ + g * C::QPW;
-      const uint32_t tS = tmem + lane_off + C::T_S + b * C::BQ + g * C::QPW;
-      const uint32_t tDP = tmem + lane_off + C::T_DP + g * C::QPW;
+      const uint32_t tS = tmem + lane_off + C::T_S + g * C::QPW;
+      const uint32_t tDP = tmem + lane_off + C::T_DP + db * C::BQ + g * C::QPW;
       float p[C::QPW];
 #pragma unroll
       for (int c = 0; c < C::QPW / 32; ++c) {
@@ -402,12 +408,14 @@ __global__ void __launch_bounds__(512, 1)
       tmem_wait_st();
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(bar(C::B_PREADY + b));
+      if (lane == 0) mbar_arrive(bar(C::B_PREADY));
 
-      if (!(ok = mbar_wait_warp(bar(C::B_DPFULL), i & 1, ab))) break;
-      // the dS staging tile is free once the previous dQ MMA has completed
-      if (i > 0 && !(ok = mbar_wait_warp(bar(C::B_DQFULL), (i - 1) & 1, ab))) break;
+      if (!(ok = mbar_wait_warp(bar(C::B_DPFULL + db), (C::ND == 2 ? (i >> 1) : i) & 1, ab)))
+        break;
+      // the dS staging tile is free once dQ(i-1) has completed
+      if (i >= 1 && !(ok = mbar_wait_warp(bar(C::B_DSMFREE), (i - 1) & 1, ab))) break;
       tc_fence_after();
+      const uint32_t sDSi = sDS;
 #pragma unroll
       for (int c = 0; c < C::QPW / 32; ++c) {
         uint32_t r[32];
@@ -424,7 +432,7 @@ __global__ void __launch_bounds__(512, 1)
         tmem_st16(tDP + 16 * c, pk);
         // dS^T row kr, queries ql .. ql+31 into the swizzled smem tile
         const int ql = g * C::QPW + 32 * c;
-        const uint32_t chunk = sDS + (ql >> 6) * C::DS_CHUNK + kr * 128;
+        const uint32_t chunk = sDSi + (ql >> 6) * C::DS_CHUNK + kr * 128;
 #pragma unroll
         for (int u4 = 0; u4 < 4; ++u4) {
           const int unit = ((ql & 63) >> 3) + u4;
@@ -437,7 +445,7 @@ __global__ void __launch_bounds__(512, 1)
       tc_fence_before();
       __syncwarp();
       if (lane == 0) {
-        mbar_arrive(bar(C::B_DSREADY));
+        mbar_arrive(bar(C::B_DSREADY + (i & 1)));
         mbar_arrive(bar(C::B_QEMPTY + st));
       }
     }

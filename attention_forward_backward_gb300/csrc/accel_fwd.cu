@@ -22,6 +22,8 @@
 // * Warp 8 is the TMA producer.
 // Every wait is bounded (a few seconds); a wait that gives up sets the device
 // error word and the CTA leaves through the same teardown as a normal exit.
+#include <string.h>
+
 #include "internal.h"
 #include "tc_common.cuh"
 #include "tmap.h"
@@ -80,7 +82,7 @@ __global__ void __launch_bounds__(320, 1)
                      const __grid_constant__ CUtensorMap tmK,
                      const __grid_constant__ CUtensorMap tmV, float *__restrict__ O,
                      float *__restrict__ LSE, int BH, int L, int D, int causal, float scale_log2,
-                     unsigned int *err, unsigned long long timeout_ns) {
+                     unsigned int *err, unsigned long long timeout_ns, int fault) {
   using C = FwdCfg<DP>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
@@ -92,6 +94,7 @@ __global__ void __launch_bounds__(320, 1)
   volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + C::OFF_MISC + 4);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  // Heaviest causal query blocks (largest qb) of every head go first.
   const int nqb = (L + 255) / 256;
   const int qb = nqb - 1 - static_cast<int>(blockIdx.x / BH);
   const int bh = static_cast<int>(blockIdx.x % BH);
@@ -128,7 +131,7 @@ __global__ void __launch_bounds__(320, 1)
   if (warp == 8) {
     // ------------------------------------------------------------ TMA producer
     if (lane == 0) {
-      int issued = 0;
+      int issued = 0, skipped = -1;
       mbar_arrive_expect_tx(bar(C::B_QFULL), C::NQ * C::Q_TILE);
       for (int q = 0; q < C::NQ; ++q)
         for (int c = 0; c < C::NCHUNK; ++c)
@@ -139,10 +142,16 @@ __global__ void __launch_bounds__(320, 1)
         if (j >= C::NSTAGE &&
             !mbar_wait(bar(C::B_KVEMPTY + s), ((j / C::NSTAGE) - 1) & 1, ab))
           break;
-        mbar_arrive_expect_tx(bar(C::B_KFULL + s), C::KV_TILE);
-        for (int c = 0; c < C::NCHUNK; ++c)
-          tma_load_3d(sbase + C::OFF_K + s * C::KV_TILE + c * C::BOX_KV, &tmK, c * 64,
-                      j * C::BN, bh, bar(C::B_KFULL + s));
+        if (fault == 1 && j == 1) {
+          // Injected fault (tests only): key tile 1 is never loaded, so the
+          // MMA issuer's bounded wait on it must expire and report a timeout.
+          skipped = j;
+        } else {
+          mbar_arrive_expect_tx(bar(C::B_KFULL + s), C::KV_TILE);
+          for (int c = 0; c < C::NCHUNK; ++c)
+            tma_load_3d(sbase + C::OFF_K + s * C::KV_TILE + c * C::BOX_KV, &tmK, c * 64,
+                        j * C::BN, bh, bar(C::B_KFULL + s));
+        }
         mbar_arrive_expect_tx(bar(C::B_VFULL + s), C::KV_TILE);
         for (int c = 0; c < C::NCHUNK; ++c)
           tma_load_3d(sbase + C::OFF_V + s * C::KV_TILE + c * C::BOX_KV, &tmV, c * 64,
@@ -153,7 +162,7 @@ __global__ void __launch_bounds__(320, 1)
       drain_wait(bar(C::B_QFULL), 0, 2000000000ull);
       for (int j = max(0, issued - C::NSTAGE); j < issued; ++j) {
         const int s = j % C::NSTAGE;
-        drain_wait(bar(C::B_KFULL + s), (j / C::NSTAGE) & 1, 2000000000ull);
+        if (j != skipped) drain_wait(bar(C::B_KFULL + s), (j / C::NSTAGE) & 1, 2000000000ull);
         drain_wait(bar(C::B_VFULL + s), (j / C::NSTAGE) & 1, 2000000000ull);
       }
     }
@@ -339,6 +348,16 @@ uint64_t wait_limit_ns() {
   return v;
 }
 
+// Test hook: MG_FAULT_INJECT=skip_k_tile makes the forward's producer skip one
+// key-tile load (read once per process; off unless the variable is set).
+int fault_mode() {
+  static int v = [] {
+    const char *e = getenv("MG_FAULT_INJECT");
+    return (e && strcmp(e, "skip_k_tile") == 0) ? 1 : 0;
+  }();
+  return v;
+}
+
 template <int DP>
 cudaError_t launch(const __nv_bfloat16 *Q, const __nv_bfloat16 *K, const __nv_bfloat16 *V,
                    float *O, float *LSE, const MgProblem &p, unsigned int *err,
@@ -357,7 +376,8 @@ cudaError_t launch(const __nv_bfloat16 *Q, const __nv_bfloat16 *K, const __nv_bf
   const int nqb = (p.L + 255) / 256;
   const long long grid = static_cast<long long>(nqb) * BH;
   kern<<<static_cast<unsigned>(grid), C::NTHREADS, C::SMEM_BYTES, st>>>(
-      tq, tk, tv, O, LSE, BH, p.L, p.D, p.causal, p.scale * kLog2e, err, wait_limit_ns());
+      tq, tk, tv, O, LSE, BH, p.L, p.D, p.causal, p.scale * kLog2e, err, wait_limit_ns(),
+      fault_mode());
   return cudaGetLastError();
 }
 
