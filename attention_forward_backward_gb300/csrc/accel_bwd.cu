@@ -21,7 +21,8 @@
 //   dQ_i = dS K               (dS^T also staged in smem; for D = 128 the MMA
 //                              computes dQ_i^T = K^T dS^T so that M = 128)
 // dQ_i leaves TMEM through a swizzled f32 staging tile and a TMA tensor
-// add-reduction into dQ (zeroed by the host call beforehand).
+// add-reduction into dQ (zeroed by the host call beforehand); bulk reductions
+// sustain far more L2 throughput than per-element f32 reductions would.
 // MMA issue order per block: dV(i), S(i+1), dP(i+1), dK(i), dQ(i), so that the
 // tensor core computes the next block's scores while the softmax warps turn
 // dP(i) into dS(i), and dK/dQ run while they turn S(i+1) into P(i+1). dP^T is
@@ -55,15 +56,17 @@ struct BwdCfg {
   static constexpr int NQC = BQ / 64;               // dS^T chunks
   static constexpr int DS_BUF = NQC * DS_CHUNK;
   static constexpr int NQS = 3;                     // Q/dO ring stages
+  static constexpr int NDS = DP == 128 ? 2 : 1;     // dS^T smem buffers
   static constexpr int DQ_BOX = BQ * 128;           // [BQ][32] f32
+  static constexpr int DQ_STAGE = (DP / 32) * DQ_BOX;
   // shared memory
   static constexpr int OFF_K = 0;
   static constexpr int OFF_V = OFF_K + KV_TILE;
   static constexpr int OFF_Q = OFF_V + KV_TILE;             // NQS stages
   static constexpr int OFF_DO = OFF_Q + NQS * Q_TILE;       // NQS stages
-  static constexpr int OFF_DS = OFF_DO + NQS * Q_TILE;      // one dS^T tile
-  static constexpr int OFF_DQ = OFF_DS + DS_BUF;            // DP/32 boxes
-  static constexpr int OFF_LSE = OFF_DQ + (DP / 32) * DQ_BOX;  // NQS stages x BQ f32
+  static constexpr int OFF_DS = OFF_DO + NQS * Q_TILE;      // NDS dS^T tiles
+  static constexpr int OFF_DQ = OFF_DS + NDS * DS_BUF;      // dQ staging
+  static constexpr int OFF_LSE = OFF_DQ + DQ_STAGE;          // NQS stages x BQ f32
   static constexpr int OFF_DV = OFF_LSE + NQS * BQ * 4;        // NQS stages x BQ f32
   static constexpr int OFF_BAR = OFF_DV + NQS * BQ * 4;
   static constexpr int B_KVFULL = 0;
@@ -73,12 +76,12 @@ struct BwdCfg {
   static constexpr int B_PREADY = 8;
   static constexpr int B_DPFULL = 9;     // 2 (dP buffer)
   static constexpr int B_DSREADY = 11;   // 2 (block parity)
-  static constexpr int B_DSMFREE = 13;
-  static constexpr int B_DQFULL = 14;
-  static constexpr int B_DQEMPTY = 15;
-  static constexpr int B_ACCDONE = 16;
-  static constexpr int B_DRAIN = 17;
-  static constexpr int NBAR = 18;
+  static constexpr int B_DSMFREE = 13;   // NDS
+  static constexpr int B_DQFULL = 15;
+  static constexpr int B_DQEMPTY = 16;
+  static constexpr int B_ACCDONE = 17;
+  static constexpr int B_DRAIN = 18;
+  static constexpr int NBAR = 19;
   static constexpr int OFF_MISC = OFF_BAR + NBAR * 8;
   static constexpr int SMEM_BYTES = OFF_MISC + 16 + 1024;
   static constexpr int NTHREADS = 512;
@@ -129,7 +132,8 @@ __global__ void __launch_bounds__(512, 1)
                       const __grid_constant__ CUtensorMap tmV,
                       const __grid_constant__ CUtensorMap tmdO,
                       const __grid_constant__ CUtensorMap tmdQ, const float *__restrict__ LSE,
-                      const float *__restrict__ Dvec, float *__restrict__ dK,
+                      const float *__restrict__ Dvec, float *__restrict__ dQ,
+                      float *__restrict__ dK,
                       float *__restrict__ dV, int BH, int L, int D, int causal, float scale,
                       float scale_log2, unsigned int *err, unsigned long long timeout_ns) {
   using C = BwdCfg<DP>;
@@ -288,7 +292,7 @@ __global__ void __launch_bounds__(512, 1)
         mma_commit(bar(C::B_QEMPTY + st));
         if (i > 0 && !(ok = mbar_wait(bar(C::B_DQEMPTY), (i - 1) & 1, ab))) break;
         tc_fence_after();
-        const uint32_t sDSi = sDS;
+        const uint32_t sDSi = sDS + (i % C::NDS) * C::DS_BUF;
 #pragma unroll
         for (int kk = 0; kk < C::BN / 16; ++kk) {
           if (DP == 128) {
@@ -302,7 +306,7 @@ __global__ void __launch_bounds__(512, 1)
           }
         }
         mma_commit(bar(C::B_DQFULL));
-        mma_commit(bar(C::B_DSMFREE));
+        mma_commit(bar(C::B_DSMFREE + i % C::NDS));
         if (C::ND == 1 && i + 1 < n && !(ok = issue_dP(i + 1))) break;
       }
       mma_commit(bar(C::B_ACCDONE));
@@ -334,6 +338,7 @@ __global__ void __launch_bounds__(512, 1)
       if (lane == 0) mbar_arrive(bar(C::B_DQEMPTY));
       // The previous reduction must have finished reading the staging tile.
       if (t == 0) bulk_wait_group_read0();
+      __syncwarp();  // bar.sync is aligned: the whole warp arrives together
       named_bar_sync(1, 128);
       if (DP == 128) {
         // thread = d; r[q] = dQ^T[d][q]
@@ -388,9 +393,15 @@ __global__ void __launch_bounds__(512, 1)
         uint32_t r[32];
         tmem_ld32(tS + 32 * c, r);
         tmem_wait_ld();
+        float lv[32];
+#pragma unroll
+        for (int e = 0; e < 32; e += 4) {
+          const float4 v4 = *reinterpret_cast<const float4 *>(lse + 32 * c + e);
+          lv[e] = v4.x; lv[e + 1] = v4.y; lv[e + 2] = v4.z; lv[e + 3] = v4.w;
+        }
 #pragma unroll
         for (int e = 0; e < 32; ++e) {
-          float x = ex2(fmaf(__uint_as_float(r[e]), scale_log2, -lse[32 * c + e]));
+          float x = ex2(fmaf(__uint_as_float(r[e]), scale_log2, -lv[e]));
           if (need_mask) {
             const int qg = q0 + g * C::QPW + 32 * c + e;
             if (kg >= L || (causal && kg > qg)) x = 0.f;
@@ -412,21 +423,28 @@ __global__ void __launch_bounds__(512, 1)
 
       if (!(ok = mbar_wait_warp(bar(C::B_DPFULL + db), (C::ND == 2 ? (i >> 1) : i) & 1, ab)))
         break;
-      // the dS staging tile is free once dQ(i-1) has completed
-      if (i >= 1 && !(ok = mbar_wait_warp(bar(C::B_DSMFREE), (i - 1) & 1, ab))) break;
+      // this dS staging tile is free once dQ(i - NDS) has completed
+      if (i >= C::NDS &&
+          !(ok = mbar_wait_warp(bar(C::B_DSMFREE + i % C::NDS), ((i / C::NDS) - 1) & 1, ab)))
+        break;
       tc_fence_after();
-      const uint32_t sDSi = sDS;
+      const uint32_t sDSi = sDS + (i % C::NDS) * C::DS_BUF;
 #pragma unroll
       for (int c = 0; c < C::QPW / 32; ++c) {
         uint32_t r[32];
         tmem_ld32(tDP + 32 * c, r);
         tmem_wait_ld();
+        float dv[32];
+#pragma unroll
+        for (int e = 0; e < 32; e += 4) {
+          const float4 v4 = *reinterpret_cast<const float4 *>(dvq + 32 * c + e);
+          dv[e] = v4.x; dv[e + 1] = v4.y; dv[e + 2] = v4.z; dv[e + 3] = v4.w;
+        }
         uint32_t pk[16];
 #pragma unroll
         for (int e = 0; e < 16; ++e) {
-          const float d0 = p[32 * c + 2 * e] * (__uint_as_float(r[2 * e]) - dvq[32 * c + 2 * e]);
-          const float d1 =
-              p[32 * c + 2 * e + 1] * (__uint_as_float(r[2 * e + 1]) - dvq[32 * c + 2 * e + 1]);
+          const float d0 = p[32 * c + 2 * e] * (__uint_as_float(r[2 * e]) - dv[2 * e]);
+          const float d1 = p[32 * c + 2 * e + 1] * (__uint_as_float(r[2 * e + 1]) - dv[2 * e + 1]);
           pk[e] = pack_bf16(d0, d1);
         }
         tmem_st16(tDP + 16 * c, pk);
@@ -478,6 +496,8 @@ __global__ void __launch_bounds__(512, 1)
   }
 
   // ------------------------------------------------------------ teardown
+  // Reconverge single-lane roles first: __syncthreads is an aligned barrier.
+  __syncwarp();
   tc_fence_before();
   __syncthreads();
   if (warp == 0) {
@@ -517,7 +537,7 @@ cudaError_t launch(const __nv_bfloat16 *Q, const __nv_bfloat16 *K, const __nv_bf
   const int nkb = (p.L + C::BN - 1) / C::BN;
   const long long grid = static_cast<long long>(nkb) * BH;
   kern<<<static_cast<unsigned>(grid), C::NTHREADS, C::SMEM_BYTES, st>>>(
-      tq, tk, tv, tdo, tdq, LSE, Dvec, dK, dV, BH, p.L, p.D, p.causal, p.scale,
+      tq, tk, tv, tdo, tdq, LSE, Dvec, dQ, dK, dV, BH, p.L, p.D, p.causal, p.scale,
       p.scale * kLog2e, err, wait_limit_ns());
   return cudaGetLastError();
 }

@@ -330,6 +330,8 @@ __global__ void __launch_bounds__(320, 1)
   }
 
   // ------------------------------------------------------------ teardown
+  // Reconverge single-lane roles first: __syncthreads is an aligned barrier.
+  __syncwarp();
   tc_fence_before();
   __syncthreads();
   if (warp == 0) {
