@@ -41,7 +41,7 @@ namespace {
 
 using namespace mg_tc;
 
-template <int DP>
+template <int DP, bool FUSED_DQ>
 struct BwdCfg {
   static constexpr int BN = 128;                    // keys per CTA
   static constexpr int BQ = DP == 128 ? 64 : 128;   // queries per block
@@ -55,10 +55,10 @@ struct BwdCfg {
   static constexpr int DS_CHUNK = BN * 128;         // [128 keys][64 q] bf16
   static constexpr int NQC = BQ / 64;               // dS^T chunks
   static constexpr int DS_BUF = NQC * DS_CHUNK;
-  static constexpr int NQS = 3;                     // Q/dO ring stages
-  static constexpr int NDS = DP == 128 ? 2 : 1;     // dS^T smem buffers
+  static constexpr int NQS = FUSED_DQ ? 3 : 4;      // Q/dO ring stages
+  static constexpr int NDS = FUSED_DQ ? (DP == 128 ? 2 : 1) : 0;  // dS^T smem buffers
   static constexpr int DQ_BOX = BQ * 128;           // [BQ][32] f32
-  static constexpr int DQ_STAGE = (DP / 32) * DQ_BOX;
+  static constexpr int DQ_STAGE = FUSED_DQ ? (DP / 32) * DQ_BOX : 0;
   // shared memory
   static constexpr int OFF_K = 0;
   static constexpr int OFF_V = OFF_K + KV_TILE;
@@ -70,18 +70,18 @@ struct BwdCfg {
   static constexpr int OFF_DV = OFF_LSE + NQS * BQ * 4;        // NQS stages x BQ f32
   static constexpr int OFF_BAR = OFF_DV + NQS * BQ * 4;
   static constexpr int B_KVFULL = 0;
-  static constexpr int B_QFULL = 1;      // NQS (Q/dO stage)
-  static constexpr int B_QEMPTY = 4;     // NQS
-  static constexpr int B_SFULL = 7;
-  static constexpr int B_PREADY = 8;
-  static constexpr int B_DPFULL = 9;     // 2 (dP buffer)
-  static constexpr int B_DSREADY = 11;   // 2 (block parity)
-  static constexpr int B_DSMFREE = 13;   // NDS
-  static constexpr int B_DQFULL = 15;
-  static constexpr int B_DQEMPTY = 16;
-  static constexpr int B_ACCDONE = 17;
-  static constexpr int B_DRAIN = 18;
-  static constexpr int NBAR = 19;
+  static constexpr int B_QFULL = 1;                  // NQS (Q/dO stage)
+  static constexpr int B_QEMPTY = B_QFULL + 4;       // NQS
+  static constexpr int B_SFULL = B_QEMPTY + 4;
+  static constexpr int B_PREADY = B_SFULL + 1;
+  static constexpr int B_DPFULL = B_PREADY + 1;      // 2 (dP buffer)
+  static constexpr int B_DSREADY = B_DPFULL + 2;     // 2 (block parity)
+  static constexpr int B_DSMFREE = B_DSREADY + 2;    // 2 (dS smem buffer)
+  static constexpr int B_DQFULL = B_DSMFREE + 2;
+  static constexpr int B_DQEMPTY = B_DQFULL + 1;
+  static constexpr int B_ACCDONE = B_DQEMPTY + 1;
+  static constexpr int B_DRAIN = B_ACCDONE + 1;
+  static constexpr int NBAR = B_DRAIN + 1;
   static constexpr int OFF_MISC = OFF_BAR + NBAR * 8;
   static constexpr int SMEM_BYTES = OFF_MISC + 16 + 1024;
   static constexpr int NTHREADS = 512;
@@ -125,7 +125,7 @@ __device__ __forceinline__ uint32_t dq_stage_off(int row, int col, int box_bytes
                                ((col & 3) << 2));
 }
 
-template <int DP>
+template <int DP, bool FUSED_DQ>
 __global__ void __launch_bounds__(512, 1)
     accel_dkdv_kernel(const __grid_constant__ CUtensorMap tmQ,
                       const __grid_constant__ CUtensorMap tmK,
@@ -136,7 +136,7 @@ __global__ void __launch_bounds__(512, 1)
                       float *__restrict__ dK,
                       float *__restrict__ dV, int BH, int L, int D, int causal, float scale,
                       float scale_log2, unsigned int *err, unsigned long long timeout_ns) {
-  using C = BwdCfg<DP>;
+  using C = BwdCfg<DP, FUSED_DQ>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                               ~static_cast<uintptr_t>(1023));
@@ -166,7 +166,7 @@ __global__ void __launch_bounds__(512, 1)
   if (threadIdx.x == 128) {
     for (int i = 0; i < C::NBAR; ++i) {
       uint32_t cnt = 1;
-      if (i >= C::B_QEMPTY && i < C::B_QEMPTY + C::NQS) cnt = 1 + 8;
+      if (i >= C::B_QEMPTY && i < C::B_QEMPTY + 4) cnt = 1 + 8;
       if (i == C::B_PREADY || i == C::B_DSREADY || i == C::B_DSREADY + 1) cnt = 8;
       if (i == C::B_DQEMPTY) cnt = 4;
       mbar_init(bar(i), cnt);
@@ -290,9 +290,10 @@ __global__ void __launch_bounds__(512, 1)
         issue_acc(tmem + C::T_DP + db * C::BQ, sbase + C::OFF_Q + st * C::Q_TILE,
                   tmem + C::T_DK, i == 0);
         mma_commit(bar(C::B_QEMPTY + st));
+        if (FUSED_DQ) {
         if (i > 0 && !(ok = mbar_wait(bar(C::B_DQEMPTY), (i - 1) & 1, ab))) break;
         tc_fence_after();
-        const uint32_t sDSi = sDS + (i % C::NDS) * C::DS_BUF;
+        const uint32_t sDSi = sDS + (i % (C::NDS > 0 ? C::NDS : 1)) * C::DS_BUF;
 #pragma unroll
         for (int kk = 0; kk < C::BN / 16; ++kk) {
           if (DP == 128) {
@@ -306,7 +307,8 @@ __global__ void __launch_bounds__(512, 1)
           }
         }
         mma_commit(bar(C::B_DQFULL));
-        mma_commit(bar(C::B_DSMFREE + i % C::NDS));
+        mma_commit(bar(C::B_DSMFREE + i % (C::NDS > 0 ? C::NDS : 1)));
+        }
         if (C::ND == 1 && i + 1 < n && !(ok = issue_dP(i + 1))) break;
       }
       mma_commit(bar(C::B_ACCDONE));
@@ -318,7 +320,7 @@ __global__ void __launch_bounds__(512, 1)
     const int t = threadIdx.x;  // TMEM lane: d (D = 128) or query row (D = 64)
     const uint32_t lane_off = static_cast<uint32_t>(32 * warp) << 16;
     const uint32_t stage = sbase + C::OFF_DQ;
-    for (int i = 0; i < n; ++i) {
+    for (int i = 0; FUSED_DQ && i < n; ++i) {
       if (!mbar_wait_warp(bar(C::B_DQFULL), i & 1, ab)) break;
       tc_fence_after();
       uint32_t r[64];
@@ -365,7 +367,7 @@ __global__ void __launch_bounds__(512, 1)
         bulk_commit_group();
       }
     }
-    if (t == 0) bulk_wait_group0();
+    if (FUSED_DQ && t == 0) bulk_wait_group0();
   } else if (warp >= 8) {
     // ------------------------------------------------------------ softmax warpgroups
     const int g = (warp - 8) >> 2;
@@ -424,11 +426,12 @@ __global__ void __launch_bounds__(512, 1)
       if (!(ok = mbar_wait_warp(bar(C::B_DPFULL + db), (C::ND == 2 ? (i >> 1) : i) & 1, ab)))
         break;
       // this dS staging tile is free once dQ(i - NDS) has completed
-      if (i >= C::NDS &&
-          !(ok = mbar_wait_warp(bar(C::B_DSMFREE + i % C::NDS), ((i / C::NDS) - 1) & 1, ab)))
+      constexpr int NDS1 = C::NDS > 0 ? C::NDS : 1;
+      if (FUSED_DQ && i >= NDS1 &&
+          !(ok = mbar_wait_warp(bar(C::B_DSMFREE + i % NDS1), ((i / NDS1) - 1) & 1, ab)))
         break;
       tc_fence_after();
-      const uint32_t sDSi = sDS + (i % C::NDS) * C::DS_BUF;
+      const uint32_t sDSi = sDS + (i % NDS1) * C::DS_BUF;
 #pragma unroll
       for (int c = 0; c < C::QPW / 32; ++c) {
         uint32_t r[32];
@@ -449,6 +452,7 @@ __global__ void __launch_bounds__(512, 1)
         }
         tmem_st16(tDP + 16 * c, pk);
         // dS^T row kr, queries ql .. ql+31 into the swizzled smem tile
+        if (!FUSED_DQ) continue;
         const int ql = g * C::QPW + 32 * c;
         const uint32_t chunk = sDSi + (ql >> 6) * C::DS_CHUNK + kr * 128;
 #pragma unroll
@@ -459,7 +463,7 @@ __global__ void __launch_bounds__(512, 1)
         }
       }
       tmem_wait_st();
-      fence_proxy_async_smem();
+      if (FUSED_DQ) fence_proxy_async_smem();
       tc_fence_before();
       __syncwarp();
       if (lane == 0) {
@@ -516,12 +520,12 @@ uint64_t wait_limit_ns() {
   return v;
 }
 
-template <int DP>
+template <int DP, bool FUSED_DQ>
 cudaError_t launch(const __nv_bfloat16 *Q, const __nv_bfloat16 *K, const __nv_bfloat16 *V,
                    const __nv_bfloat16 *dO, const float *LSE, const float *Dvec, float *dQ,
                    float *dK, float *dV, const MgProblem &p, unsigned int *err,
                    cudaStream_t st) {
-  using C = BwdCfg<DP>;
+  using C = BwdCfg<DP, FUSED_DQ>;
   const int BH = p.B * p.H;
   CUtensorMap tq, tk, tv, tdo, tdq;
   cudaError_t e;
@@ -530,9 +534,9 @@ cudaError_t launch(const __nv_bfloat16 *Q, const __nv_bfloat16 *K, const __nv_bf
   if ((e = mg_tmap_bf16(&tk, K, p.D, p.L, BH, C::BN)) != cudaSuccess) return e;
   if ((e = mg_tmap_bf16(&tv, V, p.D, p.L, BH, C::BN)) != cudaSuccess) return e;
   if ((e = mg_tmap_f32(&tdq, dQ, p.D, p.L, BH, C::BQ)) != cudaSuccess) return e;
-  auto kern = accel_dkdv_kernel<DP>;
+  auto kern = accel_dkdv_kernel<DP, FUSED_DQ>;
   if ((e = mg_set_smem_attr(reinterpret_cast<const void *>(kern), C::SMEM_BYTES,
-                            DP == 64 ? 8 : 9)) != cudaSuccess)
+                            (DP == 64 ? 8 : 9) + (FUSED_DQ ? 0 : 4))) != cudaSuccess)
     return e;
   const int nkb = (p.L + C::BN - 1) / C::BN;
   const long long grid = static_cast<long long>(nkb) * BH;
@@ -549,6 +553,11 @@ cudaError_t mg_launch_accel_dkdv(const __nv_bfloat16 *Q, const __nv_bfloat16 *K,
                                  const float *LSE, const float *Dvec, float *dQ, float *dK,
                                  float *dV, const MgProblem &p, unsigned int *err,
                                  cudaStream_t st) {
-  if (p.D <= 64) return launch<64>(Q, K, V, dO, LSE, Dvec, dQ, dK, dV, p, err, st);
-  return launch<128>(Q, K, V, dO, LSE, Dvec, dQ, dK, dV, p, err, st);
+  if (dQ) {  // fused: dQ added into a zeroed dQ with TMA reductions
+    if (p.D <= 64) return launch<64, true>(Q, K, V, dO, LSE, Dvec, dQ, dK, dV, p, err, st);
+    return launch<128, true>(Q, K, V, dO, LSE, Dvec, dQ, dK, dV, p, err, st);
+  }
+  // dK and dV only (dQ comes from the separate dQ pass)
+  if (p.D <= 64) return launch<64, false>(Q, K, V, dO, LSE, Dvec, dK, dK, dV, p, err, st);
+  return launch<128, false>(Q, K, V, dO, LSE, Dvec, dK, dK, dV, p, err, st);
 }

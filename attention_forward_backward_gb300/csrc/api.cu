@@ -7,6 +7,7 @@
 // allocate nothing while a step runs; the calls here follow the same rule:
 // they validate, then enqueue kernels on the caller's stream.
 #include <math.h>
+#include <stdlib.h>
 #include <string.h>
 
 #include <mutex>
@@ -81,8 +82,19 @@ void prof_free() {
 }
 
 const char *const kKernelNames[MGK_COUNT] = {
-    "strict_fwd", "strict_dvec", "strict_dkdv_dq", "accel_fwd",
-    "accel_dvec", "accel_dkdv_dq", "dq_zero"};
+    "strict_fwd", "strict_dvec", "strict_dkdv_dq", "accel_fwd",     "accel_dvec",
+    "accel_dkdv_dq", "dq_zero",  "accel_dkdv",    "accel_dq"};
+
+// How the ACCEL backward produces dQ: f32 TMA reductions from the fused dK/dV
+// kernel (default, measured faster on GB300) or a separate dQ pass that
+// recomputes S and dP per query block (MG_DQ_MODE=pass). Read once.
+bool accel_dq_atomic() {
+  static const bool v = [] {
+    const char *e = getenv("MG_DQ_MODE");
+    return !(e && strcmp(e, "pass") == 0);
+  }();
+  return v;
+}
 
 // ---------------------------------------------------------------- validation
 bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
@@ -250,16 +262,29 @@ int mg_attn_bwd(const void *Q, const void *K, const void *V, const void *O, cons
                               static_cast<const __nv_bfloat16 *>(dO), Dvec, p, st);
     }
     if (e != cudaSuccess) return MG_ERR_CUDA;
-    {
-      ProfScope ps(MGK_DQ_ZERO, st);
-      e = cudaMemsetAsync(dQ, 0, n * 4, st);
+    const __nv_bfloat16 *q = static_cast<const __nv_bfloat16 *>(Q);
+    const __nv_bfloat16 *k = static_cast<const __nv_bfloat16 *>(K);
+    const __nv_bfloat16 *v = static_cast<const __nv_bfloat16 *>(V);
+    const __nv_bfloat16 *d = static_cast<const __nv_bfloat16 *>(dO);
+    if (accel_dq_atomic()) {
+      {
+        ProfScope ps(MGK_DQ_ZERO, st);
+        e = cudaMemsetAsync(dQ, 0, n * 4, st);
+      }
+      if (e != cudaSuccess) return MG_ERR_CUDA;
+      ProfScope ps(MGK_ACCEL_DKDV_DQ, st);
+      e = mg_launch_accel_dkdv(q, k, v, d, LSE, Dvec, static_cast<float *>(dQ),
+                               static_cast<float *>(dK), static_cast<float *>(dV), p, err, st);
+    } else {
+      {
+        ProfScope ps(MGK_ACCEL_DKDV, st);
+        e = mg_launch_accel_dkdv(q, k, v, d, LSE, Dvec, nullptr, static_cast<float *>(dK),
+                                 static_cast<float *>(dV), p, err, st);
+      }
+      if (e != cudaSuccess) return MG_ERR_CUDA;
+      ProfScope ps(MGK_ACCEL_DQ, st);
+      e = mg_launch_accel_dq(q, k, v, d, LSE, Dvec, static_cast<float *>(dQ), p, err, st);
     }
-    if (e != cudaSuccess) return MG_ERR_CUDA;
-    ProfScope ps(MGK_ACCEL_DKDV, st);
-    e = mg_launch_accel_dkdv(
-        static_cast<const __nv_bfloat16 *>(Q), static_cast<const __nv_bfloat16 *>(K),
-        static_cast<const __nv_bfloat16 *>(V), static_cast<const __nv_bfloat16 *>(dO), LSE, Dvec,
-        static_cast<float *>(dQ), static_cast<float *>(dK), static_cast<float *>(dV), p, err, st);
   }
   return map_cuda(e);
 }

@@ -19,9 +19,11 @@ enum MgKernelId {
   MGK_STRICT_DKDV = 2,
   MGK_ACCEL_FWD = 3,
   MGK_ACCEL_DVEC = 4,
-  MGK_ACCEL_DKDV = 5,
+  MGK_ACCEL_DKDV_DQ = 5,  // fused dK/dV kernel that also adds dQ (atomic mode)
   MGK_DQ_ZERO = 6,
-  MGK_COUNT = 7
+  MGK_ACCEL_DKDV = 7,     // dK/dV kernel of the two-pass backward
+  MGK_ACCEL_DQ = 8,       // dQ pass of the two-pass backward
+  MGK_COUNT = 9
 };
 
 // Device error codes written into the device error word by bounded waits.
@@ -45,6 +47,8 @@ cudaError_t mg_launch_dvec_bf16(const float *O, const __nv_bfloat16 *dO, float *
                                 const MgProblem &p, cudaStream_t st);
 
 // ACCEL_BF16 (tcgen05 / TMEM / TMA) kernels. `err` is the device error word.
+// mg_launch_accel_dkdv: with dQ != nullptr the fused kernel also adds dQ into
+// (zeroed) dQ; with dQ == nullptr it computes dK and dV only.
 cudaError_t mg_launch_accel_fwd(const __nv_bfloat16 *Q, const __nv_bfloat16 *K,
                                 const __nv_bfloat16 *V, float *O, float *LSE,
                                 const MgProblem &p, unsigned int *err, cudaStream_t st);
@@ -56,3 +60,9 @@ cudaError_t mg_launch_accel_dkdv(const __nv_bfloat16 *Q, const __nv_bfloat16 *K,
 
 // Opt a kernel into more than 48 KB of dynamic shared memory once per device.
 cudaError_t mg_set_smem_attr(const void *func, int bytes, int slot);
+
+// ACCEL_BF16 dQ pass (one CTA per 128-row query block; dQ stored, not reduced).
+cudaError_t mg_launch_accel_dq(const __nv_bfloat16 *Q, const __nv_bfloat16 *K,
+                               const __nv_bfloat16 *V, const __nv_bfloat16 *dO, const float *LSE,
+                               const float *Dvec, float *dQ, const MgProblem &p,
+                               unsigned int *err, cudaStream_t st);

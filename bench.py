@@ -150,6 +150,17 @@ def make_inputs(w, contract, torch, device):
     return host, dev
 
 
+def kernel_matmul_flops(name: str, w) -> float | None:
+    """Matmul flops one launch of kernel `name` performs (2 B H L^2 D per L x L x D
+    product, halved when causal): forward 2 products; fused dK/dV/dQ kernel 5;
+    dK/dV kernel of the two-pass backward 4 (S, dP, dV, dK); dQ pass 3 (S, dP,
+    dQ: S and dP are recomputed, which the flops convention does not credit)."""
+    unit = w.flops_fwd() / 2.0
+    table = {"strict_fwd": 2, "accel_fwd": 2, "strict_dkdv_dq": 5, "accel_dkdv_dq": 5,
+             "accel_dkdv": 4, "accel_dq": 3}
+    return table[name] * unit if name in table else None
+
+
 def run_contract(mg, torch, w, contract, args, device, stream, peaks, sm_count, clocks):
     host, dev = make_inputs(w, contract, torch, device)
     B, H, L, D = w.shape
@@ -225,12 +236,7 @@ def run_contract(mg, torch, w, contract, args, device, stream, peaks, sm_count, 
     # roofline of the dominant kernel (largest total time)
     dom = max(per_kernel.items(), key=lambda kv: kv[1]["launches"] * kv[1]["avg_ms"])
     name, st = dom
-    if name.endswith("fwd"):
-        alg = w.flops_fwd()
-    elif "dkdv" in name:
-        alg = w.flops_bwd()
-    else:
-        alg = None
+    alg = kernel_matmul_flops(name, w)
     if contract == "accel":
         peak = peaks["bf16_tflops"]
         bound, peak_note = "tensor", f"bf16 dense, {peaks['source']} (cuBLAS burst)"
@@ -245,7 +251,10 @@ def run_contract(mg, torch, w, contract, args, device, stream, peaks, sm_count, 
                        "peak_source": peak_note,
                        "algorithmic_flops_per_launch": alg}
     res["frac_of_peak_fwd_bwd"] = res["fwd_bwd_tflops"] / ws_n / peak
-    res["gpu_launches_per_step"] = 3  # fwd, Dvec, dK/dV/dQ (+ one cudaMemsetAsync of dQ)
+    # our kernels per step: fwd, Dvec, then dK/dV + dQ pass (or the fused kernel,
+    # which then also needs one cudaMemsetAsync of dQ)
+    res["gpu_launches_per_step"] = sum(v["launches"] for k, v in per_kernel.items()
+                                       if k != "dq_zero") // args.steps
 
     if not args.no_e2e:
         res["e2e"] = run_e2e(mg, torch, w, contract, args, host, device, stream, flops_step)
@@ -408,6 +417,7 @@ def main():
                    "contract": "ACCEL_BF16" if head == "accel" else "STRICT_F32",
                    "flops_convention": "fwd 4BHL^2D, bwd 2.5x fwd, causal x1/2",
                    "l2": "flushed between timed steps (512 MiB write outside the events)",
+                   "dq_mode": os.environ.get("MG_DQ_MODE", "atomic"),
                    "parallelism": f"replica per GPU x{world()} (heads independent)"},
         "roofline": r["roofline"],
         "clocks": r["clocks"],

@@ -100,9 +100,12 @@ size_t mg_attn_bwd_workspace_bytes(int B, int H, int L, int D, int contract);
  *   dQ, dK, dV   out  [B][H][L][D] f32, overwritten (never accumulated into)
  *   workspace    scratch of at least mg_attn_bwd_workspace_bytes() bytes,
  *                16-byte aligned; its contents on entry do not matter
- * Steps on the stream: Dvec = rowsum(dO * O); dQ zeroed; one kernel per key
- * block recomputes P from Q, K, LSE and accumulates dK, dV in place while
- * adding its dQ contribution with f32 reductions.
+ * Steps on the stream: Dvec = rowsum(dO * O) into the workspace; then one
+ * kernel per key block recomputes P from Q, K, LSE and accumulates dK, dV.
+ * STRICT and the default ACCEL mode add each key block's dQ contribution into
+ * a zeroed dQ with f32 reductions (results not bitwise reproducible); with the
+ * environment variable MG_DQ_MODE=pass (read once per process) ACCEL instead
+ * runs a separate dQ pass over query blocks that stores dQ without atomics.
  */
 int mg_attn_bwd(const void *Q, const void *K, const void *V, const void *O,
                 const void *dO, const float *LSE, void *dQ, void *dK, void *dV,

@@ -95,3 +95,33 @@ def test_accel_repeatable_forward():
     b = run_gpu(dev, True, w.scale, "accel", bwd=False)
     np.testing.assert_array_equal(a["O"], b["O"])
     np.testing.assert_array_equal(a["LSE"], b["LSE"])
+
+
+def test_accel_pass_dq_mode_in_child():
+    """The two-pass backward (dK/dV kernel + separate dQ pass, MG_DQ_MODE=pass)
+    on cfg 2, cfg 3 and a ragged D = 128 case, in a child process because the
+    mode is read once per process."""
+    import os
+    import subprocess
+    import sys
+    import textwrap
+    root = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+    code = textwrap.dedent(f"""
+        import sys
+        sys.path.insert(0, {root!r}); sys.path.insert(0, {os.path.join(root, 'tests')!r})
+        import oracle
+        from attention_forward_backward_gb300 import synth
+        from parity_util import compare, device_inputs, run_gpu
+        for w in (synth.WORKLOADS[2], synth.WORKLOADS[3],
+                  synth.custom_workload(1, 3, 300, 128, True, seed_cfg=990)):
+            dev, vals = device_inputs(synth.inputs(w, "accel"), "accel")
+            got = run_gpu(dev, w.causal, w.scale, "accel")
+            ref = oracle.attn_bwd(vals["Q"], vals["K"], vals["V"], vals["dO"], w.causal, w.scale)
+            errs, bad = compare(got, ref, "accel")
+            assert not bad, (w.name, errs)
+        print("PASS-MODE-OK")
+    """)
+    env = dict(os.environ, MG_DQ_MODE="pass")
+    res = subprocess.run([sys.executable, "-c", code], env=env, capture_output=True, text=True,
+                         timeout=600)
+    assert res.returncode == 0 and "PASS-MODE-OK" in res.stdout, res.stdout + res.stderr
