@@ -41,9 +41,13 @@ UNIT = "TFLOP/s"
 L2_FLUSH_BYTES = 512 << 20  # > 129 MB L2
 
 # dram__bytes_read.sum + dram__bytes_write.sum per launch of the dominant
-# kernel, from the ncu capture summarised in profiles/ (None once the kernel
-# changed since the capture).
-NCU_TRAFFIC_BYTES = {}
+# kernel at the benchmark workload (cfg 5), from the ncu captures summarised in
+# profiles/ (taken on half of the heads and scaled by 2; per-head traffic is
+# identical). Remove an entry when its kernel changes.
+NCU_TRAFFIC_BYTES = {
+    ("accel_dkdv_dq", 5): 2 * (404.828672e6 + 349.318912e6),
+    ("accel_fwd", 5): 2 * (546.099712e6 + 99.816192e6),
+}
 
 
 def parse():
