@@ -14,8 +14,9 @@
 //   over the first 64 columns of S_q). Issue order S_A S_B PV_A S_A' PV_B S_B'
 //   ... lets one softmax warpgroup work while the tensor core serves the other.
 // * Warps 0-3 and 4-7 are the softmax warpgroups of tiles A and B: one thread
-//   per query row (its TMEM lane). Online softmax in base 2 with log2(e) folded
-//   into the scale. The running reference max only moves when a row max grows
+//   per query row (its TMEM lane), all 128 scores of a tile loaded with a
+//   single TMEM wait. Online softmax in base 2 with log2(e) folded into the
+//   scale. The running reference max only moves when a row max grows
 //   by more than 8 (a factor 256 in P); O in TMEM is then rescaled after the
 //   previous P V finished. Any reference max gives the same exact result once
 //   O is divided by the row sum taken against that same max.
@@ -240,23 +241,34 @@ __global__ void __launch_bounds__(320, 1)
       const int k0 = j * C::BN;
       const bool need_mask = (k0 + C::BN > L) || (causal && k0 + C::BN - 1 > q0 + q * C::BM);
       const int lim = causal ? min(L - 1, qrow) : (L - 1);  // last allowed key of this row
-      // pass 1: row max of the raw scores
-      float mx = -INFINITY;
+      // One pass: all 128 scores of the row in flight, a single wait.
+      uint32_t r[128];
 #pragma unroll
-      for (int c = 0; c < 4; ++c) {
-        uint32_t r[32];
-        tmem_ld32(tS + 32 * c, r);
-        tmem_wait_ld();
+      for (int c = 0; c < 4; ++c) tmem_ld32(tS + 32 * c, *reinterpret_cast<uint32_t(*)[32]>(r + 32 * c));
+      tmem_wait_ld();
+      if (need_mask) {
 #pragma unroll
-        for (int e = 0; e < 32; ++e) {
-          const float v = (need_mask && k0 + 32 * c + e > lim) ? -INFINITY : __uint_as_float(r[e]);
-          mx = fmaxf(mx, v);
-        }
+        for (int e = 0; e < 128; ++e)
+          if (k0 + e > lim) r[e] = __float_as_uint(-INFINITY);
       }
+      float mx = __uint_as_float(r[0]);
+#pragma unroll
+      for (int e = 1; e < 128; ++e) mx = fmaxf(mx, __uint_as_float(r[e]));
       const float mx2 = mx * scale_log2;
       const bool need = mx2 > m_ref + 8.f;
-      if (__any_sync(0xffffffffu, need)) {
-        const float m_new = fmaxf(m_ref, mx2);
+      const bool warp_need = __any_sync(0xffffffffu, need);
+      const float m_new = warp_need ? fmaxf(m_ref, mx2) : m_ref;
+      // P = exp2(s * scale * log2e - m_new), packed to bf16 (masked scores are -inf -> 0)
+      uint32_t pk[64];
+      float rs = 0.f;
+#pragma unroll
+      for (int e = 0; e < 64; ++e) {
+        const float p0 = ex2(fmaf(__uint_as_float(r[2 * e]), scale_log2, -m_new));
+        const float p1 = ex2(fmaf(__uint_as_float(r[2 * e + 1]), scale_log2, -m_new));
+        rs += p0 + p1;
+        pk[e] = pack_bf16(p0, p1);
+      }
+      if (warp_need) {
         const float alpha = ex2(m_ref - m_new);
         if (j > 0) {
           // O holds the sum up to tile j-1: wait for that P V, then rescale.
@@ -265,40 +277,20 @@ __global__ void __launch_bounds__(320, 1)
           tc_fence_after();
 #pragma unroll
           for (int c = 0; c < DP / 32; ++c) {
-            uint32_t r[32];
-            tmem_ld32(tO + 32 * c, r);
+            uint32_t o[32];
+            tmem_ld32(tO + 32 * c, o);
             tmem_wait_ld();
 #pragma unroll
-            for (int e = 0; e < 32; ++e) r[e] = __float_as_uint(__uint_as_float(r[e]) * alpha);
-            tmem_st32(tO + 32 * c, r);
+            for (int e = 0; e < 32; ++e) o[e] = __float_as_uint(__uint_as_float(o[e]) * alpha);
+            tmem_st32(tO + 32 * c, o);
           }
         }
         l *= alpha;
         m_ref = m_new;
       }
-      // pass 2: P = exp2(s * scale * log2e - m_ref), packed to bf16 in place over
-      // the first 64 columns of S (chunk c only overwrites columns already read).
-      float rs = 0.f;
-#pragma unroll
-      for (int c = 0; c < 4; ++c) {
-        uint32_t r[32];
-        tmem_ld32(tS + 32 * c, r);
-        tmem_wait_ld();
-        uint32_t pk[16];
-#pragma unroll
-        for (int e = 0; e < 16; ++e) {
-          const int kc = k0 + 32 * c + 2 * e;
-          float p0 = ex2(fmaf(__uint_as_float(r[2 * e]), scale_log2, -m_ref));
-          float p1 = ex2(fmaf(__uint_as_float(r[2 * e + 1]), scale_log2, -m_ref));
-          if (need_mask) {
-            if (kc > lim) p0 = 0.f;
-            if (kc + 1 > lim) p1 = 0.f;
-          }
-          rs += p0 + p1;
-          pk[e] = pack_bf16(p0, p1);
-        }
-        tmem_st16(tS + 16 * c, pk);
-      }
+      // P over the first 64 columns of S (all of S has been read)
+      tmem_st32(tS, *reinterpret_cast<uint32_t(*)[32]>(pk));
+      tmem_st32(tS + 32, *reinterpret_cast<uint32_t(*)[32]>(pk + 32));
       l += rs;
       tmem_wait_st();
       tc_fence_before();
