@@ -41,7 +41,7 @@ namespace {
 
 using namespace mg_tc;
 
-template <int DP, bool FUSED_DQ>
+template <int DP>
 struct BwdCfg {
   static constexpr int BN = 128;                    // keys per CTA
   static constexpr int BQ = DP == 128 ? 64 : 128;   // queries per block
@@ -55,10 +55,10 @@ struct BwdCfg {
   static constexpr int DS_CHUNK = BN * 128;         // [128 keys][64 q] bf16
   static constexpr int NQC = BQ / 64;               // dS^T chunks
   static constexpr int DS_BUF = NQC * DS_CHUNK;
-  static constexpr int NQS = FUSED_DQ ? 3 : 4;      // Q/dO ring stages
-  static constexpr int NDS = FUSED_DQ ? (DP == 128 ? 2 : 1) : 0;  // dS^T smem buffers
+  static constexpr int NQS = 3;                     // Q/dO ring stages
+  static constexpr int NDS = DP == 128 ? 2 : 1;     // dS^T smem buffers
   static constexpr int DQ_BOX = BQ * 128;           // [BQ][32] f32
-  static constexpr int DQ_STAGE = FUSED_DQ ? (DP / 32) * DQ_BOX : 0;
+  static constexpr int DQ_STAGE = (DP / 32) * DQ_BOX;
   // shared memory
   static constexpr int OFF_K = 0;
   static constexpr int OFF_V = OFF_K + KV_TILE;
@@ -125,7 +125,7 @@ __device__ __forceinline__ uint32_t dq_stage_off(int row, int col, int box_bytes
                                ((col & 3) << 2));
 }
 
-template <int DP, bool FUSED_DQ>
+template <int DP>
 __global__ void __launch_bounds__(512, 1)
     accel_dkdv_kernel(const __grid_constant__ CUtensorMap tmQ,
                       const __grid_constant__ CUtensorMap tmK,
@@ -136,7 +136,7 @@ __global__ void __launch_bounds__(512, 1)
                       float *__restrict__ dK,
                       float *__restrict__ dV, int BH, int L, int D, int causal, float scale,
                       float scale_log2, unsigned int *err, unsigned long long timeout_ns) {
-  using C = BwdCfg<DP, FUSED_DQ>;
+  using C = BwdCfg<DP>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                               ~static_cast<uintptr_t>(1023));
@@ -184,7 +184,7 @@ __global__ void __launch_bounds__(512, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
-  const Abort ab{abort_flag, err, timeout_ns};
+  const Abort ab = make_abort(abort_flag, err, timeout_ns);
 
   if (warp == 4) {
     // ------------------------------------------------------------ producer
@@ -233,7 +233,16 @@ __global__ void __launch_bounds__(512, 1)
       constexpr uint32_t idDQ =
           DP == 128 ? idesc_bf16_f32(128, C::BQ, true, true) : idesc_bf16_f32(128, DP, true, true);
       bool ok = mbar_wait(bar(C::B_KVFULL), 0, ab);
-      const uint32_t sK = sbase + C::OFF_K, sV = sbase + C::OFF_V, sDS = sbase + C::OFF_DS;
+      // base descriptors; each MMA adds a compile-time byte offset
+      const uint32_t sb = opaque_u32(sbase);
+      const uint64_t dK0 = sdesc_sw128(sb + C::OFF_K, 0, 1024);
+      const uint64_t dV0 = sdesc_sw128(sb + C::OFF_V, 0, 1024);
+      const uint64_t dQ0 = sdesc_sw128(sb + C::OFF_Q, 0, 1024);
+      const uint64_t dO0 = sdesc_sw128(sb + C::OFF_DO, 0, 1024);
+      const uint64_t dQmn = sdesc_sw128(sb + C::OFF_Q, C::BOX_Q, 1024);
+      const uint64_t dOmn = sdesc_sw128(sb + C::OFF_DO, C::BOX_Q, 1024);
+      const uint64_t dKmn = sdesc_sw128(sb + C::OFF_K, C::BOX_KV, 1024);
+      const uint64_t dDSmn = sdesc_sw128(sb + C::OFF_DS, C::DS_CHUNK, 1024);
       int qwaited = -1;
       auto wait_q = [&](int i) -> bool {
         if (qwaited >= i) return true;
@@ -241,19 +250,20 @@ __global__ void __launch_bounds__(512, 1)
         return mbar_wait(bar(C::B_QFULL + i % C::NQS), (i / C::NQS) & 1, ab);
       };
       // X^T = A_tile * B_i^T with A in {K, V}, B_i in {Q_i, dO_i}; both K-major.
-      auto issue_T = [&](uint32_t sA, uint32_t sB, uint32_t d) {
+      auto issue_T = [&](uint64_t dA_, uint64_t dB_, uint32_t d) {
+        // opaque copies: the per-step descriptors are formed here, not hoisted
+        const uint64_t dA = opaque_u64(dA_), dB = opaque_u64(dB_);
 #pragma unroll
         for (int kk = 0; kk < DP / 16; ++kk) {
           const uint32_t oa = (kk >> 2) * C::BOX_KV + (kk & 3) * 32;
           const uint32_t ob = (kk >> 2) * C::BOX_Q + (kk & 3) * 32;
-          mma_ss(d, sdesc_sw128(sA + oa, 0, 1024), sdesc_sw128(sB + ob, 0, 1024), idSP,
-                 kk > 0 ? 1u : 0u);
+          mma_ss(d, sdesc_add(dA, oa), sdesc_add(dB, ob), idSP, kk > 0 ? 1u : 0u);
         }
       };
       auto issue_S = [&](int i) -> bool {
         if (!wait_q(i)) return false;
         tc_fence_after();
-        issue_T(sK, sbase + C::OFF_Q + (i % C::NQS) * C::Q_TILE, tmem + C::T_S);
+        issue_T(dK0, sdesc_add(dQ0, (i % C::NQS) * C::Q_TILE), tmem + C::T_S);
         mma_commit(bar(C::B_SFULL));
         return true;
       };
@@ -261,18 +271,19 @@ __global__ void __launch_bounds__(512, 1)
         if (!wait_q(i)) return false;
         tc_fence_after();
         const int db = C::ND == 2 ? (i & 1) : 0;
-        issue_T(sV, sbase + C::OFF_DO + (i % C::NQS) * C::Q_TILE, tmem + C::T_DP + db * C::BQ);
+        issue_T(dV0, sdesc_add(dO0, (i % C::NQS) * C::Q_TILE), tmem + C::T_DP + db * C::BQ);
         mma_commit(bar(C::B_DPFULL + db));
         return true;
       };
       // acc (+)= X^T(tmem, bf16) * Y_i (MN-major smem), K = BQ queries.
-      auto issue_acc = [&](uint32_t tA, uint32_t sY, uint32_t d, bool first) {
+      auto issue_acc = [&](uint32_t tA, uint64_t dY_, uint32_t d, bool first) {
+        const uint64_t dY = opaque_u64(dY_);
+        const uint32_t acc0 = first ? 0u : 1u;
 #pragma unroll
         for (int kk = 0; kk < C::BQ / 16; ++kk) {
           const int qq = 16 * kk;
           const uint32_t acol = (qq / C::QPW) * C::QPW + (qq % C::QPW) / 2;
-          mma_ts(d, tA + acol, sdesc_sw128(sY + kk * 2048, C::BOX_Q, 1024), idKV,
-                 (!first || kk > 0) ? 1u : 0u);
+          mma_ts(d, tA + acol, sdesc_add(dY, kk * 2048), idKV, kk > 0 ? 1u : acc0);
         }
       };
       if (ok) ok = issue_S(0);
@@ -282,33 +293,32 @@ __global__ void __launch_bounds__(512, 1)
         const int db = C::ND == 2 ? (i & 1) : 0;
         if (!(ok = mbar_wait(bar(C::B_PREADY), i & 1, ab))) break;
         tc_fence_after();
-        issue_acc(tmem + C::T_S, sbase + C::OFF_DO + st * C::Q_TILE, tmem + C::T_DV, i == 0);
+        issue_acc(tmem + C::T_S, sdesc_add(dOmn, st * C::Q_TILE), tmem + C::T_DV, i == 0);
         if (i + 1 < n && !(ok = issue_S(i + 1))) break;
         if (C::ND == 2 && i + 1 < n && !(ok = issue_dP(i + 1))) break;
         if (!(ok = mbar_wait(bar(C::B_DSREADY + (i & 1)), (i >> 1) & 1, ab))) break;
         tc_fence_after();
-        issue_acc(tmem + C::T_DP + db * C::BQ, sbase + C::OFF_Q + st * C::Q_TILE,
-                  tmem + C::T_DK, i == 0);
+        issue_acc(tmem + C::T_DP + db * C::BQ, sdesc_add(dQmn, st * C::Q_TILE), tmem + C::T_DK,
+                  i == 0);
         mma_commit(bar(C::B_QEMPTY + st));
-        if (FUSED_DQ) {
         if (i > 0 && !(ok = mbar_wait(bar(C::B_DQEMPTY), (i - 1) & 1, ab))) break;
         tc_fence_after();
-        const uint32_t sDSi = sDS + (i % (C::NDS > 0 ? C::NDS : 1)) * C::DS_BUF;
+        const uint64_t dDSi = opaque_u64(sdesc_add(dDSmn, (i % C::NDS) * C::DS_BUF));
+        const uint64_t dKq = opaque_u64(dKmn);
 #pragma unroll
         for (int kk = 0; kk < C::BN / 16; ++kk) {
           if (DP == 128) {
             // dQ^T [d][q] = K^T [d][key] * dS^T [key][q]
-            mma_ss(tmem + C::T_DQ, sdesc_sw128(sK + kk * 2048, C::BOX_KV, 1024),
-                   sdesc_sw128(sDSi + kk * 2048, C::DS_CHUNK, 1024), idDQ, kk > 0 ? 1u : 0u);
+            mma_ss(tmem + C::T_DQ, sdesc_add(dKq, kk * 2048), sdesc_add(dDSi, kk * 2048), idDQ,
+                   kk > 0 ? 1u : 0u);
           } else {
             // dQ [q][d] = dS [q][key] * K [key][d]
-            mma_ss(tmem + C::T_DQ, sdesc_sw128(sDSi + kk * 2048, C::DS_CHUNK, 1024),
-                   sdesc_sw128(sK + kk * 2048, C::BOX_KV, 1024), idDQ, kk > 0 ? 1u : 0u);
+            mma_ss(tmem + C::T_DQ, sdesc_add(dDSi, kk * 2048), sdesc_add(dKq, kk * 2048), idDQ,
+                   kk > 0 ? 1u : 0u);
           }
         }
         mma_commit(bar(C::B_DQFULL));
-        mma_commit(bar(C::B_DSMFREE + i % (C::NDS > 0 ? C::NDS : 1)));
-        }
+        mma_commit(bar(C::B_DSMFREE + i % C::NDS));
         if (C::ND == 1 && i + 1 < n && !(ok = issue_dP(i + 1))) break;
       }
       mma_commit(bar(C::B_ACCDONE));
@@ -320,7 +330,7 @@ __global__ void __launch_bounds__(512, 1)
     const int t = threadIdx.x;  // TMEM lane: d (D = 128) or query row (D = 64)
     const uint32_t lane_off = static_cast<uint32_t>(32 * warp) << 16;
     const uint32_t stage = sbase + C::OFF_DQ;
-    for (int i = 0; FUSED_DQ && i < n; ++i) {
+    for (int i = 0; i < n; ++i) {
       if (!mbar_wait_warp(bar(C::B_DQFULL), i & 1, ab)) break;
       tc_fence_after();
       uint32_t r[64];
@@ -367,7 +377,7 @@ __global__ void __launch_bounds__(512, 1)
         bulk_commit_group();
       }
     }
-    if (FUSED_DQ && t == 0) bulk_wait_group0();
+    if (t == 0) bulk_wait_group0();
   } else if (warp >= 8) {
     // ------------------------------------------------------------ softmax warpgroups
     const int g = (warp - 8) >> 2;
@@ -426,12 +436,11 @@ __global__ void __launch_bounds__(512, 1)
       if (!(ok = mbar_wait_warp(bar(C::B_DPFULL + db), (C::ND == 2 ? (i >> 1) : i) & 1, ab)))
         break;
       // this dS staging tile is free once dQ(i - NDS) has completed
-      constexpr int NDS1 = C::NDS > 0 ? C::NDS : 1;
-      if (FUSED_DQ && i >= NDS1 &&
-          !(ok = mbar_wait_warp(bar(C::B_DSMFREE + i % NDS1), ((i / NDS1) - 1) & 1, ab)))
+      if (i >= C::NDS &&
+          !(ok = mbar_wait_warp(bar(C::B_DSMFREE + i % C::NDS), ((i / C::NDS) - 1) & 1, ab)))
         break;
       tc_fence_after();
-      const uint32_t sDSi = sDS + (i % NDS1) * C::DS_BUF;
+      const uint32_t sDSi = sDS + (i % C::NDS) * C::DS_BUF;
 #pragma unroll
       for (int c = 0; c < C::QPW / 32; ++c) {
         uint32_t r[32];
@@ -452,7 +461,6 @@ __global__ void __launch_bounds__(512, 1)
         }
         tmem_st16(tDP + 16 * c, pk);
         // dS^T row kr, queries ql .. ql+31 into the swizzled smem tile
-        if (!FUSED_DQ) continue;
         const int ql = g * C::QPW + 32 * c;
         const uint32_t chunk = sDSi + (ql >> 6) * C::DS_CHUNK + kr * 128;
 #pragma unroll
@@ -463,7 +471,7 @@ __global__ void __launch_bounds__(512, 1)
         }
       }
       tmem_wait_st();
-      if (FUSED_DQ) fence_proxy_async_smem();
+      fence_proxy_async_smem();
       tc_fence_before();
       __syncwarp();
       if (lane == 0) {
@@ -520,12 +528,12 @@ uint64_t wait_limit_ns() {
   return v;
 }
 
-template <int DP, bool FUSED_DQ>
+template <int DP>
 cudaError_t launch(const __nv_bfloat16 *Q, const __nv_bfloat16 *K, const __nv_bfloat16 *V,
                    const __nv_bfloat16 *dO, const float *LSE, const float *Dvec, float *dQ,
                    float *dK, float *dV, const MgProblem &p, unsigned int *err,
                    cudaStream_t st) {
-  using C = BwdCfg<DP, FUSED_DQ>;
+  using C = BwdCfg<DP>;
   const int BH = p.B * p.H;
   CUtensorMap tq, tk, tv, tdo, tdq;
   cudaError_t e;
@@ -534,9 +542,9 @@ cudaError_t launch(const __nv_bfloat16 *Q, const __nv_bfloat16 *K, const __nv_bf
   if ((e = mg_tmap_bf16(&tk, K, p.D, p.L, BH, C::BN)) != cudaSuccess) return e;
   if ((e = mg_tmap_bf16(&tv, V, p.D, p.L, BH, C::BN)) != cudaSuccess) return e;
   if ((e = mg_tmap_f32(&tdq, dQ, p.D, p.L, BH, C::BQ)) != cudaSuccess) return e;
-  auto kern = accel_dkdv_kernel<DP, FUSED_DQ>;
+  auto kern = accel_dkdv_kernel<DP>;
   if ((e = mg_set_smem_attr(reinterpret_cast<const void *>(kern), C::SMEM_BYTES,
-                            (DP == 64 ? 8 : 9) + (FUSED_DQ ? 0 : 4))) != cudaSuccess)
+                            DP == 64 ? 8 : 9)) != cudaSuccess)
     return e;
   const int nkb = (p.L + C::BN - 1) / C::BN;
   const long long grid = static_cast<long long>(nkb) * BH;
@@ -553,11 +561,7 @@ cudaError_t mg_launch_accel_dkdv(const __nv_bfloat16 *Q, const __nv_bfloat16 *K,
                                  const float *LSE, const float *Dvec, float *dQ, float *dK,
                                  float *dV, const MgProblem &p, unsigned int *err,
                                  cudaStream_t st) {
-  if (dQ) {  // fused: dQ added into a zeroed dQ with TMA reductions
-    if (p.D <= 64) return launch<64, true>(Q, K, V, dO, LSE, Dvec, dQ, dK, dV, p, err, st);
-    return launch<128, true>(Q, K, V, dO, LSE, Dvec, dQ, dK, dV, p, err, st);
-  }
-  // dK and dV only (dQ comes from the separate dQ pass)
-  if (p.D <= 64) return launch<64, false>(Q, K, V, dO, LSE, Dvec, dK, dK, dV, p, err, st);
-  return launch<128, false>(Q, K, V, dO, LSE, Dvec, dK, dK, dV, p, err, st);
+  if (!dQ) return cudaErrorInvalidValue;  // dK/dV alone: mg_launch_accel_dkdv_pp
+  if (p.D <= 64) return launch<64>(Q, K, V, dO, LSE, Dvec, dQ, dK, dV, p, err, st);
+  return launch<128>(Q, K, V, dO, LSE, Dvec, dQ, dK, dV, p, err, st);
 }

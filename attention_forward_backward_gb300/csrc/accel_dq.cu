@@ -18,7 +18,8 @@
 // warps work on tile j+1; the issue order per tile is dQ(j), dP(j+1), S(j+2).
 // Warps 0-3 and 4-7 are two warpgroups splitting the 128 key columns of a tile
 // (64 each; thread = query row = TMEM lane); warp 8 is the TMA producer
-// (K, V ring), warp 9 issues the MMAs. Every wait is bounded.
+// (separate K and V rings, since K_j is needed until dQ(j) and V_j only until
+// dP(j)), warp 9 issues the MMAs. Every wait is bounded.
 #include "internal.h"
 #include "tc_common.cuh"
 #include "tmap.h"
@@ -123,7 +124,7 @@ __global__ void __launch_bounds__(320, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
-  const Abort ab{abort_flag, err, timeout_ns};
+  const Abort ab = make_abort(abort_flag, err, timeout_ns);
 
   if (warp == 8) {
     // ------------------------------------------------------------ TMA producer
@@ -162,29 +163,36 @@ __global__ void __launch_bounds__(320, 1)
     if (lane == 0) {
       constexpr uint32_t idSD = idesc_bf16_f32(128, C::BN, false, false);
       constexpr uint32_t idQ = idesc_bf16_f32(128, DP, false, true);
-      const uint32_t sQ = sbase + C::OFF_Q, sDO = sbase + C::OFF_DO;
+      // base descriptors; each MMA adds a compile-time byte offset
+      const uint32_t sb = opaque_u32(sbase);
+      const uint64_t dQ0 = sdesc_sw128(sb + C::OFF_Q, 0, 1024);
+      const uint64_t dO0 = sdesc_sw128(sb + C::OFF_DO, 0, 1024);
+      const uint64_t dK0 = sdesc_sw128(sb + C::OFF_K, 0, 1024);
+      const uint64_t dV0 = sdesc_sw128(sb + C::OFF_V, 0, 1024);
+      const uint64_t dKmn = sdesc_sw128(sb + C::OFF_K, C::BOX_KV, 1024);
       bool ok = mbar_wait(bar(C::B_QFULL), 0, ab);
       // X = A_res B_j^T with A_res in {Q, dO} resident and B_j in {K_j, V_j}; K-major.
-      auto issue_T = [&](uint32_t sA, uint32_t sB, uint32_t d) {
+      auto issue_T = [&](uint64_t dA_, uint64_t dB_, uint32_t d) {
+        // opaque copies: the per-step descriptors are formed here, not hoisted
+        const uint64_t dA = opaque_u64(dA_), dB = opaque_u64(dB_);
 #pragma unroll
         for (int kk = 0; kk < DP / 16; ++kk) {
           const uint32_t oa = (kk >> 2) * C::BOX_Q + (kk & 3) * 32;
           const uint32_t ob = (kk >> 2) * C::BOX_KV + (kk & 3) * 32;
-          mma_ss(d, sdesc_sw128(sA + oa, 0, 1024), sdesc_sw128(sB + ob, 0, 1024), idSD,
-                 kk > 0 ? 1u : 0u);
+          mma_ss(d, sdesc_add(dA, oa), sdesc_add(dB, ob), idSD, kk > 0 ? 1u : 0u);
         }
       };
       auto issue_S = [&](int j) -> bool {
         const int s = j % C::NKS;
         if (!mbar_wait(bar(C::B_KFULL + s), (j / C::NKS) & 1, ab)) return false;
-        issue_T(sQ, sbase + C::OFF_K + s * C::KV_TILE, tmem + C::T_S + (j & 1) * 128);
+        issue_T(dQ0, sdesc_add(dK0, s * C::KV_TILE), tmem + C::T_S + (j & 1) * 128);
         mma_commit(bar(C::B_SFULL + (j & 1)));
         return true;
       };
       auto issue_dP = [&](int j) -> bool {
         const int s = j % C::NVS;
         if (!mbar_wait(bar(C::B_VFULL + s), (j / C::NVS) & 1, ab)) return false;
-        issue_T(sDO, sbase + C::OFF_V + s * C::KV_TILE, tmem + C::T_DP);
+        issue_T(dO0, sdesc_add(dV0, s * C::KV_TILE), tmem + C::T_DP);
         mma_commit(bar(C::B_DPFULL));
         mma_commit(bar(C::B_VEMPTY + s));  // V_j is free once dP(j) completes
         return true;
@@ -198,12 +206,12 @@ __global__ void __launch_bounds__(320, 1)
         tc_fence_after();
         // dQ += dS K_j: A = dS (bf16 packed in the S buffer; warpgroup g holds keys
         // 64g .. 64g+63 in columns 64g .. 64g+31), B = K_j MN-major.
-        const uint32_t sk = sbase + C::OFF_K + s * C::KV_TILE;
+        const uint64_t dk = opaque_u64(sdesc_add(dKmn, s * C::KV_TILE));
+        const uint32_t aS = tmem + C::T_S + (j & 1) * 128, acc0 = j > 0 ? 1u : 0u;
 #pragma unroll
         for (int kk = 0; kk < C::BN / 16; ++kk) {
           const uint32_t acol = (kk >> 2) * 64 + (kk & 3) * 8;
-          mma_ts(tmem + C::T_DQ, tmem + C::T_S + (j & 1) * 128 + acol,
-                 sdesc_sw128(sk + kk * 2048, C::BOX_KV, 1024), idQ, (j > 0 || kk > 0) ? 1u : 0u);
+          mma_ts(tmem + C::T_DQ, aS + acol, sdesc_add(dk, kk * 2048), idQ, kk > 0 ? 1u : acc0);
         }
         mma_commit(bar(C::B_KEMPTY + s));
         if (j + 1 < n && !(ok = issue_dP(j + 1))) break;

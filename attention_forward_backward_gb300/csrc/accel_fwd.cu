@@ -127,7 +127,7 @@ __global__ void __launch_bounds__(320, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
-  const Abort ab{abort_flag, err, timeout_ns};
+  const Abort ab = make_abort(abort_flag, err, timeout_ns);
 
   if (warp == 8) {
     // ------------------------------------------------------------ TMA producer
@@ -173,6 +173,11 @@ __global__ void __launch_bounds__(320, 1)
       constexpr uint32_t idS = idesc_bf16_f32(128, C::BN, false, false);
       constexpr uint32_t idO = idesc_bf16_f32(128, DP, false, true);
       bool ok = mbar_wait(bar(C::B_QFULL), 0, ab);
+      // base descriptors; each MMA adds a compile-time byte offset
+      const uint32_t sb = opaque_u32(sbase);
+      const uint64_t dQ0 = sdesc_sw128(sb + C::OFF_Q, 0, 1024);
+      const uint64_t dK0 = sdesc_sw128(sb + C::OFF_K, 0, 1024);
+      const uint64_t dV0 = sdesc_sw128(sb + C::OFF_V, C::BOX_KV, 1024);
       int kwaited = -1;
       auto wait_k = [&](int j) -> bool {
         if (kwaited >= j) return true;
@@ -182,14 +187,14 @@ __global__ void __launch_bounds__(320, 1)
       auto issue_S = [&](int q, int j) -> bool {
         if (!wait_k(j)) return false;
         tc_fence_after();
-        const uint32_t sq = sbase + C::OFF_Q + q * C::Q_TILE;
-        const uint32_t sk = sbase + C::OFF_K + (j % C::NSTAGE) * C::KV_TILE;
+        const uint64_t dq = opaque_u64(sdesc_add(dQ0, q * C::Q_TILE));
+        const uint64_t dk = opaque_u64(sdesc_add(dK0, (j % C::NSTAGE) * C::KV_TILE));
+        const uint32_t dS = tmem + C::T_S + q * 128;
 #pragma unroll
         for (int kk = 0; kk < DP / 16; ++kk) {
           const uint32_t off = (kk >> 2) * C::BOX_Q + (kk & 3) * 32;
           const uint32_t offk = (kk >> 2) * C::BOX_KV + (kk & 3) * 32;
-          mma_ss(tmem + C::T_S + q * 128, sdesc_sw128(sq + off, 0, 1024),
-                 sdesc_sw128(sk + offk, 0, 1024), idS, kk > 0 ? 1u : 0u);
+          mma_ss(dS, sdesc_add(dq, off), sdesc_add(dk, offk), idS, kk > 0 ? 1u : 0u);
         }
         mma_commit(bar(C::B_SFULL + q));
         return true;
@@ -198,13 +203,12 @@ __global__ void __launch_bounds__(320, 1)
         if (!mbar_wait(bar(C::B_PREADY + q), j & 1, ab)) return false;
         if (!mbar_wait(bar(C::B_VFULL + j % C::NSTAGE), (j / C::NSTAGE) & 1, ab)) return false;
         tc_fence_after();
-        const uint32_t sv = sbase + C::OFF_V + (j % C::NSTAGE) * C::KV_TILE;
+        const uint64_t dv = opaque_u64(sdesc_add(dV0, (j % C::NSTAGE) * C::KV_TILE));
+        const uint32_t dO = tmem + C::T_O + q * DP, aP = tmem + C::T_S + q * 128;
+        const uint32_t acc0 = j > 0 ? 1u : 0u;
 #pragma unroll
-        for (int kk = 0; kk < C::BN / 16; ++kk) {
-          mma_ts(tmem + C::T_O + q * DP, tmem + C::T_S + q * 128 + kk * 8,
-                 sdesc_sw128(sv + kk * 2048, C::BOX_KV, 1024), idO,
-                 (j > 0 || kk > 0) ? 1u : 0u);
-        }
+        for (int kk = 0; kk < C::BN / 16; ++kk)
+          mma_ts(dO, aP + kk * 8, sdesc_add(dv, kk * 2048), idO, kk > 0 ? 1u : acc0);
         mma_commit(bar(C::B_ODONE + q));
         return true;
       };

@@ -278,8 +278,8 @@ int mg_attn_bwd(const void *Q, const void *K, const void *V, const void *O, cons
     } else {
       {
         ProfScope ps(MGK_ACCEL_DKDV, st);
-        e = mg_launch_accel_dkdv(q, k, v, d, LSE, Dvec, nullptr, static_cast<float *>(dK),
-                                 static_cast<float *>(dV), p, err, st);
+        e = mg_launch_accel_dkdv_pp(q, k, v, d, LSE, Dvec, static_cast<float *>(dK),
+                                    static_cast<float *>(dV), p, err, st);
       }
       if (e != cudaSuccess) return MG_ERR_CUDA;
       ProfScope ps(MGK_ACCEL_DQ, st);

@@ -47,8 +47,8 @@ cudaError_t mg_launch_dvec_bf16(const float *O, const __nv_bfloat16 *dO, float *
                                 const MgProblem &p, cudaStream_t st);
 
 // ACCEL_BF16 (tcgen05 / TMEM / TMA) kernels. `err` is the device error word.
-// mg_launch_accel_dkdv: with dQ != nullptr the fused kernel also adds dQ into
-// (zeroed) dQ; with dQ == nullptr it computes dK and dV only.
+// mg_launch_accel_dkdv: the fused kernel; it computes dK and dV and adds dQ
+// into a zeroed dQ (dQ must not be null).
 cudaError_t mg_launch_accel_fwd(const __nv_bfloat16 *Q, const __nv_bfloat16 *K,
                                 const __nv_bfloat16 *V, float *O, float *LSE,
                                 const MgProblem &p, unsigned int *err, cudaStream_t st);
@@ -57,6 +57,12 @@ cudaError_t mg_launch_accel_dkdv(const __nv_bfloat16 *Q, const __nv_bfloat16 *K,
                                  const float *LSE, const float *Dvec, float *dQ, float *dK,
                                  float *dV, const MgProblem &p, unsigned int *err,
                                  cudaStream_t st);
+
+// dK/dV kernel of the two-pass backward: two query blocks in flight per CTA.
+cudaError_t mg_launch_accel_dkdv_pp(const __nv_bfloat16 *Q, const __nv_bfloat16 *K,
+                                    const __nv_bfloat16 *V, const __nv_bfloat16 *dO,
+                                    const float *LSE, const float *Dvec, float *dK, float *dV,
+                                    const MgProblem &p, unsigned int *err, cudaStream_t st);
 
 // Opt a kernel into more than 48 KB of dynamic shared memory once per device.
 cudaError_t mg_set_smem_attr(const void *func, int bytes, int slot);

@@ -67,27 +67,49 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
 struct Abort {
   volatile int *flag;     // shared memory
   unsigned int *err;      // device error word (global)
-  uint64_t timeout_ns;
+  uint32_t timeout_units; // wait limit in units of 1024 ns
 };
+
+// Abort state from a wait limit in nanoseconds.
+__device__ __forceinline__ Abort make_abort(volatile int *flag, unsigned int *err,
+                                            unsigned long long timeout_ns) {
+  const unsigned long long u = timeout_ns >> 10;
+  return Abort{flag, err, static_cast<uint32_t>(u > 0xFFFFFFFFull ? 0xFFFFFFFFull : u)};
+}
+
+// try_wait that may suspend the thread (up to `hint_ns`) until the phase
+// completes, instead of returning at once: waiting warps then leave the issue
+// slots and the shared-memory pipe to the roles doing work.
+__device__ __forceinline__ bool mbar_try_wait_hint(uint32_t bar, uint32_t parity,
+                                                   uint32_t hint_ns) {
+  uint32_t ok;
+  asm volatile(
+      "{\n"
+      " .reg .pred p;\n"
+      " mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n"
+      " selp.u32 %0, 1, 0, p;\n"
+      "}\n"
+      : "=r"(ok)
+      : "r"(bar), "r"(parity), "r"(hint_ns)
+      : "memory");
+  return ok != 0;
+}
 
 // Bounded wait on phase `parity` of an mbarrier, for one thread. Returns false
 // if the CTA is aborting or if the wait exceeded the time limit (then it sets
-// the abort flag and the device error word). Never traps, never spins forever.
+// the abort flag and the device error word). Never traps, never spins forever:
+// each suspended try_wait gives up after 100 us, and the abort flag and the
+// clock are checked between them.
 __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, const Abort &ab) {
   if (mbar_try_wait(bar, parity)) return true;
-  uint64_t t0 = 0;
-  for (uint32_t it = 1;; ++it) {
-    if (mbar_try_wait(bar, parity)) return true;
-    if ((it & 255u) == 0) {
-      if (*ab.flag) return false;
-      const uint64_t now = globaltimer();
-      if (t0 == 0) {
-        t0 = now;
-      } else if (now - t0 > ab.timeout_ns) {
-        *ab.flag = 1;
-        atomicOr(ab.err, 1u);
-        return false;
-      }
+  const uint32_t t0 = static_cast<uint32_t>(globaltimer() >> 10);
+  for (;;) {
+    if (mbar_try_wait_hint(bar, parity, 100000u)) return true;
+    if (*ab.flag) return false;
+    if (static_cast<uint32_t>(globaltimer() >> 10) - t0 > ab.timeout_units) {
+      *ab.flag = 1;
+      atomicOr(ab.err, 1u);
+      return false;
     }
   }
 }
@@ -248,6 +270,30 @@ __device__ __forceinline__ uint64_t sdesc_sw128(uint32_t saddr, uint32_t lbo, ui
   d |= static_cast<uint64_t>(1) << 46;
   d |= static_cast<uint64_t>(2) << 61;
   return d;
+}
+
+// Returns `v` through an opaque move: values derived from it are computed where
+// they are used (inside one warp role's branch) instead of being hoisted to the
+// kernel entry, where they would stay live in every role's registers.
+__device__ __forceinline__ uint32_t opaque_u32(uint32_t v) {
+  uint32_t r;
+  asm volatile("mov.b32 %0, %1;" : "=r"(r) : "r"(v));
+  return r;
+}
+
+__device__ __forceinline__ uint64_t opaque_u64(uint64_t v) {
+  uint64_t r;
+  asm volatile("mov.b64 %0, %1;" : "=l"(r) : "l"(v));
+  return r;
+}
+
+// Descriptor of the same operand `byte_off` bytes further on: the start address
+// field holds addr >> 4 in 14 bits, and every shared-memory address of this GPU
+// (below 228 KB) stays inside it, so the add never carries into LBO. With
+// `byte_off` a compile-time constant this is one add per MMA instead of
+// rebuilding the descriptor.
+__device__ __forceinline__ uint64_t sdesc_add(uint64_t desc, uint32_t byte_off) {
+  return desc + (byte_off >> 4);
 }
 
 // Instruction descriptor of kind::f16 with bf16 A and B, f32 accumulator.

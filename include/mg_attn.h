@@ -105,7 +105,8 @@ size_t mg_attn_bwd_workspace_bytes(int B, int H, int L, int D, int contract);
  * STRICT and the default ACCEL mode add each key block's dQ contribution into
  * a zeroed dQ with f32 reductions (results not bitwise reproducible); with the
  * environment variable MG_DQ_MODE=pass (read once per process) ACCEL instead
- * runs a separate dQ pass over query blocks that stores dQ without atomics.
+ * runs a dK/dV kernel and a separate dQ pass over query blocks that stores dQ
+ * without atomics (bitwise reproducible; slower on GB300 at long sequences).
  */
 int mg_attn_bwd(const void *Q, const void *K, const void *V, const void *O,
                 const void *dO, const float *LSE, void *dQ, void *dK, void *dV,
