@@ -45,8 +45,8 @@ L2_FLUSH_BYTES = 512 << 20  # > 129 MB L2
 # profiles/ (taken on half of the heads and scaled by 2; per-head traffic is
 # identical). Remove an entry when its kernel changes.
 NCU_TRAFFIC_BYTES = {
-    ("accel_dkdv_dq", 5): 2 * (404.828672e6 + 349.318912e6),
-    ("accel_fwd", 5): 2 * (546.099712e6 + 99.816192e6),
+    ("accel_dkdv_dq", 5): 2 * (405.024512e6 + 349.171712e6),
+    ("accel_fwd", 5): 2 * (551.054080e6 + 102.975744e6),
 }
 
 
