@@ -98,9 +98,10 @@ def test_accel_repeatable_forward():
 
 
 def test_accel_pass_dq_mode_in_child():
-    """The two-pass backward (dK/dV kernel + separate dQ pass, MG_DQ_MODE=pass)
-    on cfg 2, cfg 3 and a ragged D = 128 case, in a child process because the
-    mode is read once per process."""
+    """The two-pass backward (dK/dV kernel with two query blocks in flight, then
+    the separate dQ pass; MG_DQ_MODE=pass) on cfg 2, 3 and 4 and on sub-tile,
+    one-tile and ragged lengths for every head dim, causal and not, in a child
+    process because the mode is read once per process."""
     import os
     import subprocess
     import sys
@@ -112,8 +113,13 @@ def test_accel_pass_dq_mode_in_child():
         import oracle
         from attention_forward_backward_gb300 import synth
         from parity_util import compare, device_inputs, run_gpu
-        for w in (synth.WORKLOADS[2], synth.WORKLOADS[3],
-                  synth.custom_workload(1, 3, 300, 128, True, seed_cfg=990)):
+        cases = [synth.WORKLOADS[2], synth.WORKLOADS[3], synth.WORKLOADS[4],
+                 synth.custom_workload(1, 3, 300, 128, True, seed_cfg=990)]
+        for D in (32, 64, 128):
+            for L in (1, 63, 64, 65, 200):
+                for causal in (True, False):
+                    cases.append(synth.custom_workload(1, 2, L, D, causal, seed_cfg=991 + D))
+        for w in cases:
             dev, vals = device_inputs(synth.inputs(w, "accel"), "accel")
             got = run_gpu(dev, w.causal, w.scale, "accel")
             ref = oracle.attn_bwd(vals["Q"], vals["K"], vals["V"], vals["dO"], w.causal, w.scale)
