@@ -270,49 +270,54 @@ def run_e2e(mg, torch, w, contract, args, host, device, stream, flops_step):
     """Same metric through the C ABI with host buffers: every step copies its
     inputs from pinned host memory and reads every output (O, LSE, dQ, dK, dV)
     back into pinned host memory. Consecutive steps overlap the way a training
-    loop would: step k+1's inputs are copied in and step k-1's outputs copied out
-    while step k computes (two device buffer sets; host-to-device, compute and
-    device-to-host on three streams, ordered by events)."""
+    loop would: while step k computes, step k+1's inputs are copied in and the
+    outputs of earlier steps copied out (host-to-device, compute and
+    device-to-host on three streams ordered by events; two input and three
+    output buffer sets, so that a slow read-back does not hold up the next
+    step's compute)."""
     B, H, L, D = w.shape
     f32 = torch.float32
-    sets = []
-    for _ in range(2):
-        dev = {k: torch.empty_like(v, device=device) for k, v in host.items()}
+    n_in, n_out = 2, 3
+    ins = [{k: torch.empty_like(v, device=device) for k, v in host.items()} for _ in range(n_in)]
+    outs, houts = [], []
+    for _ in range(n_out):
         O = torch.empty((B, H, L, D), dtype=f32, device=device)
-        outs = {"O": O, "LSE": torch.empty((B, H, L), dtype=f32, device=device),
-                "dQ": torch.empty_like(O), "dK": torch.empty_like(O), "dV": torch.empty_like(O)}
-        hout = {k: torch.empty(v.shape, dtype=v.dtype).pin_memory() for k, v in outs.items()}
-        sets.append((dev, outs, hout))
+        o = {"O": O, "LSE": torch.empty((B, H, L), dtype=f32, device=device),
+             "dQ": torch.empty_like(O), "dK": torch.empty_like(O), "dV": torch.empty_like(O)}
+        outs.append(o)
+        houts.append({k: torch.empty(v.shape, dtype=v.dtype).pin_memory() for k, v in o.items()})
     ws = torch.empty(mg.mg_attn_bwd_workspace_bytes(B, H, L, D, contract), dtype=torch.uint8,
                      device=device)
     h2d = sum(v.numel() * v.element_size() for v in host.values())
-    d2h = sum(v.numel() * v.element_size() for v in sets[0][1].values())
+    d2h = sum(v.numel() * v.element_size() for v in outs[0].values())
     s_in, s_comp, s_out = torch.cuda.Stream(device), stream, torch.cuda.Stream(device)
-    in_ready = [torch.cuda.Event() for _ in range(2)]
-    comp_done = [torch.cuda.Event() for _ in range(2)]
-    out_done = [torch.cuda.Event() for _ in range(2)]
+    in_ready = [torch.cuda.Event() for _ in range(n_in)]
+    in_free = [torch.cuda.Event() for _ in range(n_in)]
+    comp_done = [torch.cuda.Event() for _ in range(n_out)]
+    out_done = [torch.cuda.Event() for _ in range(n_out)]
 
     def step(k):
-        b = k % 2
-        dev, outs, hout = sets[b]
-        s_in.wait_event(comp_done[b])  # step k-2 no longer reads this input set
+        bi, bo = k % n_in, k % n_out
+        dev, o, ho = ins[bi], outs[bo], houts[bo]
+        s_in.wait_event(in_free[bi])  # the step that last read this input set is done
         with torch.cuda.stream(s_in):
             for key in host:
                 dev[key].copy_(host[key], non_blocking=True)
-        in_ready[b].record(s_in)
-        s_comp.wait_event(in_ready[b])
-        s_comp.wait_event(out_done[b])  # step k-2's outputs have left this set
+        in_ready[bi].record(s_in)
+        s_comp.wait_event(in_ready[bi])
+        s_comp.wait_event(out_done[bo])  # this output set's previous contents have left
         c = s_comp.cuda_stream
-        mg.mg_attn_fwd(dev["Q"], dev["K"], dev["V"], outs["O"], outs["LSE"], w.causal, w.scale,
+        mg.mg_attn_fwd(dev["Q"], dev["K"], dev["V"], o["O"], o["LSE"], w.causal, w.scale,
                        contract, c)
-        mg.mg_attn_bwd(dev["Q"], dev["K"], dev["V"], outs["O"], dev["dO"], outs["LSE"],
-                       outs["dQ"], outs["dK"], outs["dV"], w.causal, w.scale, contract, ws, c)
-        comp_done[b].record(s_comp)
-        s_out.wait_event(comp_done[b])
+        mg.mg_attn_bwd(dev["Q"], dev["K"], dev["V"], o["O"], dev["dO"], o["LSE"], o["dQ"],
+                       o["dK"], o["dV"], w.causal, w.scale, contract, ws, c)
+        in_free[bi].record(s_comp)
+        comp_done[bo].record(s_comp)
+        s_out.wait_event(comp_done[bo])
         with torch.cuda.stream(s_out):
-            for key in outs:
-                hout[key].copy_(outs[key], non_blocking=True)
-        out_done[b].record(s_out)
+            for key in o:
+                ho[key].copy_(o[key], non_blocking=True)
+        out_done[bo].record(s_out)
 
     for k in range(args.warmup):
         step(k)
@@ -330,7 +335,8 @@ def run_e2e(mg, torch, w, contract, args, host, device, stream, flops_step):
     return {"value": job_tflops(flops_step, args.steps, ms, world()), "unit": UNIT,
             "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
             "ms_per_step": ms / args.steps,
-            "overlap": "inputs of step k+1 and outputs of step k-1 copied while step k computes"}
+            "overlap": "inputs of step k+1 copied in and outputs of earlier steps copied out "
+                       "while step k computes (2 input, 3 output buffer sets)"}
 
 
 # ------------------------------------------------------------------ distributed
