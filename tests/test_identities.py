@@ -94,3 +94,24 @@ def test_cfg5_identities_two_pass_backward_in_child():
     r = subprocess.run([sys.executable, "-c", code], env=env, capture_output=True, text=True,
                        timeout=900)
     assert r.returncode == 0 and "IDENTITIES-OK" in r.stdout, r.stdout + r.stderr
+
+
+@pytest.mark.gpu
+@pytest.mark.parametrize("contract", ["accel", "strict"])
+def test_long_single_head_identities_and_rows(contract):
+    """One head of L = 32768 (D = 128, causal): 512 query blocks per key block in
+    the backward and 256 key tiles per query tile in the forward. Sampled rows of
+    O and LSE against the oracle, and both identities over the whole head."""
+    import oracle
+    from parity_util import compare
+    w = synth.custom_workload(1, 1, 32768, 128, True, seed_cfg=1995)
+    dev, vals = device_inputs(synth.inputs(w, contract), contract)
+    got = run_gpu(dev, w.causal, w.scale, contract, bwd=True)
+    res = identity_residuals(got, vals, w)
+    assert all(v <= TOL[contract] for v in res.values()), res
+    rows = np.array([0, 1, 127, 128, 16383, 16384, 32766, 32767])
+    Q, K, V = (vals[k].reshape(w.L, w.D) for k in ("Q", "K", "V"))
+    O, LSE = oracle.attn_fwd_rows(Q, K, V, rows, True, w.scale)
+    errs, bad = compare({"O": got["O"].reshape(w.L, w.D)[rows], "LSE": got["LSE"].reshape(w.L)[rows]},
+                        {"O": O, "LSE": LSE}, contract)
+    assert not bad, errs
