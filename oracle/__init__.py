@@ -15,6 +15,10 @@ central finite differences of sum(dO*O) for dQ, dK, dV; softmax rows summing to
 one; the causal first row; dV with dO = 1 giving the column sums of P; the
 softmax-Jacobian invariant sum_j dK_j = 0; L = 1 and equal-key closed forms; the
 key-shift metamorphic relation; torch float64 SDPA + autograd on tiny shapes.
+For cross attention (Lq != Lk) and the two causal alignments: central finite
+differences for every alignment, the alignments coinciding when Lq = Lk, a
+single bottom-right query seeing every key, empty-softmax rows contributing
+nothing, and torch float64 SDPA with explicit boolean masks + autograd.
 """
 from __future__ import annotations
 
@@ -61,6 +65,11 @@ def _load():
             lib.oracle_attn_bwd.argtypes = [dp, dp, dp, dp, dp, dp, dp, dp, dp, dp,
                                             L, L, I, I, D, I]
             lib.oracle_attn_bwd.restype = I
+            lib.oracle_attn_fwd_ex.argtypes = [dp, dp, dp, dp, dp, L, L, L, I, I, D, I]
+            lib.oracle_attn_fwd_ex.restype = I
+            lib.oracle_attn_bwd_ex.argtypes = [dp, dp, dp, dp, dp, dp, dp, dp, dp, dp,
+                                               L, L, L, I, I, D, I]
+            lib.oracle_attn_bwd_ex.restype = I
             lib.oracle_max_threads.argtypes = []
             lib.oracle_max_threads.restype = I
             _lib = lib
@@ -82,6 +91,61 @@ def _shape(Q):
     L, D = Q.shape[-2], Q.shape[-1]
     BH = int(np.prod(Q.shape[:-2])) if Q.ndim > 2 else 1
     return BH, L, D
+
+
+MASKS = {"none": 0, "causal": 1, "causal_bottom_right": 2}
+
+
+def _mask_id(mask) -> int:
+    if isinstance(mask, str):
+        return MASKS[mask]
+    if int(mask) not in MASKS.values():
+        raise ValueError(f"unknown mask {mask}")
+    return int(mask)
+
+
+def _shape_ex(Q, K):
+    if Q.ndim < 2 or K.ndim != Q.ndim or Q.shape[:-2] != K.shape[:-2] or Q.shape[-1] != K.shape[-1]:
+        raise ValueError("expected Q [..., Lq, D] and K, V [..., Lk, D] with the same leading dims")
+    BH = int(np.prod(Q.shape[:-2])) if Q.ndim > 2 else 1
+    return BH, Q.shape[-2], K.shape[-2], Q.shape[-1]
+
+
+def attn_fwd_ex(Q, K, V, mask, scale: float, nthreads: int = 0):
+    """(O, LSE) in float64 for Q [..., Lq, D] and K, V [..., Lk, D]. ``mask``:
+    "none", "causal" (top-left, j <= i) or "causal_bottom_right" (j <= i + Lk - Lq).
+    Rows with no allowed key get O = 0 and LSE = -inf."""
+    lib = _load()
+    Q, K, V = _f64(Q), _f64(K), _f64(V)
+    if K.shape != V.shape:
+        raise ValueError("K and V must share one shape")
+    BH, Lq, Lk, D = _shape_ex(Q, K)
+    O = np.empty_like(Q)
+    LSE = np.empty(Q.shape[:-1], dtype=np.float64)
+    rc = lib.oracle_attn_fwd_ex(_ptr(Q), _ptr(K), _ptr(V), _ptr(O), _ptr(LSE), BH, Lq, Lk, D,
+                                _mask_id(mask), float(scale), int(nthreads))
+    if rc:
+        raise RuntimeError(f"oracle_attn_fwd_ex failed ({rc})")
+    return O, LSE
+
+
+def attn_bwd_ex(Q, K, V, dO, mask, scale: float, nthreads: int = 0) -> dict:
+    """Forward and backward in float64 for Q, dO [..., Lq, D] and K, V [..., Lk, D]:
+    O, LSE, Dvec, dQ, dK, dV (see ``attn_fwd_ex`` for ``mask``)."""
+    lib = _load()
+    Q, K, V, dO = _f64(Q), _f64(K), _f64(V), _f64(dO)
+    if K.shape != V.shape or Q.shape != dO.shape:
+        raise ValueError("K, V and Q, dO must share shapes")
+    BH, Lq, Lk, D = _shape_ex(Q, K)
+    out = {"O": np.empty_like(Q), "LSE": np.empty(Q.shape[:-1]), "Dvec": np.empty(Q.shape[:-1]),
+           "dQ": np.empty_like(Q), "dK": np.empty_like(K), "dV": np.empty_like(K)}
+    rc = lib.oracle_attn_bwd_ex(_ptr(Q), _ptr(K), _ptr(V), _ptr(dO), _ptr(out["O"]),
+                                _ptr(out["LSE"]), _ptr(out["Dvec"]), _ptr(out["dQ"]),
+                                _ptr(out["dK"]), _ptr(out["dV"]), BH, Lq, Lk, D,
+                                _mask_id(mask), float(scale), int(nthreads))
+    if rc:
+        raise RuntimeError(f"oracle_attn_bwd_ex failed ({rc})")
+    return out
 
 
 def max_threads() -> int:

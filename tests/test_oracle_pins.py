@@ -273,3 +273,106 @@ def test_bf16_rounding_matches_torch():
     ours = synth.round_to_bf16(x)
     ref = torch.tensor(x).to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16)
     np.testing.assert_array_equal(ours, ref)
+
+
+# ---------------------------------------------------------------- cross attention and mask alignment
+MASKS_EX = ("none", "causal", "causal_bottom_right")
+
+
+def loss_ex(Q, K, V, dO, mask, scale):
+    O, _ = oracle.attn_fwd_ex(Q, K, V, mask, scale)
+    return float(np.sum(O * dO))
+
+
+@pytest.mark.parametrize("Lq,Lk", [(3, 5), (5, 3), (1, 4), (4, 1)])
+@pytest.mark.parametrize("mask", MASKS_EX)
+def test_cross_attention_finite_differences(Lq, Lk, mask):
+    """Lq != Lk: dQ, dK, dV equal central differences of sum(dO * O) for every
+    mask alignment, including rows with an empty softmax (their O is constant 0,
+    so they contribute nothing)."""
+    D, scale, h = 3, 0.6, 1e-6
+    Q, dO = rand(1, 2, Lq, D), rand(1, 2, Lq, D)
+    K, V = rand(1, 2, Lk, D), rand(1, 2, Lk, D)
+    g = oracle.attn_bwd_ex(Q, K, V, dO, mask, scale)
+    for name, X in (("dQ", Q), ("dK", K), ("dV", V)):
+        num = np.zeros_like(X)
+        for idx in np.ndindex(X.shape):
+            orig = X[idx]
+            X[idx] = orig + h
+            lp = loss_ex(Q, K, V, dO, mask, scale)
+            X[idx] = orig - h
+            lm = loss_ex(Q, K, V, dO, mask, scale)
+            X[idx] = orig
+            num[idx] = (lp - lm) / (2 * h)
+        if np.max(np.abs(num)) < 1e-8:
+            assert np.max(np.abs(g[name])) < 1e-12, name
+        else:
+            err = np.max(np.abs(num - g[name])) / np.max(np.abs(num))
+            assert err < 1e-6, (name, err)
+
+
+def test_mask_alignments_coincide_when_square():
+    """With Lq = Lk the top-left and bottom-right causal masks are the same mask,
+    and the self-attention entry points agree with the general ones."""
+    Q, K, V, dO = (rand(2, 2, 9, 4) for _ in range(4))
+    a = oracle.attn_bwd_ex(Q, K, V, dO, "causal", 0.4)
+    b = oracle.attn_bwd_ex(Q, K, V, dO, "causal_bottom_right", 0.4)
+    c = oracle.attn_bwd(Q, K, V, dO, True, 0.4)
+    for k in ("O", "LSE", "dQ", "dK", "dV"):
+        np.testing.assert_array_equal(a[k], b[k])
+        np.testing.assert_array_equal(a[k], c[k])
+
+
+def test_single_query_bottom_right_sees_every_key():
+    """One query aligned at the bottom right attends to all Lk keys: the same as
+    no mask, and (for the top-left alignment) only key 0."""
+    Q, dO = rand(1, 1, 1, 6), rand(1, 1, 1, 6)
+    K, V = rand(1, 1, 13, 6), rand(1, 1, 13, 6)
+    br = oracle.attn_bwd_ex(Q, K, V, dO, "causal_bottom_right", 0.5)
+    full = oracle.attn_bwd_ex(Q, K, V, dO, "none", 0.5)
+    for k in ("O", "LSE", "dQ", "dK", "dV"):
+        np.testing.assert_array_equal(br[k], full[k])
+    tl = oracle.attn_bwd_ex(Q, K, V, dO, "causal", 0.5)
+    np.testing.assert_allclose(tl["O"][0, 0, 0], V[0, 0, 0], rtol=0, atol=1e-15)
+    assert np.all(tl["dK"][0, 0, 1:] == 0) and np.all(tl["dV"][0, 0, 1:] == 0)
+
+
+def test_empty_rows_contribute_nothing():
+    """Bottom-right alignment with Lq > Lk leaves the first Lq - Lk rows without
+    keys: O = 0, LSE = -inf, dQ = 0, and dK, dV equal those of the problem
+    without those rows (same alignment, Lq' = Lk)."""
+    Lq, Lk, D = 11, 4, 5
+    Q, dO = rand(1, 2, Lq, D), rand(1, 2, Lq, D)
+    K, V = rand(1, 2, Lk, D), rand(1, 2, Lk, D)
+    g = oracle.attn_bwd_ex(Q, K, V, dO, "causal_bottom_right", 0.45)
+    e = Lq - Lk
+    assert np.all(g["O"][:, :, :e] == 0) and np.all(g["dQ"][:, :, :e] == 0)
+    assert np.all(np.isneginf(g["LSE"][:, :, :e])) and np.all(np.isfinite(g["LSE"][:, :, e:]))
+    r = oracle.attn_bwd_ex(Q[:, :, e:], K, V, dO[:, :, e:], "causal_bottom_right", 0.45)
+    for k in ("dK", "dV"):
+        np.testing.assert_allclose(g[k], r[k], rtol=1e-13, atol=1e-14)
+    for k in ("O", "LSE", "dQ"):
+        np.testing.assert_allclose(g[k][:, :, e:], r[k], rtol=1e-13, atol=1e-14)
+
+
+@pytest.mark.parametrize("mask", MASKS_EX)
+def test_torch_float64_sdpa_cross_attention(mask):
+    """Third implementation for Lq != Lk: torch CPU float64 SDPA with an explicit
+    boolean mask of each alignment, + autograd (no empty rows here)."""
+    torch = pytest.importorskip("torch")
+    import torch.nn.functional as F
+    B, H, Lq, Lk, D, scale = 2, 2, 7, 10, 4, 0.5
+    Q, dO = rand(B, H, Lq, D), rand(B, H, Lq, D)
+    K, V = rand(B, H, Lk, D), rand(B, H, Lk, D)
+    i = np.arange(Lq)[:, None]
+    j = np.arange(Lk)[None, :]
+    allow = {"none": np.ones((Lq, Lk), bool), "causal": j <= i,
+             "causal_bottom_right": j <= i + (Lk - Lq)}[mask]
+    tq, tk, tv = (torch.tensor(x, dtype=torch.float64, requires_grad=True) for x in (Q, K, V))
+    out = F.scaled_dot_product_attention(tq, tk, tv, attn_mask=torch.tensor(allow), scale=scale)
+    out.backward(torch.tensor(dO, dtype=torch.float64))
+    g = oracle.attn_bwd_ex(Q, K, V, dO, mask, scale)
+    np.testing.assert_allclose(g["O"], out.detach().numpy(), rtol=1e-12, atol=1e-12)
+    np.testing.assert_allclose(g["dQ"], tq.grad.numpy(), rtol=1e-11, atol=1e-12)
+    np.testing.assert_allclose(g["dK"], tk.grad.numpy(), rtol=1e-11, atol=1e-12)
+    np.testing.assert_allclose(g["dV"], tv.grad.numpy(), rtol=1e-11, atol=1e-12)
