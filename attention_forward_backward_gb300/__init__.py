@@ -63,6 +63,13 @@ def load_library(path: str | None = None):
         lib.mg_attn_bwd.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, i, i, i, i, i, f, i,
                                     vp, sz, vp]
         lib.mg_attn_bwd.restype = i
+        lib.mg_attn_fwd_ex.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, i, i, f, i, vp]
+        lib.mg_attn_fwd_ex.restype = i
+        lib.mg_attn_bwd_workspace_bytes_ex.argtypes = [i, i, i, i, i, i]
+        lib.mg_attn_bwd_workspace_bytes_ex.restype = sz
+        lib.mg_attn_bwd_ex.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, i, i, i, i, i, i, f,
+                                       i, vp, sz, vp]
+        lib.mg_attn_bwd_ex.restype = i
         lib.mg_status_string.argtypes = [i]
         lib.mg_status_string.restype = ctypes.c_char_p
         lib.mg_get_device_error.argtypes = [vp]
@@ -134,6 +141,45 @@ def mg_attn_bwd(Q, K, V, O, dO, LSE, dQ, dK, dV, causal, scale, contract, worksp
                                     _ptr(workspace), ws_bytes, _stream(stream))
     if rc != MG_OK:
         raise MgError(rc, "mg_attn_bwd")
+    return rc
+
+
+MASKS = {"none": 0, "causal": 1, "causal_bottom_right": 2}
+
+
+def _mask(m) -> int:
+    return MASKS[m] if isinstance(m, str) else int(m)
+
+
+def mg_attn_fwd_ex(Q, K, V, O, LSE, mask, scale, contract, stream=None) -> int:
+    """Cross-attention forward: Q, O [B, H, Lq, D]; K, V [B, H, Lk, D]; LSE [B, H, Lq];
+    mask "none", "causal" (top-left) or "causal_bottom_right"."""
+    B, H, Lq, D = _dims(Q)
+    Lk = int(K.shape[2])
+    rc = load_library().mg_attn_fwd_ex(_ptr(Q), _ptr(K), _ptr(V), _ptr(O), _ptr(LSE), B, H, Lq,
+                                       Lk, D, _mask(mask), float(scale), _contract(contract),
+                                       _stream(stream))
+    if rc != MG_OK:
+        raise MgError(rc, "mg_attn_fwd_ex")
+    return rc
+
+
+def mg_attn_bwd_workspace_bytes_ex(B, H, Lq, Lk, D, contract) -> int:
+    return int(load_library().mg_attn_bwd_workspace_bytes_ex(B, H, Lq, Lk, D, _contract(contract)))
+
+
+def mg_attn_bwd_ex(Q, K, V, O, dO, LSE, dQ, dK, dV, mask, scale, contract, workspace,
+                   stream=None) -> int:
+    """Cross-attention backward (shapes as in mg_attn_fwd_ex; dQ like Q, dK and dV like K)."""
+    B, H, Lq, D = _dims(Q)
+    Lk = int(K.shape[2])
+    ws_bytes = workspace.numel() * workspace.element_size() if workspace is not None else 0
+    rc = load_library().mg_attn_bwd_ex(_ptr(Q), _ptr(K), _ptr(V), _ptr(O), _ptr(dO), _ptr(LSE),
+                                       _ptr(dQ), _ptr(dK), _ptr(dV), B, H, Lq, Lk, D,
+                                       _mask(mask), float(scale), _contract(contract),
+                                       _ptr(workspace), ws_bytes, _stream(stream))
+    if rc != MG_OK:
+        raise MgError(rc, "mg_attn_bwd_ex")
     return rc
 
 

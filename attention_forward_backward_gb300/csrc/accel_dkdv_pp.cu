@@ -87,7 +87,8 @@ __global__ void __launch_bounds__(320, 1)
                          const __grid_constant__ CUtensorMap tmV,
                          const __grid_constant__ CUtensorMap tmdO, const float *__restrict__ LSE,
                          const float *__restrict__ Dvec, float *__restrict__ dK,
-                         float *__restrict__ dV, int BH, int L, int D, int causal, float scale,
+                         float *__restrict__ dV, int BH, int L, int Lk, int D, int causal,
+                         int off, float scale,
                          float scale_log2, unsigned int *err, unsigned long long timeout_ns) {
   using C = PPCfg<DP>;
   extern __shared__ uint8_t smem_raw[];
@@ -104,13 +105,14 @@ __global__ void __launch_bounds__(320, 1)
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   // Head-major order: CTAs that run together share a few heads' Q/dO in L2;
   // within a head the heaviest causal key block (kb = 0) goes first.
-  const int nkb = (L + C::BN - 1) / C::BN;
+  // L query rows, Lk key rows; causal: query i sees key j iff j <= i + off
+  const int nkb = (Lk + C::BN - 1) / C::BN;
   const int bh = static_cast<int>(blockIdx.x / nkb);
   const int kb = static_cast<int>(blockIdx.x % nkb);
   const int k0 = kb * C::BN;
   const int nqb = (L + C::BQ - 1) / C::BQ;
-  const int qb0 = causal ? (k0 / C::BQ) : 0;
-  const int n = nqb - qb0;
+  const int qb0 = causal ? max(0, k0 - off) / C::BQ : 0;  // first block with a query seeing k0
+  const int n = max(0, nqb - qb0);
 
   if (warp == 0) {
     tmem_alloc(smem_u32(tmem_slot), C::TMEM_COLS);
@@ -156,7 +158,9 @@ __global__ void __launch_bounds__(320, 1)
       for (int r = lane; r < C::BQ; r += 32) {
         const int qg = q0 + r;
         const bool v = qg < L;
-        sLse[st * C::BQ + r] = v ? LSE[static_cast<size_t>(bh) * L + qg] * kLog2e : INFINITY;
+        // +inf also for a row with an empty softmax (LSE = -inf): its P is 0
+        const float lse = v ? LSE[static_cast<size_t>(bh) * L + qg] : -INFINITY;
+        sLse[st * C::BQ + r] = lse == -INFINITY ? INFINITY : lse * kLog2e;
         sDv[st * C::BQ + r] = v ? Dvec[static_cast<size_t>(bh) * L + qg] : 0.f;
       }
       __syncwarp();
@@ -254,7 +258,7 @@ __global__ void __launch_bounds__(320, 1)
       if (!(ok = mbar_wait_warp(bar(C::B_QFULL + st), (i / C::NQS) & 1, ab))) break;
       if (!(ok = mbar_wait_warp(bar(C::B_SFULL + w), ph, ab))) break;
       tc_fence_after();
-      const bool need_mask = (kg >= L) || (causal && k0 + C::BN - 1 > q0);
+      const bool need_mask = (kg >= Lk) || (causal && k0 + C::BN - 1 > q0 + off);
       const float *lse = sLse + st * C::BQ;
       const float *dvq = sDv + st * C::BQ;
       float p[C::BQ];
@@ -274,7 +278,7 @@ __global__ void __launch_bounds__(320, 1)
         if (need_mask) {
 #pragma unroll
           for (int e = 0; e < 64; ++e)
-            if (kg >= L || (causal && kg > q0 + e)) p[e] = 0.f;
+            if (kg >= Lk || (causal && kg > q0 + e + off)) p[e] = 0.f;
         }
       }
       // P^T over the first 32 columns of S^T (already read)
@@ -325,10 +329,18 @@ __global__ void __launch_bounds__(320, 1)
     }
     // dK (scaled) and dV of this key block: warpgroup w stores half the columns
     if (ok && n > 0) ok = mbar_wait_warp(bar(C::B_ACCDONE), 0, ab);
+    if (ok && n == 0 && kg < Lk) {
+      // no query sees this key block: dK = dV = 0 (warpgroup w writes its half)
+      const size_t row = (static_cast<size_t>(bh) * Lk + kg) * D;
+      for (int c = 0; c < DP / 2 && w * (DP / 2) + c < D; c += 4) {
+        *reinterpret_cast<float4 *>(dV + row + w * (DP / 2) + c) = make_float4(0.f, 0.f, 0.f, 0.f);
+        *reinterpret_cast<float4 *>(dK + row + w * (DP / 2) + c) = make_float4(0.f, 0.f, 0.f, 0.f);
+      }
+    }
     if (ok && n > 0) {
       tc_fence_after();
-      const bool valid = kg < L;
-      const size_t row = (static_cast<size_t>(bh) * L + (valid ? kg : 0)) * D;
+      const bool valid = kg < Lk;
+      const size_t row = (static_cast<size_t>(bh) * Lk + (valid ? kg : 0)) * D;
 #pragma unroll
       for (int c = 0; c < DP / 64; ++c) {
         const int col = w * (DP / 2) + 32 * c;
@@ -382,16 +394,17 @@ cudaError_t launch(const __nv_bfloat16 *Q, const __nv_bfloat16 *K, const __nv_bf
   cudaError_t e;
   if ((e = mg_tmap_bf16(&tq, Q, p.D, p.L, BH, C::BQ)) != cudaSuccess) return e;
   if ((e = mg_tmap_bf16(&tdo, dO, p.D, p.L, BH, C::BQ)) != cudaSuccess) return e;
-  if ((e = mg_tmap_bf16(&tk, K, p.D, p.L, BH, C::BN)) != cudaSuccess) return e;
-  if ((e = mg_tmap_bf16(&tv, V, p.D, p.L, BH, C::BN)) != cudaSuccess) return e;
+  if ((e = mg_tmap_bf16(&tk, K, p.D, p.Lk, BH, C::BN)) != cudaSuccess) return e;
+  if ((e = mg_tmap_bf16(&tv, V, p.D, p.Lk, BH, C::BN)) != cudaSuccess) return e;
   auto kern = accel_dkdv_pp_kernel<DP>;
   if ((e = mg_set_smem_attr(reinterpret_cast<const void *>(kern), C::SMEM_BYTES,
                             DP == 64 ? 16 : 17)) != cudaSuccess)
     return e;
-  const int nkb = (p.L + C::BN - 1) / C::BN;
+  const int nkb = (p.Lk + C::BN - 1) / C::BN;
   const long long grid = static_cast<long long>(nkb) * BH;
   kern<<<static_cast<unsigned>(grid), C::NTHREADS, C::SMEM_BYTES, st>>>(
-      tq, tk, tv, tdo, LSE, Dvec, dK, dV, BH, p.L, p.D, p.causal, p.scale, p.scale * kLog2e, err,
+      tq, tk, tv, tdo, LSE, Dvec, dK, dV, BH, p.L, p.Lk, p.D, p.causal, p.off, p.scale,
+      p.scale * kLog2e, err,
       wait_limit_ns());
   return cudaGetLastError();
 }

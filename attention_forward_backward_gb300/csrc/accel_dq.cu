@@ -80,8 +80,8 @@ __global__ void __launch_bounds__(320, 1)
                     const __grid_constant__ CUtensorMap tmdO,
                     const __grid_constant__ CUtensorMap tmK,
                     const __grid_constant__ CUtensorMap tmV, const float *__restrict__ LSE,
-                    const float *__restrict__ Dvec, float *__restrict__ dQ, int BH, int L, int D,
-                    int causal, float scale, float scale_log2, unsigned int *err,
+                    const float *__restrict__ Dvec, float *__restrict__ dQ, int BH, int L, int Lk,
+                    int D, int causal, int off, float scale, float scale_log2, unsigned int *err,
                     unsigned long long timeout_ns) {
   using C = DqCfg<DP>;
   extern __shared__ uint8_t smem_raw[];
@@ -99,8 +99,10 @@ __global__ void __launch_bounds__(320, 1)
   const int qb = nqb - 1 - static_cast<int>(blockIdx.x / BH);
   const int bh = static_cast<int>(blockIdx.x % BH);
   const int q0 = qb * C::BM;
-  const int nkt_all = (L + C::BN - 1) / C::BN;
-  const int n = causal ? min(nkt_all, (q0 + C::BM - 1) / C::BN + 1) : nkt_all;
+  // Lk key rows; causal: query i sees key j iff j <= i + off
+  const int nkt_all = (Lk + C::BN - 1) / C::BN;
+  const int last = min(q0 + C::BM, L) - 1 + off;  // last key any row of the block sees
+  const int n = !causal ? nkt_all : (last < 0 ? 0 : min(nkt_all, last / C::BN + 1));
 
   if (warp == 0) {
     tmem_alloc(smem_u32(tmem_slot), C::TMEM_COLS);
@@ -197,8 +199,8 @@ __global__ void __launch_bounds__(320, 1)
         mma_commit(bar(C::B_VEMPTY + s));  // V_j is free once dP(j) completes
         return true;
       };
-      if (ok) ok = issue_S(0);
-      if (ok) ok = issue_dP(0);
+      if (ok && n > 0) ok = issue_S(0);
+      if (ok && n > 0) ok = issue_dP(0);
       if (ok && n > 1) ok = issue_S(1);
       for (int j = 0; ok && j < n; ++j) {
         const int s = j % C::NKS;
@@ -231,7 +233,9 @@ __global__ void __launch_bounds__(320, 1)
     const uint32_t lane_off = static_cast<uint32_t>(32 * (warp & 3)) << 16;
     const float lse2 = vrow ? LSE[static_cast<size_t>(bh) * L + qrow] * kLog2e : INFINITY;
     const float dvr = vrow ? Dvec[static_cast<size_t>(bh) * L + qrow] : 0.f;
-    const int lim = causal ? min(L - 1, qrow) : (L - 1);  // last allowed key of this row
+    // last allowed key of this row (negative: none, the row's softmax is empty and
+    // every P is masked to 0 after the exponential)
+    const int lim = causal ? min(Lk - 1, qrow + off) : (Lk - 1);
     bool ok = true;
     for (int j = 0; j < n; ++j) {
       const int k0 = j * C::BN + 64 * g;
@@ -276,6 +280,12 @@ __global__ void __launch_bounds__(320, 1)
       if (lane == 0) mbar_arrive(bar(C::B_DSREADY + (j & 1)));
     }
     if (ok && n > 0) ok = mbar_wait_warp(bar(C::B_DQDONE), 0, ab);
+    if (ok && n == 0 && vrow) {
+      // no key tile for this query block: dQ = 0 (warpgroup g writes its half)
+      float *row = dQ + (static_cast<size_t>(bh) * L + qrow) * D;
+      for (int c = 0; c < DP / 2 && g * (DP / 2) + c < D; c += 4)
+        *reinterpret_cast<float4 *>(row + g * (DP / 2) + c) = make_float4(0.f, 0.f, 0.f, 0.f);
+    }
     if (ok && n > 0) {
       tc_fence_after();
       float *row = dQ + (static_cast<size_t>(bh) * L + (vrow ? qrow : 0)) * D;
@@ -326,8 +336,8 @@ cudaError_t launch(const __nv_bfloat16 *Q, const __nv_bfloat16 *K, const __nv_bf
   cudaError_t e;
   if ((e = mg_tmap_bf16(&tq, Q, p.D, p.L, BH, C::BM)) != cudaSuccess) return e;
   if ((e = mg_tmap_bf16(&tdo, dO, p.D, p.L, BH, C::BM)) != cudaSuccess) return e;
-  if ((e = mg_tmap_bf16(&tk, K, p.D, p.L, BH, C::BN)) != cudaSuccess) return e;
-  if ((e = mg_tmap_bf16(&tv, V, p.D, p.L, BH, C::BN)) != cudaSuccess) return e;
+  if ((e = mg_tmap_bf16(&tk, K, p.D, p.Lk, BH, C::BN)) != cudaSuccess) return e;
+  if ((e = mg_tmap_bf16(&tv, V, p.D, p.Lk, BH, C::BN)) != cudaSuccess) return e;
   auto kern = accel_dq_kernel<DP>;
   if ((e = mg_set_smem_attr(reinterpret_cast<const void *>(kern), C::SMEM_BYTES,
                             DP == 64 ? 10 : 11)) != cudaSuccess)
@@ -335,7 +345,8 @@ cudaError_t launch(const __nv_bfloat16 *Q, const __nv_bfloat16 *K, const __nv_bf
   const int nqb = (p.L + C::BM - 1) / C::BM;
   const long long grid = static_cast<long long>(nqb) * BH;
   kern<<<static_cast<unsigned>(grid), C::NTHREADS, C::SMEM_BYTES, st>>>(
-      tq, tdo, tk, tv, LSE, Dvec, dQ, BH, p.L, p.D, p.causal, p.scale, p.scale * kLog2e, err,
+      tq, tdo, tk, tv, LSE, Dvec, dQ, BH, p.L, p.Lk, p.D, p.causal, p.off, p.scale,
+      p.scale * kLog2e, err,
       wait_limit_ns());
   return cudaGetLastError();
 }

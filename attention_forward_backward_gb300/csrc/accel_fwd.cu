@@ -82,8 +82,9 @@ __global__ void __launch_bounds__(320, 1)
     accel_fwd_kernel(const __grid_constant__ CUtensorMap tmQ,
                      const __grid_constant__ CUtensorMap tmK,
                      const __grid_constant__ CUtensorMap tmV, float *__restrict__ O,
-                     float *__restrict__ LSE, int BH, int L, int D, int causal, float scale_log2,
-                     unsigned int *err, unsigned long long timeout_ns, int fault) {
+                     float *__restrict__ LSE, int BH, int L, int Lk, int D, int causal, int off,
+                     float scale_log2, unsigned int *err, unsigned long long timeout_ns,
+                     int fault) {
   using C = FwdCfg<DP>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
@@ -100,11 +101,14 @@ __global__ void __launch_bounds__(320, 1)
   const int qb = nqb - 1 - static_cast<int>(blockIdx.x / BH);
   const int bh = static_cast<int>(blockIdx.x % BH);
   const int q0 = qb * 256;
-  const int nkt = (L + C::BN - 1) / C::BN;
+  // key tiles of each query tile: Lk keys; causal: query i sees key j iff j <= i + off
+  const int nkt = (Lk + C::BN - 1) / C::BN;
   int nT[2];
-  nT[0] = causal ? min(nkt, (q0 + 128) / C::BN) : nkt;
-  nT[1] = causal ? min(nkt, (q0 + 256) / C::BN) : nkt;
-  const int nmax = nT[1];
+  for (int q = 0; q < 2; ++q) {
+    const int last = min(q0 + (q + 1) * C::BM, L) - 1 + off;  // last key the tile's rows see
+    nT[q] = !causal ? nkt : (last < 0 ? 0 : min(nkt, last / C::BN + 1));
+  }
+  const int nmax = max(nT[0], nT[1]);
 
   if (warp == 0) {
     tmem_alloc(smem_u32(tmem_slot), C::TMEM_COLS);
@@ -212,8 +216,8 @@ __global__ void __launch_bounds__(320, 1)
         mma_commit(bar(C::B_ODONE + q));
         return true;
       };
-      if (ok) ok = issue_S(0, 0);
-      if (ok) ok = issue_S(1, 0);
+      if (ok && nT[0] > 0) ok = issue_S(0, 0);
+      if (ok && nT[1] > 0) ok = issue_S(1, 0);
       for (int j = 0; ok && j < nmax; ++j) {
         if (j < nT[0]) {
           ok = issue_PV(0, j);
@@ -243,8 +247,10 @@ __global__ void __launch_bounds__(320, 1)
       if (!ok) break;
       tc_fence_after();
       const int k0 = j * C::BN;
-      const bool need_mask = (k0 + C::BN > L) || (causal && k0 + C::BN - 1 > q0 + q * C::BM);
-      const int lim = causal ? min(L - 1, qrow) : (L - 1);  // last allowed key of this row
+      const bool need_mask =
+          (k0 + C::BN > Lk) || (causal && k0 + C::BN - 1 > q0 + q * C::BM + off);
+      // last allowed key of this row (negative: none)
+      const int lim = causal ? min(Lk - 1, qrow + off) : (Lk - 1);
       // One pass: all 128 scores of the row in flight, a single wait.
       uint32_t r[128];
 #pragma unroll
@@ -262,18 +268,20 @@ __global__ void __launch_bounds__(320, 1)
       const bool need = mx2 > m_ref + 8.f;
       const bool warp_need = __any_sync(0xffffffffu, need);
       const float m_new = warp_need ? fmaxf(m_ref, mx2) : m_ref;
+      // a row that has seen no allowed key yet keeps m = -inf; its P is 0
+      const float m_use = m_new == -INFINITY ? 0.f : m_new;
       // P = exp2(s * scale * log2e - m_new), packed to bf16 (masked scores are -inf -> 0)
       uint32_t pk[64];
       float rs = 0.f;
 #pragma unroll
       for (int e = 0; e < 64; ++e) {
-        const float p0 = ex2(fmaf(__uint_as_float(r[2 * e]), scale_log2, -m_new));
-        const float p1 = ex2(fmaf(__uint_as_float(r[2 * e + 1]), scale_log2, -m_new));
+        const float p0 = ex2(fmaf(__uint_as_float(r[2 * e]), scale_log2, -m_use));
+        const float p1 = ex2(fmaf(__uint_as_float(r[2 * e + 1]), scale_log2, -m_use));
         rs += p0 + p1;
         pk[e] = pack_bf16(p0, p1);
       }
       if (warp_need) {
-        const float alpha = ex2(m_ref - m_new);
+        const float alpha = m_new == -INFINITY ? 1.f : ex2(m_ref - m_new);
         if (j > 0) {
           // O holds the sum up to tile j-1: wait for that P V, then rescale.
           ok = mbar_wait_warp(bar(C::B_ODONE + q), (j - 1) & 1, ab);
@@ -301,9 +309,16 @@ __global__ void __launch_bounds__(320, 1)
       mbar_arrive(bar(C::B_PREADY + q));
     }
     if (ok && n > 0) ok = mbar_wait_warp(bar(C::B_ODONE + q), (n - 1) & 1, ab);
+    if (ok && n == 0 && qrow < L) {
+      // no key tile at all for this query tile: every row has an empty softmax
+      float *orow = O + (static_cast<size_t>(bh) * L + qrow) * D;
+      for (int c = 0; c < D; c += 4)
+        *reinterpret_cast<float4 *>(orow + c) = make_float4(0.f, 0.f, 0.f, 0.f);
+      LSE[static_cast<size_t>(bh) * L + qrow] = -INFINITY;
+    }
     if (ok && n > 0) {
       tc_fence_after();
-      const float inv = 1.f / l;
+      const float inv = l > 0.f ? 1.f / l : 0.f;  // l = 0: no allowed key, O = 0
       const bool valid = qrow < L;
       float *orow = O + (static_cast<size_t>(bh) * L + (valid ? qrow : 0)) * D;
 #pragma unroll
@@ -321,7 +336,8 @@ __global__ void __launch_bounds__(320, 1)
           }
         }
       }
-      if (valid) LSE[static_cast<size_t>(bh) * L + qrow] = (m_ref + log2f(l)) * kLn2;
+      if (valid)
+        LSE[static_cast<size_t>(bh) * L + qrow] = l > 0.f ? (m_ref + log2f(l)) * kLn2 : -INFINITY;
     }
   }
 
@@ -365,8 +381,8 @@ cudaError_t launch(const __nv_bfloat16 *Q, const __nv_bfloat16 *K, const __nv_bf
   CUtensorMap tq, tk, tv;
   cudaError_t e;
   if ((e = mg_tmap_bf16(&tq, Q, p.D, p.L, BH, C::BM)) != cudaSuccess) return e;
-  if ((e = mg_tmap_bf16(&tk, K, p.D, p.L, BH, C::BN)) != cudaSuccess) return e;
-  if ((e = mg_tmap_bf16(&tv, V, p.D, p.L, BH, C::BN)) != cudaSuccess) return e;
+  if ((e = mg_tmap_bf16(&tk, K, p.D, p.Lk, BH, C::BN)) != cudaSuccess) return e;
+  if ((e = mg_tmap_bf16(&tv, V, p.D, p.Lk, BH, C::BN)) != cudaSuccess) return e;
   auto kern = accel_fwd_kernel<DP>;
   if ((e = mg_set_smem_attr(reinterpret_cast<const void *>(kern), C::SMEM_BYTES,
                             DP == 64 ? 6 : 7)) != cudaSuccess)
@@ -374,8 +390,8 @@ cudaError_t launch(const __nv_bfloat16 *Q, const __nv_bfloat16 *K, const __nv_bf
   const int nqb = (p.L + 255) / 256;
   const long long grid = static_cast<long long>(nqb) * BH;
   kern<<<static_cast<unsigned>(grid), C::NTHREADS, C::SMEM_BYTES, st>>>(
-      tq, tk, tv, O, LSE, BH, p.L, p.D, p.causal, p.scale * kLog2e, err, wait_limit_ns(),
-      fault_mode());
+      tq, tk, tv, O, LSE, BH, p.L, p.Lk, p.D, p.causal, p.off, p.scale * kLog2e, err,
+      wait_limit_ns(), fault_mode());
   return cudaGetLastError();
 }
 

@@ -104,15 +104,23 @@ struct Range {
 };
 bool overlap(Range a, Range b) { return a.lo < b.hi && b.lo < a.hi; }
 
-int check_common(int B, int H, int L, int D, int causal, float scale, int contract) {
-  if (B < 1 || H < 1 || L < 1) return MG_ERR_INVALID_ARG;
-  if (static_cast<long long>(B) * H > (1LL << 24) || L > (1 << 20)) return MG_ERR_INVALID_ARG;
-  if (causal != 0 && causal != 1) return MG_ERR_INVALID_ARG;
+int check_common(int B, int H, int Lq, int Lk, int D, int mask, float scale, int contract) {
+  if (B < 1 || H < 1 || Lq < 1 || Lk < 1) return MG_ERR_INVALID_ARG;
+  if (static_cast<long long>(B) * H > (1LL << 24) || Lq > (1 << 20) || Lk > (1 << 20))
+    return MG_ERR_INVALID_ARG;
+  if (mask != MG_MASK_NONE && mask != MG_MASK_CAUSAL && mask != MG_MASK_CAUSAL_BOTTOM_RIGHT)
+    return MG_ERR_INVALID_ARG;
   if (!(scale > 0.f) || !isfinite(scale)) return MG_ERR_INVALID_ARG;
   if (contract != MG_CONTRACT_STRICT_F32 && contract != MG_CONTRACT_ACCEL_BF16)
     return MG_ERR_INVALID_ARG;
   if (D != 32 && D != 64 && D != 128) return MG_ERR_UNSUPPORTED;
   return MG_OK;
+}
+
+MgProblem make_problem(int B, int H, int Lq, int Lk, int D, int mask, float scale) {
+  MgProblem p{B, H, Lq, D, mask != MG_MASK_NONE ? 1 : 0, scale, Lk, 0};
+  if (mask == MG_MASK_CAUSAL_BOTTOM_RIGHT) p.off = Lk - Lq;
+  return p;
 }
 
 int check_ptrs(const void *const *ptrs, int n) {
@@ -177,19 +185,21 @@ const char *mg_status_string(int status) {
   }
 }
 
-int mg_attn_fwd(const void *Q, const void *K, const void *V, void *O, float *LSE, int B, int H,
-                int L, int D, int causal, float scale, int contract, void *stream) {
-  int rc = check_common(B, H, L, D, causal, scale, contract);
+int mg_attn_fwd_ex(const void *Q, const void *K, const void *V, void *O, float *LSE, int B,
+                   int H, int Lq, int Lk, int D, int mask, float scale, int contract,
+                   void *stream) {
+  int rc = check_common(B, H, Lq, Lk, D, mask, scale, contract);
   if (rc) return rc;
   const void *ptrs[] = {Q, K, V, O, LSE};
   if ((rc = check_ptrs(ptrs, 5))) return rc;
-  const size_t n = static_cast<size_t>(B) * H * L * D;
+  const size_t nq = static_cast<size_t>(B) * H * Lq * D;
+  const size_t nk = static_cast<size_t>(B) * H * Lk * D;
   const size_t in_el = contract == MG_CONTRACT_STRICT_F32 ? 4 : 2;
-  const Range in[] = {rng(Q, n * in_el), rng(K, n * in_el), rng(V, n * in_el)};
-  const Range out[] = {rng(O, n * 4), rng(LSE, static_cast<size_t>(B) * H * L * 4)};
+  const Range in[] = {rng(Q, nq * in_el), rng(K, nk * in_el), rng(V, nk * in_el)};
+  const Range out[] = {rng(O, nq * 4), rng(LSE, static_cast<size_t>(B) * H * Lq * 4)};
   if ((rc = check_alias(in, 3, out, 2))) return rc;
 
-  const MgProblem p{B, H, L, D, causal, scale};
+  const MgProblem p = make_problem(B, H, Lq, Lk, D, mask, scale);
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   cudaError_t e;
   if (contract == MG_CONTRACT_STRICT_F32) {
@@ -208,31 +218,53 @@ int mg_attn_fwd(const void *Q, const void *K, const void *V, void *O, float *LSE
   return map_cuda(e);
 }
 
+int mg_attn_fwd(const void *Q, const void *K, const void *V, void *O, float *LSE, int B, int H,
+                int L, int D, int causal, float scale, int contract, void *stream) {
+  if (causal != 0 && causal != 1) return MG_ERR_INVALID_ARG;
+  return mg_attn_fwd_ex(Q, K, V, O, LSE, B, H, L, L, D, causal ? MG_MASK_CAUSAL : MG_MASK_NONE,
+                        scale, contract, stream);
+}
+
+size_t mg_attn_bwd_workspace_bytes_ex(int B, int H, int Lq, int Lk, int D, int contract) {
+  if (check_common(B, H, Lq, Lk, D, MG_MASK_NONE, 1.f, contract) != MG_OK) return 0;
+  return ws_bytes(B, H, Lq);
+}
+
 size_t mg_attn_bwd_workspace_bytes(int B, int H, int L, int D, int contract) {
-  if (check_common(B, H, L, D, 0, 1.f, contract) != MG_OK) return 0;
-  return ws_bytes(B, H, L);
+  return mg_attn_bwd_workspace_bytes_ex(B, H, L, L, D, contract);
 }
 
 int mg_attn_bwd(const void *Q, const void *K, const void *V, const void *O, const void *dO,
                 const float *LSE, void *dQ, void *dK, void *dV, int B, int H, int L, int D,
                 int causal, float scale, int contract, void *workspace, size_t workspace_bytes,
                 void *stream) {
-  int rc = check_common(B, H, L, D, causal, scale, contract);
+  if (causal != 0 && causal != 1) return MG_ERR_INVALID_ARG;
+  return mg_attn_bwd_ex(Q, K, V, O, dO, LSE, dQ, dK, dV, B, H, L, L, D,
+                        causal ? MG_MASK_CAUSAL : MG_MASK_NONE, scale, contract, workspace,
+                        workspace_bytes, stream);
+}
+
+int mg_attn_bwd_ex(const void *Q, const void *K, const void *V, const void *O, const void *dO,
+                   const float *LSE, void *dQ, void *dK, void *dV, int B, int H, int Lq, int Lk,
+                   int D, int mask, float scale, int contract, void *workspace,
+                   size_t workspace_bytes, void *stream) {
+  int rc = check_common(B, H, Lq, Lk, D, mask, scale, contract);
   if (rc) return rc;
   const void *ptrs[] = {Q, K, V, O, dO, LSE, dQ, dK, dV};
   if ((rc = check_ptrs(ptrs, 9))) return rc;
-  if (!workspace || !aligned16(workspace) || workspace_bytes < ws_bytes(B, H, L))
+  if (!workspace || !aligned16(workspace) || workspace_bytes < ws_bytes(B, H, Lq))
     return MG_ERR_WORKSPACE;
-  const size_t n = static_cast<size_t>(B) * H * L * D;
-  const size_t rows = static_cast<size_t>(B) * H * L;
+  const size_t n = static_cast<size_t>(B) * H * Lq * D;   // Q, O, dO, dQ
+  const size_t nk = static_cast<size_t>(B) * H * Lk * D;  // K, V, dK, dV
+  const size_t rows = static_cast<size_t>(B) * H * Lq;
   const size_t in_el = contract == MG_CONTRACT_STRICT_F32 ? 4 : 2;
-  const Range in[] = {rng(Q, n * in_el), rng(K, n * in_el), rng(V, n * in_el),
+  const Range in[] = {rng(Q, n * in_el), rng(K, nk * in_el), rng(V, nk * in_el),
                       rng(dO, n * in_el), rng(O, n * 4),      rng(LSE, rows * 4)};
-  const Range out[] = {rng(dQ, n * 4), rng(dK, n * 4), rng(dV, n * 4),
-                       rng(workspace, ws_bytes(B, H, L))};
+  const Range out[] = {rng(dQ, n * 4), rng(dK, nk * 4), rng(dV, nk * 4),
+                       rng(workspace, ws_bytes(B, H, Lq))};
   if ((rc = check_alias(in, 6, out, 4))) return rc;
 
-  const MgProblem p{B, H, L, D, causal, scale};
+  const MgProblem p = make_problem(B, H, Lq, Lk, D, mask, scale);
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   float *Dvec = static_cast<float *>(workspace);
   cudaError_t e;

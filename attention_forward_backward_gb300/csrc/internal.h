@@ -6,10 +6,15 @@
 #include <cuda_bf16.h>
 #include <stdint.h>
 
+// One attention problem. L is the number of query rows (Lq), Lk the number of
+// key rows. With causal set, query i may see key j iff j <= i + off, where off
+// is 0 for the top-left alignment and Lk - Lq for the bottom-right one.
 struct MgProblem {
   int B, H, L, D;
   int causal;
   float scale;
+  int Lk;
+  int off;
 };
 
 // Kernel ids, in the order mg_attn_kernel_name() reports them.

@@ -43,7 +43,8 @@ __global__ void __launch_bounds__(256, 1)
                        const float *__restrict__ V, const float *__restrict__ dO,
                        const float *__restrict__ LSE, const float *__restrict__ Dvec,
                        float *__restrict__ dQ, float *__restrict__ dK, float *__restrict__ dV,
-                       int BH, int L, int causal, float scale, float scale_log2) {
+                       int BH, int L, int Lk, int causal, int off, float scale,
+                       float scale_log2) {
   using C = BwdCfg<D>;
   using VecV = typename VecT<C::VW>::T;
   extern __shared__ float4 smem_f4[];
@@ -60,17 +61,21 @@ __global__ void __launch_bounds__(256, 1)
   const int kt = static_cast<int>(blockIdx.x / BH);  // heaviest (kt = 0) first
   const int bh = static_cast<int>(blockIdx.x % BH);
   const int k0 = kt * C::BC;
+  // query rows L, key rows Lk; causal: query i sees key j iff j <= i + off
   const size_t head = static_cast<size_t>(bh) * L * D;
-  const float *Qh = Q + head, *Kh = K + head, *Vh = V + head, *dOh = dO + head;
+  const size_t khead = static_cast<size_t>(bh) * Lk * D;
+  const float *Qh = Q + head, *Kh = K + khead, *Vh = V + khead, *dOh = dO + head;
   const float *Lh = LSE + static_cast<size_t>(bh) * L, *Dh = Dvec + static_cast<size_t>(bh) * L;
   float *dQh = dQ + head;
 
   const int tid = threadIdx.x, tx = tid & 15, ty = tid >> 4;
   const int nqt = (L + C::BR - 1) / C::BR;
-  const int qt0 = causal ? kt : 0;  // BR == BC: tile kt holds the first queries that see key k0
+  // first query tile holding a query that sees key k0 (none past nqt: the key
+  // block then keeps dK = dV = 0)
+  const int qt0 = causal ? max(0, k0 - off) / C::BR : 0;
 
-  stage_rows<D, 64, C::NT>(sK, C::RS, Kh, k0, L, tid);
-  stage_rows<D, 64, C::NT>(sV, C::RS, Vh, k0, L, tid);
+  stage_rows<D, 64, C::NT>(sK, C::RS, Kh, k0, Lk, tid);
+  stage_rows<D, 64, C::NT>(sV, C::RS, Vh, k0, Lk, tid);
   stage_rows<D, 64, C::NT>(sQ, C::RS, Qh, qt0 * C::BR, L, tid);
   stage_rows<D, 64, C::NT>(sdO, C::RS, dOh, qt0 * C::BR, L, tid);
   stage_vec<64>(sLse, Lh, qt0 * C::BR, L, tid);
@@ -121,7 +126,8 @@ __global__ void __launch_bounds__(256, 1)
     }
 
     // ---- P^T = exp(S^T scale - LSE), dS^T = P^T (dP^T - Dvec)
-    const bool need_mask = (q0 + C::BR > L) || (k0 + C::BC > L) || (causal && q0 < k0 + C::BC - 1);
+    const bool need_mask =
+        (q0 + C::BR > L) || (k0 + C::BC > Lk) || (causal && q0 + off < k0 + C::BC - 1);
 #pragma unroll
     for (int b = 0; b < 4; ++b) {
       const int ql = tx + 16 * b;
@@ -133,7 +139,7 @@ __global__ void __launch_bounds__(256, 1)
         float p = exp2f(fmaf(st[a][b], scale_log2, -lse2));
         if (need_mask) {
           const int qg = q0 + ql, kg = k0 + kl;
-          if (qg >= L || kg >= L || (causal && kg > qg)) p = 0.f;
+          if (qg >= L || kg >= Lk || (causal && kg > qg + off)) p = 0.f;
         }
         const float ds = p * (dpt[a][b] - dvq);
         sPT[kl * C::TS + ql] = p;
@@ -233,13 +239,15 @@ __global__ void __launch_bounds__(256, 1)
     }
   }
 
+  cp_async_wait<0>();  // no copy may outlive the block (a key block with no queries)
+
   // ---- store dK (scaled) and dV for this key block
 #pragma unroll
   for (int a = 0; a < 4; ++a) {
     const int kg = k0 + ty + 16 * a;
-    if (kg < L) {
-      float *krow = dK + head + static_cast<size_t>(kg) * D;
-      float *vrow = dV + head + static_cast<size_t>(kg) * D;
+    if (kg < Lk) {
+      float *krow = dK + khead + static_cast<size_t>(kg) * D;
+      float *vrow = dV + khead + static_cast<size_t>(kg) * D;
 #pragma unroll
       for (int v = 0; v < C::NV; ++v) {
         VecV kk, vv;
@@ -300,10 +308,11 @@ cudaError_t launch_dkdv(const float *Q, const float *K, const float *V, const fl
                                    D == 32 ? 3 : (D == 64 ? 4 : 5));
   if (e != cudaSuccess) return e;
   const int BH = p.B * p.H;
-  const int nkt = (p.L + C::BC - 1) / C::BC;
+  const int nkt = (p.Lk + C::BC - 1) / C::BC;
   const long long grid = static_cast<long long>(nkt) * BH;
   kern<<<static_cast<unsigned>(grid), C::NT, C::SMEM_BYTES, st>>>(
-      Q, K, V, dO, LSE, Dvec, dQ, dK, dV, BH, p.L, p.causal, p.scale, p.scale * kLog2e);
+      Q, K, V, dO, LSE, Dvec, dQ, dK, dV, BH, p.L, p.Lk, p.causal, p.off, p.scale,
+      p.scale * kLog2e);
   return cudaGetLastError();
 }
 

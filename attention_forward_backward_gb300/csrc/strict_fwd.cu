@@ -40,7 +40,8 @@ template <int D>
 __global__ void __launch_bounds__(256, 1)
     strict_fwd_kernel(const float *__restrict__ Q, const float *__restrict__ K,
                       const float *__restrict__ V, float *__restrict__ O,
-                      float *__restrict__ LSE, int BH, int L, int causal, float scale_log2) {
+                      float *__restrict__ LSE, int BH, int L, int Lk, int causal, int off,
+                      float scale_log2) {
   using C = FwdCfg<D>;
   using VecV = typename VecT<C::VW>::T;
   extern __shared__ float4 smem_f4[];
@@ -54,18 +55,23 @@ __global__ void __launch_bounds__(256, 1)
   const int qt = nqt - 1 - static_cast<int>(blockIdx.x / BH);
   const int bh = static_cast<int>(blockIdx.x % BH);
   const int q0 = qt * C::BR;
+  // query rows L, key rows Lk; causal: query i sees key j iff j <= i + off
   const size_t head = static_cast<size_t>(bh) * L * D;
-  const float *Qh = Q + head, *Kh = K + head, *Vh = V + head;
+  const size_t khead = static_cast<size_t>(bh) * Lk * D;
+  const float *Qh = Q + head, *Kh = K + khead, *Vh = V + khead;
 
   const int tid = threadIdx.x, tx = tid & 15, ty = tid >> 4;
 
-  int nkt = (L + C::BC - 1) / C::BC;
-  if (causal) nkt = min(nkt, (min(q0 + C::BR, L) - 1) / C::BC + 1);
+  int nkt = (Lk + C::BC - 1) / C::BC;
+  if (causal) {
+    const int last = min(q0 + C::BR, L) - 1 + off;  // last key any row of the tile sees
+    nkt = last < 0 ? 0 : min(nkt, last / C::BC + 1);
+  }
 
   stage_rows<D, C::BR, C::NT>(sQ, C::QS, Qh, q0, L, tid);
-  stage_rows<D, C::BC, C::NT>(sK, C::KS, Kh, 0, L, tid);
+  stage_rows<D, C::BC, C::NT>(sK, C::KS, Kh, 0, Lk, tid);
   cp_async_commit();
-  stage_rows<D, C::BC, C::NT>(sV, C::VS, Vh, 0, L, tid);
+  stage_rows<D, C::BC, C::NT>(sV, C::VS, Vh, 0, Lk, tid);
   cp_async_commit();
 
   float o[8][C::DPT];
@@ -109,12 +115,12 @@ __global__ void __launch_bounds__(256, 1)
     }
     __syncthreads();  // every thread is done reading sK
     if (kt + 1 < nkt) {
-      stage_rows<D, C::BC, C::NT>(sK, C::KS, Kh, k0 + C::BC, L, tid);
+      stage_rows<D, C::BC, C::NT>(sK, C::KS, Kh, k0 + C::BC, Lk, tid);
       cp_async_commit();
     }
 
     // ---- online softmax (base 2), P tile to shared memory
-    const bool need_mask = (k0 + C::BC > L) || (causal && k0 + C::BC - 1 > q0);
+    const bool need_mask = (k0 + C::BC > Lk) || (causal && k0 + C::BC - 1 > q0 + off);
     float alpha[8];
 #pragma unroll
     for (int i = 0; i < 8; ++i) {
@@ -125,7 +131,7 @@ __global__ void __launch_bounds__(256, 1)
         float v = s[i][j] * scale_log2;
         if (need_mask) {
           const int kj = k0 + tx + 16 * j;
-          if (kj >= L || (causal && kj > qi)) v = -CUDART_INF_F;
+          if (kj >= Lk || (causal && kj > qi + off)) v = -CUDART_INF_F;
         }
         s[i][j] = v;
         mx = fmaxf(mx, v);
@@ -183,18 +189,21 @@ __global__ void __launch_bounds__(256, 1)
     }
     __syncthreads();  // every thread is done reading sV
     if (kt + 1 < nkt) {
-      stage_rows<D, C::BC, C::NT>(sV, C::VS, Vh, k0 + C::BC, L, tid);
+      stage_rows<D, C::BC, C::NT>(sV, C::VS, Vh, k0 + C::BC, Lk, tid);
       cp_async_commit();
     }
   }
 
-  // ---- epilogue: O = O_acc / l, LSE = ln 2 * (m + log2 l)
+  cp_async_wait<0>();  // no copy may outlive the block (a tile with no keys skips the loop)
+
+  // ---- epilogue: O = O_acc / l, LSE = ln 2 * (m + log2 l); a row without any
+  // allowed key (l = 0) gets O = 0 and LSE = -inf
 #pragma unroll
   for (int i = 0; i < 8; ++i) {
     const float lt = group_sum<16>(l[i]);
     const int qi = q0 + ty + 16 * i;
     if (qi < L) {
-      const float inv = 1.f / lt;
+      const float inv = lt > 0.f ? 1.f / lt : 0.f;
       float *orow = O + head + static_cast<size_t>(qi) * D;
 #pragma unroll
       for (int v = 0; v < C::NV; ++v) {
@@ -220,8 +229,8 @@ cudaError_t launch(const float *Q, const float *K, const float *V, float *O, flo
   const int BH = p.B * p.H;
   const int nqt = (p.L + C::BR - 1) / C::BR;
   const long long grid = static_cast<long long>(nqt) * BH;
-  kern<<<static_cast<unsigned>(grid), C::NT, C::SMEM_BYTES, st>>>(Q, K, V, O, LSE, BH, p.L,
-                                                                  p.causal, p.scale * kLog2e);
+  kern<<<static_cast<unsigned>(grid), C::NT, C::SMEM_BYTES, st>>>(
+      Q, K, V, O, LSE, BH, p.L, p.Lk, p.causal, p.off, p.scale * kLog2e);
   return cudaGetLastError();
 }
 

@@ -155,3 +155,21 @@ def custom_workload(B, H, L, D, causal, seed_cfg=900, qk_gain=1.0) -> Workload:
     """An ad-hoc workload (edge cases in tests) with its own seed block."""
     return Workload(seed_cfg, B, H, L, D, bool(causal), ("strict", "accel"), qk_gain,
                     name=f"custom B{B} H{H} L{L} D{D} {'causal' if causal else 'full'}")
+
+
+def cross_inputs(B, H, Lq, Lk, D, contract: str, seed_cfg: int = 950):
+    """Seeded inputs with Lq query rows and Lk key rows (cross attention): Q and
+    dO are [B, H, Lq, D], K and V [B, H, Lk, D]; same generator, seeds and
+    formats as ``inputs``."""
+    out = {}
+    for t in ("Q", "K", "V", "dO"):
+        rows = Lq if t in ("Q", "dO") else Lk
+        x = normal_f32(1000 * seed_cfg + TENSOR_IDS[t], B * H * rows * D).reshape(B, H, rows, D)
+        if contract == "strict":
+            out[t] = x
+        elif contract == "accel":
+            bits = round_to_bf16(x)
+            out[t] = {"bits": bits, "values": bf16_bits_to_f32(bits)}
+        else:
+            raise ValueError(contract)
+    return out

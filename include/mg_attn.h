@@ -33,7 +33,15 @@
  *
  * Layout. Q, K, V, O, dO, dQ, dK, dV are dense row-major [B][H][L][D] (D
  * innermost, no padding, no strides). LSE (and the workspace's Dvec) are
- * [B][H][L] f32. Lq = Lk = L.
+ * [B][H][L] f32. The self-attention calls take Lq = Lk = L; the _ex calls take
+ * Q, O, dO, dQ as [B][H][Lq][D], K, V, dK, dV as [B][H][Lk][D] and LSE as
+ * [B][H][Lq] (cross attention), with a mask of mg_mask_t:
+ *   MG_MASK_NONE                 every key allowed
+ *   MG_MASK_CAUSAL               allowed(i,j) = (j <= i)           (top-left)
+ *   MG_MASK_CAUSAL_BOTTOM_RIGHT  allowed(i,j) = (j <= i + Lk - Lq) (the last
+ *                                query sees every key)
+ * A query row with no allowed key (bottom-right with Lq > Lk) has an empty
+ * softmax: O row 0, LSE -inf, and no contribution to any gradient.
  *
  * Ownership. The caller owns every buffer (device memory, e.g. from PyTorch).
  * The library never allocates or frees device memory on these calls; the
@@ -48,9 +56,10 @@
  * Nothing aborts the process.
  *
  * Preconditions checked: pointers non-NULL and 16-byte aligned; B, H, L >= 1;
- * B*H <= 2^24, L <= 2^20; D in {32, 64, 128} (else MG_ERR_UNSUPPORTED);
- * causal in {0, 1}; scale finite and > 0; contract valid; no output buffer
- * overlaps an input buffer or another output.
+ * B*H <= 2^24, L (Lq, Lk) <= 2^20; D in {32, 64, 128} (else
+ * MG_ERR_UNSUPPORTED); causal in {0, 1} (mask one of mg_mask_t); scale finite
+ * and > 0; contract valid; no output buffer overlaps an input buffer or
+ * another output.
  */
 #ifndef MG_ATTN_H
 #define MG_ATTN_H
@@ -65,6 +74,12 @@ typedef enum {
   MG_CONTRACT_STRICT_F32 = 0,
   MG_CONTRACT_ACCEL_BF16 = 1
 } mg_contract_t;
+
+typedef enum {
+  MG_MASK_NONE = 0,
+  MG_MASK_CAUSAL = 1,              /* j <= i (top-left aligned) */
+  MG_MASK_CAUSAL_BOTTOM_RIGHT = 2  /* j <= i + Lk - Lq */
+} mg_mask_t;
 
 typedef enum {
   MG_OK = 0,
@@ -85,6 +100,16 @@ typedef enum {
 int mg_attn_fwd(const void *Q, const void *K, const void *V, void *O, float *LSE,
                 int B, int H, int L, int D, int causal, float scale, int contract,
                 void *stream);
+
+/*
+ * Forward with Lq query rows and Lk key rows (cross attention) and a mask of
+ * mg_mask_t. Q, O [B][H][Lq][D]; K, V [B][H][Lk][D]; LSE [B][H][Lq]. Same
+ * contracts, ownership and errors as mg_attn_fwd, which is this call with
+ * Lq = Lk = L and mask = causal ? MG_MASK_CAUSAL : MG_MASK_NONE.
+ */
+int mg_attn_fwd_ex(const void *Q, const void *K, const void *V, void *O, float *LSE,
+                   int B, int H, int Lq, int Lk, int D, int mask, float scale, int contract,
+                   void *stream);
 
 /* Bytes of device workspace mg_attn_bwd needs for this shape (holds Dvec,
  * [B][H][L] f32, rounded up to 256 bytes). 0 for invalid arguments. */
@@ -112,6 +137,24 @@ int mg_attn_bwd(const void *Q, const void *K, const void *V, const void *O,
                 const void *dO, const float *LSE, void *dQ, void *dK, void *dV,
                 int B, int H, int L, int D, int causal, float scale, int contract,
                 void *workspace, size_t workspace_bytes, void *stream);
+
+/* Workspace bytes for mg_attn_bwd_ex (Dvec is [B][H][Lq] f32, rounded up to
+ * 256 bytes). 0 for invalid arguments. */
+size_t mg_attn_bwd_workspace_bytes_ex(int B, int H, int Lq, int Lk, int D, int contract);
+
+/*
+ * Backward with Lq query rows and Lk key rows and a mask of mg_mask_t, given
+ * the O and LSE of mg_attn_fwd_ex with the same arguments. Q, O, dO, dQ
+ * [B][H][Lq][D]; K, V, dK, dV [B][H][Lk][D]; LSE [B][H][Lq]; workspace of at
+ * least mg_attn_bwd_workspace_bytes_ex() bytes. Same contracts, steps,
+ * ownership and errors as mg_attn_bwd, which is this call with Lq = Lk = L and
+ * mask = causal ? MG_MASK_CAUSAL : MG_MASK_NONE. Key rows that no query may
+ * see get dK = dV = 0; query rows with an empty softmax get dQ = 0.
+ */
+int mg_attn_bwd_ex(const void *Q, const void *K, const void *V, const void *O,
+                   const void *dO, const float *LSE, void *dQ, void *dK, void *dV,
+                   int B, int H, int Lq, int Lk, int D, int mask, float scale, int contract,
+                   void *workspace, size_t workspace_bytes, void *stream);
 
 /*
  * mg_attn_bwd without a workspace, for callers that cannot allocate device

@@ -95,3 +95,44 @@ def compare(got: dict, ref: dict, contract: str, keys=("O", "dQ", "dK", "dV")):
 
 def workload_inputs(w: synth.Workload, contract: str):
     return synth.inputs(w, contract)
+
+
+def run_gpu_ex(dev: dict, mask: str, scale: float, contract: str, bwd: bool = True):
+    """Cross-attention forward (+ backward) through the _ex calls, outputs
+    poisoned with NaN first. Q, dO [B, H, Lq, D]; K, V [B, H, Lk, D]."""
+    import torch
+    Q, K, V, dO = dev["Q"], dev["K"], dev["V"], dev["dO"]
+    B, H, Lq, D = Q.shape
+    Lk = K.shape[2]
+    nan = float("nan")
+    O = torch.full((B, H, Lq, D), nan, device=Q.device)
+    LSE = torch.full((B, H, Lq), nan, device=Q.device)
+    mg.mg_attn_fwd_ex(Q, K, V, O, LSE, mask, scale, contract)
+    out = {"O": O, "LSE": LSE}
+    if bwd:
+        dQ = torch.full((B, H, Lq, D), nan, device=Q.device)
+        dK = torch.full((B, H, Lk, D), nan, device=Q.device)
+        dV = torch.full((B, H, Lk, D), nan, device=Q.device)
+        nbytes = mg.mg_attn_bwd_workspace_bytes_ex(B, H, Lq, Lk, D, contract)
+        ws = torch.full((nbytes // 4,), nan, device=Q.device)
+        mg.mg_attn_bwd_ex(Q, K, V, O, dO, LSE, dQ, dK, dV, mask, scale, contract, ws)
+        out.update(dQ=dQ, dK=dK, dV=dV)
+    torch.cuda.synchronize()
+    assert mg.mg_get_device_error() == mg.MG_OK
+    return {k: v.cpu().numpy() for k, v in out.items()}
+
+
+def compare_ex(got: dict, ref: dict, contract: str):
+    """compare() for results that may hold empty-softmax rows: LSE must be -inf
+    exactly where the oracle's is, the finite LSE values are compared as usual."""
+    errs, bad = compare({k: v for k, v in got.items() if k != "LSE"},
+                        {k: v for k, v in ref.items() if k != "LSE"}, contract)
+    if "LSE" in got:
+        empty = np.isneginf(ref["LSE"])
+        if not np.array_equal(np.isneginf(got["LSE"]), empty):
+            errs["LSE"] = float("inf")
+        else:
+            errs["LSE"] = lse_err(got["LSE"][~empty], ref["LSE"][~empty]) if (~empty).any() else 0.0
+        if not errs["LSE"] <= TOL[contract]:
+            bad = dict(bad, LSE=errs["LSE"])
+    return errs, bad
