@@ -33,6 +33,8 @@
 // issuer, 8-15 two softmax warpgroups splitting the query columns.
 // Every wait is bounded; on a give-up the CTA sets the device error word and
 // leaves through the normal teardown (own copies and MMAs drained first).
+#include <climits>
+
 #include "internal.h"
 #include "tc_common.cuh"
 #include "tmap.h"
@@ -390,6 +392,8 @@ __global__ void __launch_bounds__(512, 1)
     const int kg = k0 + kr;
     const uint32_t lane_off = static_cast<uint32_t>(32 * quarter) << 16;
     const uint32_t sDS = sbase + C::OFF_DS;
+    // smallest query index that may see this thread's key (past Lk: none may)
+    const int qmin = kg >= Lk ? INT_MAX : (causal ? kg - off : INT_MIN);
     bool ok = true;
     for (int i = 0; i < n; ++i) {
       const int st = i % C::NQS;
@@ -398,7 +402,10 @@ __global__ void __launch_bounds__(512, 1)
       if (!(ok = mbar_wait_warp(bar(C::B_QFULL + st), (i / C::NQS) & 1, ab))) break;
       if (!(ok = mbar_wait_warp(bar(C::B_SFULL), i & 1, ab))) break;
       tc_fence_after();
-      const bool need_mask = (kg >= Lk) || (causal && k0 + C::BN - 1 > q0 + off);
+      // query column e of this warpgroup's slice is masked iff e < lim0 (e is q - q0 - g QPW)
+      const int lim0 = qmin == INT_MIN ? INT_MIN
+                                       : (qmin == INT_MAX ? INT_MAX : qmin - (q0 + g * C::QPW));
+      const bool need_mask = lim0 > 0;
       const float *lse = sLse + st * C::BQ + g * C::QPW;
       const float *dvq = sDv + st * C::BQ + g * C::QPW;
       const uint32_t tS = tmem + lane_off + C::T_S + g * C::QPW;
@@ -418,10 +425,7 @@ __global__ void __launch_bounds__(512, 1)
 #pragma unroll
         for (int e = 0; e < 32; ++e) {
           float x = ex2(fmaf(__uint_as_float(r[e]), scale_log2, -lv[e]));
-          if (need_mask) {
-            const int qg = q0 + g * C::QPW + 32 * c + e;
-            if (kg >= Lk || (causal && kg > qg + off)) x = 0.f;
-          }
+          if (need_mask && 32 * c + e < lim0) x = 0.f;
           p[32 * c + e] = x;
         }
       }

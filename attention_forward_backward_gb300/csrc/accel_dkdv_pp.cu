@@ -26,6 +26,8 @@
 // blocks), 8 TMA producer (plus LSE/Dvec staging), 9 MMA issuer. Every wait is
 // bounded; on a give-up the CTA sets the device error word and leaves through the
 // normal teardown (own copies and MMAs drained first).
+#include <climits>
+
 #include "internal.h"
 #include "tc_common.cuh"
 #include "tmap.h"
@@ -250,6 +252,8 @@ __global__ void __launch_bounds__(320, 1)
     const uint32_t lane_off = static_cast<uint32_t>(32 * quarter) << 16;
     const uint32_t tS = tmem + lane_off + C::T_W + 128 * w;
     const uint32_t tDP = tS + 64;
+    // smallest query index that may see this thread's key (past Lk: none may)
+    const int qmin = kg >= Lk ? INT_MAX : (causal ? kg - off : INT_MIN);
     bool ok = true;
     for (int i = w; i < n; i += 2) {
       const int st = i % C::NQS;
@@ -258,7 +262,10 @@ __global__ void __launch_bounds__(320, 1)
       if (!(ok = mbar_wait_warp(bar(C::B_QFULL + st), (i / C::NQS) & 1, ab))) break;
       if (!(ok = mbar_wait_warp(bar(C::B_SFULL + w), ph, ab))) break;
       tc_fence_after();
-      const bool need_mask = (kg >= Lk) || (causal && k0 + C::BN - 1 > q0 + off);
+      // query column e of the block is masked iff e < lim0 (e is q - q0)
+      const int lim0 =
+          qmin == INT_MIN ? INT_MIN : (qmin == INT_MAX ? INT_MAX : qmin - q0);
+      const bool need_mask = lim0 > 0;
       const float *lse = sLse + st * C::BQ;
       const float *dvq = sDv + st * C::BQ;
       float p[C::BQ];
@@ -278,7 +285,7 @@ __global__ void __launch_bounds__(320, 1)
         if (need_mask) {
 #pragma unroll
           for (int e = 0; e < 64; ++e)
-            if (kg >= Lk || (causal && kg > q0 + e + off)) p[e] = 0.f;
+            if (e < lim0) p[e] = 0.f;
         }
       }
       // P^T over the first 32 columns of S^T (already read)

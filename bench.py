@@ -61,6 +61,9 @@ def parse():
     ap.add_argument("--shape", default=None,
                     help="B,H,L,D,causal: a custom seeded workload instead of --cfg "
                          "(used for small profiling captures)")
+    ap.add_argument("--cross", default=None,
+                    help="B,H,Lq,Lk,D,mask (mask: none|causal|causal_bottom_right): measure "
+                         "cross attention through the _ex calls instead of the default workload")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=15.0,
@@ -402,8 +405,90 @@ def oracle_sample(w, contract: str, target_s: float):
 
 
 # ------------------------------------------------------------------ main
+def allowed_pairs(Lq: int, Lk: int, mask: str) -> int:
+    """Number of (query, key) pairs a head's softmax covers under the mask."""
+    if mask == "none":
+        return Lq * Lk
+    off = (Lk - Lq) if mask == "causal_bottom_right" else 0
+    i = np.arange(Lq, dtype=np.int64)
+    return int(np.clip(i + off + 1, 0, Lk).sum())
+
+
+def run_cross(args):
+    """Cross attention (Lq != Lk) through mg_attn_fwd_ex / mg_attn_bwd_ex: forward
+    and forward+backward TFLOP/s per contract, counting 4 D flops per allowed
+    (query, key) pair in the forward and 2.5x that in the backward (exactly the
+    pairs the mask allows, not the causal x1/2 convention). One JSON line."""
+    import torch
+    import attention_forward_backward_gb300 as mg
+    B, H, Lq, Lk, D = (int(x) for x in args.cross.split(",")[:5])
+    mask = args.cross.split(",")[5]
+    device = torch.device("cuda", 0)
+    mg.load_library()
+    stream = torch.cuda.Stream(device)
+    s = stream.cuda_stream
+    pairs = B * H * allowed_pairs(Lq, Lk, mask)
+    f_fwd = 4.0 * D * pairs
+    f_step = 3.5 * f_fwd
+    contracts = ["accel", "strict"] if args.contract == "both" else [args.contract]
+    flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=device)
+    res = {}
+    for c in contracts:
+        host = synth.cross_inputs(B, H, Lq, Lk, D, c, seed_cfg=801)
+        dev = {}
+        for k, x in host.items():
+            if c == "strict":
+                dev[k] = torch.from_numpy(x).to(device)
+            else:
+                dev[k] = torch.from_numpy(np.ascontiguousarray(x["bits"]).view(np.int16)).view(
+                    torch.bfloat16).to(device)
+        O = torch.empty((B, H, Lq, D), dtype=torch.float32, device=device)
+        LSE = torch.empty((B, H, Lq), dtype=torch.float32, device=device)
+        dQ = torch.empty_like(O)
+        dK = torch.empty((B, H, Lk, D), dtype=torch.float32, device=device)
+        dV = torch.empty_like(dK)
+        ws = torch.empty(mg.mg_attn_bwd_workspace_bytes_ex(B, H, Lq, Lk, D, c), dtype=torch.uint8,
+                         device=device)
+        scale = D ** -0.5
+        ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True),
+               torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
+        with torch.cuda.stream(stream):
+            for i in range(args.warmup + args.steps):
+                if i >= args.warmup:
+                    flush.fill_(float(i))
+                    ev[i - args.warmup][0].record(stream)
+                mg.mg_attn_fwd_ex(dev["Q"], dev["K"], dev["V"], O, LSE, mask, scale, c, s)
+                if i >= args.warmup:
+                    ev[i - args.warmup][1].record(stream)
+                mg.mg_attn_bwd_ex(dev["Q"], dev["K"], dev["V"], O, dev["dO"], LSE, dQ, dK, dV,
+                                  mask, scale, c, ws, s)
+                if i >= args.warmup:
+                    ev[i - args.warmup][2].record(stream)
+            torch.cuda.synchronize()
+        if mg.mg_get_device_error(s) != mg.MG_OK:
+            raise RuntimeError(f"{c}: device error word set")
+        fwd = sum(a.elapsed_time(b) for a, b, _ in ev)
+        tot = sum(a.elapsed_time(e) for a, _, e in ev)
+        res[c] = {"fwd_tflops": f_fwd * args.steps / (fwd * 1e-3) / 1e12,
+                  "fwd_bwd_tflops": f_step * args.steps / (tot * 1e-3) / 1e12,
+                  "fwd_ms": fwd / args.steps, "step_ms": tot / args.steps}
+    head = "accel" if "accel" in res else "strict"
+    print(json.dumps({
+        "metric": "cross-attention fwd+bwd TFLOP/s on 1 GB300 (exact allowed pairs)",
+        "value": res[head]["fwd_bwd_tflops"], "unit": UNIT, "n_gpus": 1, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": res[head]["step_ms"], "higher_is_better": True,
+        "dtype": "bf16" if head == "accel" else "f32", "data": "synthetic",
+        "config": {"workload": f"cross attention B{B} H{H} Lq{Lq} Lk{Lk} D{D} {mask}",
+                   "allowed_pairs_per_head": allowed_pairs(Lq, Lk, mask),
+                   "l2": "flushed between timed steps"},
+        "contracts": res}))
+    return 0
+
+
 def main():
     args = parse()
+    if args.cross:
+        return run_cross(args)
     if args.shape:
         B, H, L, D, causal = (int(x) for x in args.shape.split(","))
         w = synth.custom_workload(B, H, L, D, bool(causal), seed_cfg=800)
