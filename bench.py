@@ -45,8 +45,8 @@ L2_FLUSH_BYTES = 512 << 20  # > 129 MB L2
 # profiles/ (taken on half of the heads and scaled by 2; per-head traffic is
 # identical). Remove an entry when its kernel changes.
 NCU_TRAFFIC_BYTES = {
-    ("accel_dkdv_dq", 5): 2 * (405.024512e6 + 349.171712e6),
-    ("accel_fwd", 5): 2 * (551.054080e6 + 102.975744e6),
+    ("accel_dkdv_dq", 5): 2 * (404.883968e6 + 349.094912e6),
+    ("accel_fwd", 5): 2 * (552.298752e6 + 103.339776e6),
 }
 
 
