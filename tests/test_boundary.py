@@ -140,3 +140,49 @@ def test_binding_raises_on_error(lib):
         mg.mg_attn_fwd(q, FakeT(P(1), q.shape), FakeT(P(2), q.shape), FakeT(P(3), q.shape),
                        FakeT(P(4), q.shape[:3]), True, 0.1, "strict", stream=0)
     assert ei.value.status == mg.MG_ERR_UNSUPPORTED
+
+
+# ---------------------------------------------------------------- cross attention (_ex calls)
+def fwd_ex(lib, Q=P(0), K=P(1), V=P(2), O=P(3), LSE=P(4), B=1, H=2, Lq=64, Lk=96, D=64, mask=2,
+           scale=0.125, contract=0):
+    return lib.mg_attn_fwd_ex(Q, K, V, O, LSE, B, H, Lq, Lk, D, mask, scale, contract, None)
+
+
+def bwd_ex(lib, Q=P(0), K=P(1), V=P(2), O=P(3), dO=P(4), LSE=P(5), dQ=P(6), dK=P(7), dV=P(8),
+           B=1, H=2, Lq=64, Lk=96, D=64, mask=2, scale=0.125, contract=0, ws=P(9),
+           ws_bytes=1 << 20):
+    return lib.mg_attn_bwd_ex(Q, K, V, O, dO, LSE, dQ, dK, dV, B, H, Lq, Lk, D, mask, scale,
+                              contract, ws, ws_bytes, None)
+
+
+@pytest.mark.parametrize("kw,code", [
+    (dict(mask=3), mg.MG_ERR_INVALID_ARG),
+    (dict(mask=-1), mg.MG_ERR_INVALID_ARG),
+    (dict(Lk=0), mg.MG_ERR_INVALID_ARG),
+    (dict(Lq=0), mg.MG_ERR_INVALID_ARG),
+    (dict(Lk=(1 << 20) + 1), mg.MG_ERR_INVALID_ARG),
+    (dict(D=96), mg.MG_ERR_UNSUPPORTED),
+    (dict(V=P(1) + 8), mg.MG_ERR_INVALID_ARG),       # misaligned
+    (dict(O=P(2)), mg.MG_ERR_INVALID_ARG),           # O aliases V
+])
+def test_fwd_ex_rejects(lib, kw, code):
+    assert fwd_ex(lib, **kw) == code
+
+
+@pytest.mark.parametrize("kw,code", [
+    (dict(mask=7), mg.MG_ERR_INVALID_ARG),
+    (dict(Lk=0), mg.MG_ERR_INVALID_ARG),
+    (dict(ws_bytes=64 * 4 * 2 - 16), mg.MG_ERR_WORKSPACE),  # Dvec is [B][H][Lq]
+    (dict(dK=P(1)), mg.MG_ERR_INVALID_ARG),          # dK aliases K
+])
+def test_bwd_ex_rejects(lib, kw, code):
+    assert bwd_ex(lib, **kw) == code
+
+
+def test_workspace_bytes_ex_follows_the_query_length(lib):
+    for contract in (0, 1):
+        assert lib.mg_attn_bwd_workspace_bytes_ex(2, 3, 1000, 7, 64, contract) == \
+            lib.mg_attn_bwd_workspace_bytes(2, 3, 1000, 64, contract)
+        assert lib.mg_attn_bwd_workspace_bytes_ex(2, 3, 7, 1000, 64, contract) == \
+            lib.mg_attn_bwd_workspace_bytes(2, 3, 7, 64, contract)
+        assert lib.mg_attn_bwd_workspace_bytes_ex(1, 1, 1, 0, 64, contract) == 0
