@@ -41,7 +41,8 @@ UNIT = "TFLOP/s"
 L2_FLUSH_BYTES = 512 << 20  # > 129 MB L2
 
 # dram__bytes_read.sum + dram__bytes_write.sum per launch of the dominant
-# kernel at the benchmark workload (cfg 5), from the ncu captures summarised in
+# kernel at the benchmark workload (long-sequence causal, B=2 H=32 L=8192 D=128),
+# from the ncu captures summarised in
 # profiles/ (taken on half of the heads and scaled by 2; per-head traffic is
 # identical). Remove an entry when its kernel changes.
 NCU_TRAFFIC_BYTES = {

@@ -60,7 +60,7 @@ def test_identity_check_flags_planted_mistakes():
 
 @pytest.mark.gpu
 @pytest.mark.parametrize("contract", ["accel", "strict"])
-def test_cfg5_identities_every_head(contract):
+def test_long_sequence_identities_every_head(contract):
     w = synth.WORKLOADS[5]
     dev, vals = device_inputs(synth.inputs(w, contract), contract)
     got = run_gpu(dev, w.causal, w.scale, contract, bwd=True)
@@ -72,7 +72,7 @@ def test_cfg5_identities_every_head(contract):
 
 
 @pytest.mark.gpu
-def test_cfg5_identities_two_pass_backward_in_child():
+def test_long_sequence_identities_two_pass_backward_in_child():
     """The same identities through the two-pass backward (dK/dV kernel with two
     query blocks in flight, then the dQ pass; MG_DQ_MODE=pass), in a child
     process because the mode is read once per process."""

@@ -50,8 +50,8 @@ def test_accel_large_logits_noncausal():
     _full_check(synth.custom_workload(2, 3, 300, 64, False, seed_cfg=970, qk_gain=4.0))
 
 
-def test_accel_cfg5_sampled():
-    """Config 5 (B=2, H=32, L=8192, D=128, causal) in the launch configuration
+def test_accel_long_sequence_sampled():
+    """The long-sequence causal workload (B=2, H=32, L=8192, D=128) in the launch configuration
     the benchmark times: two heads in full (forward and backward) and every
     fifth head on sampled query rows (O and LSE)."""
     w = synth.WORKLOADS[5]
@@ -99,7 +99,8 @@ def test_accel_repeatable_forward():
 
 def test_accel_pass_dq_mode_in_child():
     """The two-pass backward (dK/dV kernel with two query blocks in flight, then
-    the separate dQ pass; MG_DQ_MODE=pass) on cfg 2, 3 and 4 and on sub-tile,
+    the separate dQ pass; MG_DQ_MODE=pass) on the decoder, encoder and large-logit
+    workloads and on sub-tile,
     one-tile and ragged lengths for every head dim, causal and not, in a child
     process because the mode is read once per process."""
     import os

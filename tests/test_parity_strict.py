@@ -41,8 +41,8 @@ def test_strict_large_logits_noncausal():
     _full_check(synth.custom_workload(2, 3, 300, 64, False, seed_cfg=920, qk_gain=4.0))
 
 
-def test_strict_cfg5_sampled():
-    """Config 5 (B=2, H=32, L=8192, D=128, causal) in the launch configuration
+def test_strict_long_sequence_sampled():
+    """The long-sequence causal workload (B=2, H=32, L=8192, D=128) in the launch configuration
     the benchmark times: two heads are checked in full (forward and backward)
     and every head on sampled query rows (O and LSE)."""
     w = synth.WORKLOADS[5]
