@@ -11,6 +11,10 @@ The function names mirror the C ABI in ``include/mg_attn.h``:
 * ``mg_attn_bwd_workspace_bytes(B, H, L, D, contract)``
 * ``mg_attn_bwd(Q, K, V, O, dO, LSE, dQ, dK, dV, causal, scale, contract,
   workspace, stream=None)``
+* ``mg_attn_fwd_ex``, ``mg_attn_bwd_workspace_bytes_ex``, ``mg_attn_bwd_ex`` (cross
+  attention, Lq != Lk, with a mask)
+* ``mg_attn_fwd_decode_workspace_bytes``, ``mg_attn_fwd_decode`` (split-key
+  forward for at most 8 query rows)
 * ``mg_status_string(status)``, ``mg_get_device_error(stream=None)``
 * ``mg_attn_profile_enable``, ``mg_attn_profile_read``, ``mg_attn_kernel_name``
 
@@ -70,6 +74,11 @@ def load_library(path: str | None = None):
         lib.mg_attn_bwd_ex.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, i, i, i, i, i, i, f,
                                        i, vp, sz, vp]
         lib.mg_attn_bwd_ex.restype = i
+        lib.mg_attn_fwd_decode_workspace_bytes.argtypes = [i, i, i, i, i, i]
+        lib.mg_attn_fwd_decode_workspace_bytes.restype = sz
+        lib.mg_attn_fwd_decode.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, i, i, f, i, vp, sz,
+                                           vp]
+        lib.mg_attn_fwd_decode.restype = i
         lib.mg_status_string.argtypes = [i]
         lib.mg_status_string.restype = ctypes.c_char_p
         lib.mg_get_device_error.argtypes = [vp]
@@ -180,6 +189,26 @@ def mg_attn_bwd_ex(Q, K, V, O, dO, LSE, dQ, dK, dV, mask, scale, contract, works
                                        _ptr(workspace), ws_bytes, _stream(stream))
     if rc != MG_OK:
         raise MgError(rc, "mg_attn_bwd_ex")
+    return rc
+
+
+def mg_attn_fwd_decode_workspace_bytes(B, H, Lq, Lk, D, contract) -> int:
+    return int(load_library().mg_attn_fwd_decode_workspace_bytes(B, H, Lq, Lk, D,
+                                                                  _contract(contract)))
+
+
+def mg_attn_fwd_decode(Q, K, V, O, LSE, mask, scale, contract, workspace, stream=None) -> int:
+    """Split-key forward for Lq <= 8 query rows (decoding); shapes and mask as in
+    mg_attn_fwd_ex, plus a workspace of mg_attn_fwd_decode_workspace_bytes() bytes."""
+    B, H, Lq, D = _dims(Q)
+    Lk = int(K.shape[2])
+    ws_bytes = workspace.numel() * workspace.element_size() if workspace is not None else 0
+    rc = load_library().mg_attn_fwd_decode(_ptr(Q), _ptr(K), _ptr(V), _ptr(O), _ptr(LSE), B, H,
+                                           Lq, Lk, D, _mask(mask), float(scale),
+                                           _contract(contract), _ptr(workspace), ws_bytes,
+                                           _stream(stream))
+    if rc != MG_OK:
+        raise MgError(rc, "mg_attn_fwd_decode")
     return rc
 
 

@@ -83,7 +83,7 @@ void prof_free() {
 
 const char *const kKernelNames[MGK_COUNT] = {
     "strict_fwd", "strict_dvec", "strict_dkdv_dq", "accel_fwd",     "accel_dvec",
-    "accel_dkdv_dq", "dq_zero",  "accel_dkdv",    "accel_dq"};
+    "accel_dkdv_dq", "dq_zero",  "accel_dkdv",    "accel_dq",    "decode_fwd"};
 
 // How the ACCEL backward produces dQ: f32 TMA reductions from the fused dK/dV
 // kernel (default, measured faster on GB300) or a separate dQ pass that
@@ -223,6 +223,38 @@ int mg_attn_fwd(const void *Q, const void *K, const void *V, void *O, float *LSE
   if (causal != 0 && causal != 1) return MG_ERR_INVALID_ARG;
   return mg_attn_fwd_ex(Q, K, V, O, LSE, B, H, L, L, D, causal ? MG_MASK_CAUSAL : MG_MASK_NONE,
                         scale, contract, stream);
+}
+
+size_t mg_attn_fwd_decode_workspace_bytes(int B, int H, int Lq, int Lk, int D, int contract) {
+  if (check_common(B, H, Lq, Lk, D, MG_MASK_NONE, 1.f, contract) != MG_OK) return 0;
+  if (Lq > mg_decode_max_rows()) return 0;
+  const MgProblem p = make_problem(B, H, Lq, Lk, D, MG_MASK_NONE, 1.f);
+  return (mg_decode_workspace_floats(p) * sizeof(float) + 255) & ~static_cast<size_t>(255);
+}
+
+int mg_attn_fwd_decode(const void *Q, const void *K, const void *V, void *O, float *LSE, int B,
+                       int H, int Lq, int Lk, int D, int mask, float scale, int contract,
+                       void *workspace, size_t workspace_bytes, void *stream) {
+  int rc = check_common(B, H, Lq, Lk, D, mask, scale, contract);
+  if (rc) return rc;
+  if (Lq > mg_decode_max_rows()) return MG_ERR_UNSUPPORTED;
+  const void *ptrs[] = {Q, K, V, O, LSE};
+  if ((rc = check_ptrs(ptrs, 5))) return rc;
+  const size_t need = mg_attn_fwd_decode_workspace_bytes(B, H, Lq, Lk, D, contract);
+  if (!workspace || !aligned16(workspace) || workspace_bytes < need) return MG_ERR_WORKSPACE;
+  const size_t nq = static_cast<size_t>(B) * H * Lq * D;
+  const size_t nk = static_cast<size_t>(B) * H * Lk * D;
+  const size_t in_el = contract == MG_CONTRACT_STRICT_F32 ? 4 : 2;
+  const Range in[] = {rng(Q, nq * in_el), rng(K, nk * in_el), rng(V, nk * in_el)};
+  const Range out[] = {rng(O, nq * 4), rng(LSE, static_cast<size_t>(B) * H * Lq * 4),
+                       rng(workspace, need)};
+  if ((rc = check_alias(in, 3, out, 3))) return rc;
+  const MgProblem p = make_problem(B, H, Lq, Lk, D, mask, scale);
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  ProfScope ps(MGK_DECODE_FWD, st);
+  return map_cuda(mg_launch_decode_fwd(Q, K, V, static_cast<float *>(O), LSE,
+                                       static_cast<float *>(workspace), p,
+                                       contract == MG_CONTRACT_ACCEL_BF16, st));
 }
 
 size_t mg_attn_bwd_workspace_bytes_ex(int B, int H, int Lq, int Lk, int D, int contract) {

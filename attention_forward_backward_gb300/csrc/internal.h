@@ -28,7 +28,8 @@ enum MgKernelId {
   MGK_DQ_ZERO = 6,
   MGK_ACCEL_DKDV = 7,     // dK/dV kernel of the two-pass backward
   MGK_ACCEL_DQ = 8,       // dQ pass of the two-pass backward
-  MGK_COUNT = 9
+  MGK_DECODE_FWD = 9,     // split-key forward for a few query rows (partials + merge)
+  MGK_COUNT = 10
 };
 
 // Device error codes written into the device error word by bounded waits.
@@ -68,6 +69,15 @@ cudaError_t mg_launch_accel_dkdv_pp(const __nv_bfloat16 *Q, const __nv_bfloat16 
                                     const __nv_bfloat16 *V, const __nv_bfloat16 *dO,
                                     const float *LSE, const float *Dvec, float *dK, float *dV,
                                     const MgProblem &p, unsigned int *err, cudaStream_t st);
+
+// Split-key forward for at most mg_decode_max_rows() query rows (decoding). The
+// partial records need mg_decode_workspace_floats() floats of scratch.
+int mg_decode_max_rows();
+void mg_decode_split(const MgProblem &p, int *S, int *chunk);
+size_t mg_decode_workspace_floats(const MgProblem &p);
+cudaError_t mg_launch_decode_fwd(const void *Q, const void *K, const void *V, float *O,
+                                 float *LSE, float *part, const MgProblem &p, bool bf16,
+                                 cudaStream_t st);
 
 // Opt a kernel into more than 48 KB of dynamic shared memory once per device.
 cudaError_t mg_set_smem_attr(const void *func, int bytes, int slot);

@@ -65,6 +65,9 @@ def parse():
     ap.add_argument("--cross", default=None,
                     help="B,H,Lq,Lk,D,mask (mask: none|causal|causal_bottom_right): measure "
                          "cross attention through the _ex calls instead of the default workload")
+    ap.add_argument("--decode", default=None,
+                    help="B,H,Lq,Lk,D,mask with Lq <= 8: measure the split-key decode forward "
+                         "(mg_attn_fwd_decode) beside mg_attn_fwd_ex on the same inputs")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=15.0,
@@ -486,10 +489,85 @@ def run_cross(args):
     return 0
 
 
+def run_decode(args):
+    """Decode-shaped forward (a few query rows against a long key axis): the
+    split-key mg_attn_fwd_decode and the generic mg_attn_fwd_ex on the same
+    inputs, per contract, as GB/s of algorithmic traffic (K and V read once, Q
+    read, O and LSE written) against the measured HBM copy bandwidth. L2 flushed
+    between timed steps. One JSON line."""
+    import torch
+    import attention_forward_backward_gb300 as mg
+    B, H, Lq, Lk, D = (int(x) for x in args.decode.split(",")[:5])
+    mask = args.decode.split(",")[5]
+    device = torch.device("cuda", 0)
+    mg.load_library()
+    stream = torch.cuda.Stream(device)
+    s = stream.cuda_stream
+    peaks = load_peaks()
+    contracts = ["accel", "strict"] if args.contract == "both" else [args.contract]
+    flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=device)
+    res = {}
+    for c in contracts:
+        el = 2 if c == "accel" else 4
+        nbytes = el * B * H * (2 * Lk + Lq) * D + 4 * B * H * Lq * (D + 1)
+        host = synth.cross_inputs(B, H, Lq, Lk, D, c, seed_cfg=802)
+        dev = {}
+        for k in ("Q", "K", "V"):
+            x = host[k]
+            if c == "strict":
+                dev[k] = torch.from_numpy(x).to(device)
+            else:
+                dev[k] = torch.from_numpy(np.ascontiguousarray(x["bits"]).view(np.int16)).view(
+                    torch.bfloat16).to(device)
+        O = torch.empty((B, H, Lq, D), dtype=torch.float32, device=device)
+        LSE = torch.empty((B, H, Lq), dtype=torch.float32, device=device)
+        ws = torch.empty(mg.mg_attn_fwd_decode_workspace_bytes(B, H, Lq, Lk, D, c),
+                         dtype=torch.uint8, device=device)
+        scale = D ** -0.5
+        calls = {
+            "split_key": lambda: mg.mg_attn_fwd_decode(dev["Q"], dev["K"], dev["V"], O, LSE,
+                                                       mask, scale, c, ws, s),
+            "generic": lambda: mg.mg_attn_fwd_ex(dev["Q"], dev["K"], dev["V"], O, LSE, mask,
+                                                 scale, c, s)}
+        res[c] = {"bytes_per_call": nbytes}
+        for name, call in calls.items():
+            ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+                  for _ in range(args.steps)]
+            with torch.cuda.stream(stream):
+                for i in range(args.warmup + args.steps):
+                    if i >= args.warmup:
+                        flush.fill_(float(i))
+                        ev[i - args.warmup][0].record(stream)
+                    call()
+                    if i >= args.warmup:
+                        ev[i - args.warmup][1].record(stream)
+                torch.cuda.synchronize()
+            if mg.mg_get_device_error(s) != mg.MG_OK:
+                raise RuntimeError(f"{c} {name}: device error word set")
+            ms = sum(a.elapsed_time(b) for a, b in ev) / args.steps
+            gbs = nbytes / (ms * 1e-3) / 1e9
+            res[c][name] = {"us": ms * 1e3, "gbs": gbs, "frac_of_measured_hbm": gbs / peaks["hbm_gbs"]}
+    head = "accel" if "accel" in res else "strict"
+    print(json.dumps({
+        "metric": "decode forward GB/s on 1 GB300 (K, V read once; Q read; O, LSE written)",
+        "value": res[head]["split_key"]["gbs"], "unit": "GB/s", "n_gpus": 1,
+        "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": res[head]["split_key"]["us"] * 1e-3, "higher_is_better": True,
+        "dtype": "bf16" if head == "accel" else "f32", "data": "synthetic",
+        "config": {"workload": f"decode B{B} H{H} Lq{Lq} Lk{Lk} D{D} {mask}",
+                   "l2": "flushed between timed steps"},
+        "roofline": {"bound": "hbm", "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                     "peak_source": peaks["source"]},
+        "contracts": res}))
+    return 0
+
+
 def main():
     args = parse()
     if args.cross:
         return run_cross(args)
+    if args.decode:
+        return run_decode(args)
     if args.shape:
         B, H, L, D, causal = (int(x) for x in args.shape.split(","))
         w = synth.custom_workload(B, H, L, D, bool(causal), seed_cfg=800)

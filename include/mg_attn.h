@@ -84,7 +84,7 @@ typedef enum {
 typedef enum {
   MG_OK = 0,
   MG_ERR_INVALID_ARG = 1, /* null/misaligned pointer, bad size, aliasing, bad scale */
-  MG_ERR_UNSUPPORTED = 2, /* D not in {32,64,128} */
+  MG_ERR_UNSUPPORTED = 2, /* D not in {32,64,128}; Lq > 8 for the decode forward */
   MG_ERR_WORKSPACE = 3,   /* workspace missing or smaller than the query says */
   MG_ERR_CUDA = 4,        /* a CUDA runtime call or launch failed */
   MG_ERR_TIMEOUT = 5      /* a kernel gave up on a bounded wait (device error word) */
@@ -176,6 +176,35 @@ int mg_attn_bwd_noalloc(const void *Q, const void *K, const void *V, const void 
                         const void *dO, const float *LSE, void *dQ, void *dK, void *dV,
                         int B, int H, int L, int D, int causal, float scale, int contract,
                         void *stream);
+
+/* Workspace bytes for mg_attn_fwd_decode (one partial record of D + 2 f32 per
+ * head, key split and query row, rounded up to 256 bytes). 0 for invalid
+ * arguments or Lq > 8. */
+size_t mg_attn_fwd_decode_workspace_bytes(int B, int H, int Lq, int Lk, int D, int contract);
+
+/*
+ * Forward for a few query rows against a long key axis (decoding: Lq <= 8
+ * rows per head, e.g. the newest tokens against a key/value cache). Computes
+ * exactly what mg_attn_fwd_ex computes for the same arguments, with a different
+ * schedule: the key axis is split over many CTAs, each of which keeps the
+ * running max, sum and unnormalised output of its keys (the online softmax of
+ * the tiled forward archetype, Section 3.3 of the paper), and a second kernel
+ * merges the splits. The split count depends on (B, H, Lk) only.
+ *   Q, O       [B][H][Lq][D] (Q f32 or bf16 by contract, O f32), Lq in [1, 8]
+ *   K, V       [B][H][Lk][D]
+ *   LSE        out [B][H][Lq] f32
+ *   mask       mg_mask_t; rows with no allowed key get O = 0, LSE = -inf
+ *   workspace  scratch of at least mg_attn_fwd_decode_workspace_bytes() bytes,
+ *              16-byte aligned, not overlapping any tensor; contents on entry do
+ *              not matter
+ * Both contracts compute in f32 on the CUDA cores (bf16 inputs are widened on
+ * load); the work is one pass over K and V and is bound by HBM, not by the
+ * tensor cores. Lq > 8 returns MG_ERR_UNSUPPORTED (use mg_attn_fwd_ex). Other
+ * preconditions, ownership and errors as mg_attn_fwd_ex.
+ */
+int mg_attn_fwd_decode(const void *Q, const void *K, const void *V, void *O, float *LSE,
+                       int B, int H, int Lq, int Lk, int D, int mask, float scale,
+                       int contract, void *workspace, size_t workspace_bytes, void *stream);
 
 /* Static, human-readable name of a status code. Never NULL. */
 const char *mg_status_string(int status);

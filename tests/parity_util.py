@@ -136,3 +136,21 @@ def compare_ex(got: dict, ref: dict, contract: str):
         if not errs["LSE"] <= TOL[contract]:
             bad = dict(bad, LSE=errs["LSE"])
     return errs, bad
+
+
+def run_gpu_decode(dev: dict, mask: str, scale: float, contract: str):
+    """Split-key decode forward (mg_attn_fwd_decode), outputs and workspace
+    poisoned with NaN first. Q [B, H, Lq, D] with Lq <= 8; K, V [B, H, Lk, D]."""
+    import torch
+    Q, K, V = dev["Q"], dev["K"], dev["V"]
+    B, H, Lq, D = Q.shape
+    Lk = K.shape[2]
+    nan = float("nan")
+    O = torch.full((B, H, Lq, D), nan, device=Q.device)
+    LSE = torch.full((B, H, Lq), nan, device=Q.device)
+    nbytes = mg.mg_attn_fwd_decode_workspace_bytes(B, H, Lq, Lk, D, contract)
+    ws = torch.full((nbytes // 4,), nan, device=Q.device)
+    mg.mg_attn_fwd_decode(Q, K, V, O, LSE, mask, scale, contract, ws)
+    torch.cuda.synchronize()
+    assert mg.mg_get_device_error() == mg.MG_OK
+    return {"O": O.cpu().numpy(), "LSE": LSE.cpu().numpy()}

@@ -186,3 +186,48 @@ def test_workspace_bytes_ex_follows_the_query_length(lib):
         assert lib.mg_attn_bwd_workspace_bytes_ex(2, 3, 7, 1000, 64, contract) == \
             lib.mg_attn_bwd_workspace_bytes(2, 3, 7, 64, contract)
         assert lib.mg_attn_bwd_workspace_bytes_ex(1, 1, 1, 0, 64, contract) == 0
+
+
+# ---------------------------------------------------------------- decode forward
+def fwd_decode(lib, Q=P(0), K=P(1), V=P(2), O=P(3), LSE=P(4), B=1, H=2, Lq=4, Lk=1000, D=64,
+               mask=2, scale=0.125, contract=0, ws=P(5), ws_bytes=1 << 24):
+    return lib.mg_attn_fwd_decode(Q, K, V, O, LSE, B, H, Lq, Lk, D, mask, scale, contract, ws,
+                                  ws_bytes, None)
+
+
+@pytest.mark.parametrize("kw,code", [
+    (dict(Lq=9), mg.MG_ERR_UNSUPPORTED),             # more rows than the decode schedule takes
+    (dict(Lq=0), mg.MG_ERR_INVALID_ARG),
+    (dict(Lk=0), mg.MG_ERR_INVALID_ARG),
+    (dict(D=48), mg.MG_ERR_UNSUPPORTED),
+    (dict(mask=3), mg.MG_ERR_INVALID_ARG),
+    (dict(scale=0.0), mg.MG_ERR_INVALID_ARG),
+    (dict(contract=2), mg.MG_ERR_INVALID_ARG),
+    (dict(ws=None), mg.MG_ERR_WORKSPACE),
+    (dict(ws=P(5) + 8), mg.MG_ERR_WORKSPACE),        # misaligned workspace
+    (dict(ws_bytes=16), mg.MG_ERR_WORKSPACE),
+    (dict(K=P(1) + 4), mg.MG_ERR_INVALID_ARG),       # misaligned
+    (dict(O=P(0)), mg.MG_ERR_INVALID_ARG),           # O aliases Q
+    (dict(ws=P(2)), mg.MG_ERR_INVALID_ARG),          # workspace aliases V
+])
+def test_fwd_decode_rejects(lib, kw, code):
+    assert fwd_decode(lib, **kw) == code
+
+
+def test_decode_workspace_bytes(lib):
+    """One record of D + 2 floats per (head, key split, query row); the split
+    count is at least one, at most one per 256 keys, and the size is a multiple
+    of 256 bytes. Worked case: B=1, H=8, Lk=32768 asks for ceil(608 / 8) = 76
+    splits of ceil(32768 / 76) = 432 -> 448 keys (whole 32-key tiles), which
+    covers the keys in 74 splits: 8 * 74 * 1 * 130 floats = 307,840 bytes,
+    rounded up to 307,968."""
+    assert lib.mg_attn_fwd_decode_workspace_bytes(1, 8, 1, 32768, 128, 1) == 307968
+    for (B, H, Lq, Lk, D) in [(1, 1, 1, 1, 32), (2, 3, 8, 5000, 64), (4, 32, 3, 100000, 128),
+                              (64, 64, 1, 4096, 128)]:
+        for contract in (0, 1):
+            n = lib.mg_attn_fwd_decode_workspace_bytes(B, H, Lq, Lk, D, contract)
+            rec = B * H * Lq * (D + 2) * 4
+            assert n % 256 == 0 and rec <= n < rec * max(1, -(-Lk // 256)) + 256, (B, H, Lq, Lk)
+    assert lib.mg_attn_fwd_decode_workspace_bytes(1, 1, 9, 100, 64, 0) == 0
+    assert lib.mg_attn_fwd_decode_workspace_bytes(1, 1, 1, 0, 64, 0) == 0
+    assert lib.mg_attn_fwd_decode_workspace_bytes(1, 1, 1, 100, 96, 0) == 0
