@@ -8,9 +8,10 @@
 // query rows. With so few rows the work is one pass over K and V, bound by HBM,
 // and the generic kernels leave most SMs idle when there are few heads: splitting
 // the keys lets every SM stream its share. Arithmetic is f32 on the CUDA cores for
-// both contracts (bf16 inputs are widened on load); scores are in base 2 with
-// scale * log2(e) folded into Q, and each split keeps the exact online-softmax
-// state, so the merge is exact up to rounding:
+// both contracts (bf16 inputs are widened on load) with K, V and Q held in
+// registers, never staged in shared memory; scores are in base 2 with
+// scale * log2(e) folded into Q, and every partial state is the exact
+// online-softmax state of its keys, so merging is exact up to rounding:
 //   m = max_s m_s,  l = sum_s l_s 2^(m_s - m),  O = sum_s O_s 2^(m_s - m) / l,
 //   LSE = ln 2 (m + log2 l);  a row with no allowed key gets O = 0, LSE = -inf.
 #include <math.h>
@@ -22,8 +23,8 @@ namespace {
 constexpr float kLog2eF = 1.4426950408889634f;
 constexpr float kLn2F = 0.6931471805599453f;
 constexpr int kMaxLq = 8;   // query rows per head handled here
-constexpr int kTile = 32;   // keys per shared-memory tile
-constexpr int kThreads = 256;
+constexpr int kTile = 32;   // split lengths are whole multiples of this many keys
+constexpr int kThreads = 128;
 
 __device__ __forceinline__ float load_in(const float *p, size_t i) { return p[i]; }
 __device__ __forceinline__ float load_in(const __nv_bfloat16 *p, size_t i) {
@@ -66,179 +67,259 @@ __device__ __forceinline__ float warp_max(float v) {
   for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
   return v;
 }
-__device__ __forceinline__ float warp_sum(float v) {
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
-  return v;
-}
 
-// One CTA: head bh, keys [k_begin, k_end). Partial record per (bh, split, q):
-// [m (base 2), l, O_0 .. O_{D-1}] in `part`.
-template <int D, typename TIn>
+// One CTA of four warps: head bh, keys [k_begin, k_end). Nothing is staged in
+// shared memory: a key row of D elements is spread over LPR = D / 8 lanes (eight
+// consecutive elements each, one 16-byte load for bf16, two for f32), so a warp
+// reads RPW = 32 / LPR whole rows per load, coalesced. Each group of LPR lanes
+// keeps its own online-softmax state (m, l, O slice) for every query row; Q lives
+// in registers. The next kUnroll rows per group are in flight while the current
+// ones are used. At the end the CTA's G = 4 RPW states are combined in shared
+// memory into one partial record per query row:
+//   [O_0 .. O_{D-1} (unnormalised, relative to m), m (base 2), l, -, -].
+template <int D, int LQ, typename TIn>
 __global__ void __launch_bounds__(kThreads)
     decode_partial_kernel(const TIn *__restrict__ Q, const TIn *__restrict__ K,
                           const TIn *__restrict__ V, float *__restrict__ part, int Lq, int Lk,
                           int causal, int off, int S, int chunk, float scale_log2) {
-  constexpr int KS = D + 1;                       // padded K row: conflict-free column reads
-  constexpr int QPT = kMaxLq * D / kThreads;      // output (q, d) cells per thread
-  constexpr int QSTEP = kThreads / D;             // q stride between a thread's cells
-  constexpr int CH = kTile * D / 8;               // 8-element chunks per tile of K (and V)
-  constexpr int CPT = (CH + kThreads - 1) / kThreads;
-  static_assert(QPT >= 1 && kThreads % D == 0 && D % 8 == 0, "layout");
-  __shared__ float sQ[kMaxLq][D];
-  __shared__ float sK[kTile][KS];
-  __shared__ float sV[kTile][D];
-  __shared__ float sP[kMaxLq][kTile];
-  __shared__ float sAlpha[kMaxLq];
+  constexpr int LPR = D / 8;
+  constexpr int RPW = 32 / LPR;
+  constexpr int G = (kThreads / 32) * RPW;
+  constexpr int U = LQ >= 8 ? 2 : 4;  // rows per group per step (register budget)
+  constexpr int STEP = G * U;         // keys per CTA step
+  __shared__ float sM[LQ][G], sL[LQ][G];
+  __shared__ float sO[LQ][G][D];
 
   const int bh = blockIdx.x / S, s = blockIdx.x % S;
-  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int tid = threadIdx.x, lane = tid & 31;
+  const int c = lane % LPR;                          // elements 8c .. 8c+7 of a row
+  const int grp = (tid >> 5) * RPW + lane / LPR;     // this lane's softmax state
   const int k_begin = s * chunk;
   const int k_end = min(Lk, k_begin + chunk);
-  const size_t qbase = static_cast<size_t>(bh) * Lq * D;
-  const size_t kbase = static_cast<size_t>(bh) * Lk * D;
+  const TIn *Kb = K + static_cast<size_t>(bh) * Lk * D + c * 8;
+  const TIn *Vb = V + static_cast<size_t>(bh) * Lk * D + c * 8;
 
-  for (int i = tid; i < kMaxLq * D; i += kThreads) {
-    const int q = i / D, d = i % D;
-    sQ[q][d] = q < Lq ? load_in(Q, qbase + static_cast<size_t>(q) * D + d) * scale_log2 : 0.f;
+  float qr[LQ][8], o[LQ][8], m[LQ], l[LQ];
+#pragma unroll
+  for (int q = 0; q < LQ; ++q) {
+#pragma unroll
+    for (int e = 0; e < 8; ++e) {
+      qr[q][e] = q < Lq
+          ? load_in(Q, (static_cast<size_t>(bh) * Lq + q) * D + c * 8 + e) * scale_log2
+          : 0.f;
+      o[q][e] = 0.f;
+    }
+    m[q] = -INFINITY;
+    l[q] = 0.f;
   }
-  // running state: warp q owns m, l of query q; thread owns O cells (q0 + j QSTEP, dd)
-  float m = -INFINITY, l = 0.f;
-  float o[QPT];
-#pragma unroll
-  for (int j = 0; j < QPT; ++j) o[j] = 0.f;
-  const int dd = tid % D, q0 = tid / D;
 
-  // K and V chunks of the next tile, in flight while the current one is used
-  Raw8<TIn> rk[CPT], rv[CPT];
-  auto fetch = [&](int k0) {
+  Raw8<TIn> rk[U], rv[U];
+  auto fetch = [&](int kb) {
 #pragma unroll
-    for (int c = 0; c < CPT; ++c) {
-      const int i = tid + c * kThreads, r = i / (D / 8);
-      if (i < CH && k0 + r < k_end) {
-        const size_t g = kbase + static_cast<size_t>(k0 + r) * D + (i % (D / 8)) * 8;
-        rk[c].load(K + g);
-        rv[c].load(V + g);
+    for (int u = 0; u < U; ++u) {
+      const int row = kb + u * G + grp;
+      if (row < k_end) {
+        rk[u].load(Kb + static_cast<size_t>(row) * D);
+        rv[u].load(Vb + static_cast<size_t>(row) * D);
       } else {
-        rk[c].zero();
-        rv[c].zero();
+        rk[u].zero();
+        rv[u].zero();
       }
     }
   };
   fetch(k_begin);
 
-  for (int k0 = k_begin; k0 < k_end; k0 += kTile) {
-    __syncthreads();  // previous tile fully consumed (and sQ written, first time)
-    const int nk = min(kTile, k_end - k0);
+  for (int kb = k_begin; kb < k_end; kb += STEP) {
+    float kf[U][8], vf[U][8];
 #pragma unroll
-    for (int c = 0; c < CPT; ++c) {
-      const int i = tid + c * kThreads;
-      if (i < CH) {
-        const int r = i / (D / 8), d = (i % (D / 8)) * 8;
-        rk[c].put(&sK[r][d]);
-        rv[c].put(&sV[r][d]);
+    for (int u = 0; u < U; ++u) {
+      rk[u].put(kf[u]);
+      rv[u].put(vf[u]);
+    }
+    if (kb + STEP < k_end) fetch(kb + STEP);
+    // scores (base 2): partial dot over this lane's 8 elements, summed over the
+    // LPR lanes of the row (xor offsets below LPR stay inside the group)
+    float sc[U][LQ];
+#pragma unroll
+    for (int u = 0; u < U; ++u) {
+#pragma unroll
+      for (int q = 0; q < LQ; ++q) {
+        float a = 0.f;
+#pragma unroll
+        for (int e = 0; e < 8; ++e) a = fmaf(qr[q][e], kf[u][e], a);
+        sc[u][q] = a;
       }
     }
-    if (k0 + kTile < k_end) fetch(k0 + kTile);
-    __syncthreads();
-    // scores: warp q (< Lq) -> query q, lane -> key k0 + lane
-    if (warp < Lq) {
-      const int q = warp, j = lane;
-      float sc = 0.f;
-#pragma unroll 8
-      for (int d = 0; d < D; ++d) sc = fmaf(sQ[q][d], sK[j][d], sc);
-      const int kg = k0 + j;
-      const bool allowed = j < nk && (!causal || kg <= q + off);
-      sP[q][j] = allowed ? sc : -INFINITY;
-    }
-    __syncthreads();
-    // online softmax: warp q updates query q's state over the tile's 32 keys
-    if (warp < Lq) {
-      const float x = sP[warp][lane];
-      const float mt = warp_max(x);
-      const float mn = fmaxf(m, mt);
-      const float mu = mn == -INFINITY ? 0.f : mn;  // no allowed key yet: P = 0
-      const float p = exp2f(x - mu);
-      const float alpha = exp2f(m - mu);
-      l = l * alpha + warp_sum(p);
-      m = mn;
-      sP[warp][lane] = p;
-      if (lane == 0) sAlpha[warp] = alpha;
-    }
-    __syncthreads();
-    // O[q][dd] = alpha_q O[q][dd] + sum_j P[q][j] V[j][dd]
 #pragma unroll
-    for (int jq = 0; jq < QPT; ++jq) {
-      const int q = q0 + jq * QSTEP;
-      if (q < Lq) {
-        float acc = o[jq] * sAlpha[q];
-#pragma unroll 8
-        for (int j = 0; j < kTile; ++j) acc = fmaf(sP[q][j], sV[j][dd], acc);
-        o[jq] = acc;
+    for (int w = LPR / 2; w >= 1; w >>= 1) {
+#pragma unroll
+      for (int u = 0; u < U; ++u) {
+#pragma unroll
+        for (int q = 0; q < LQ; ++q) sc[u][q] += __shfl_xor_sync(0xffffffffu, sc[u][q], w);
+      }
+    }
+#pragma unroll
+    for (int u = 0; u < U; ++u) {
+      const int key = kb + u * G + grp;
+#pragma unroll
+      for (int q = 0; q < LQ; ++q) {
+        const bool allowed = key < k_end && q < Lq && (!causal || key <= q + off);
+        if (!allowed) sc[u][q] = -INFINITY;
+      }
+    }
+    // online softmax of each query row over this group's U keys
+#pragma unroll
+    for (int q = 0; q < LQ; ++q) {
+      float mt = sc[0][q];
+#pragma unroll
+      for (int u = 1; u < U; ++u) mt = fmaxf(mt, sc[u][q]);
+      const float mn = fmaxf(m[q], mt);
+      const float mu = mn == -INFINITY ? 0.f : mn;  // no allowed key yet: P = 0
+      const float alpha = exp2f(m[q] - mu);
+      float ps = 0.f;
+#pragma unroll
+      for (int u = 0; u < U; ++u) {
+        sc[u][q] = exp2f(sc[u][q] - mu);
+        ps += sc[u][q];
+      }
+      l[q] = l[q] * alpha + ps;
+      m[q] = mn;
+#pragma unroll
+      for (int e = 0; e < 8; ++e) {
+        float a = o[q][e] * alpha;
+#pragma unroll
+        for (int u = 0; u < U; ++u) a = fmaf(sc[u][q], vf[u][e], a);
+        o[q][e] = a;
       }
     }
   }
 
-  // partial record of this split
-  float *rec = part + (static_cast<size_t>(bh) * S + s) * Lq * (D + 2);
-  if (warp < Lq && lane == 0) {
-    rec[warp * (D + 2)] = m;
-    rec[warp * (D + 2) + 1] = l;
-  }
+  // combine the CTA's G states: the lanes of a group hold the same m and l
 #pragma unroll
-  for (int jq = 0; jq < QPT; ++jq) {
-    const int q = q0 + jq * QSTEP;
-    if (q < Lq) rec[q * (D + 2) + 2 + dd] = o[jq];
+  for (int q = 0; q < LQ; ++q) {
+    if (c == 0) {
+      sM[q][grp] = m[q];
+      sL[q][grp] = l[q];
+    }
+#pragma unroll
+    for (int e = 0; e < 8; ++e) sO[q][grp][c * 8 + e] = o[q][e];
+  }
+  __syncthreads();
+  float *rec = part + (static_cast<size_t>(bh) * S + s) * Lq * (D + 4);
+  for (int i = tid; i < Lq * D; i += kThreads) {
+    const int q = i / D, d = i % D;
+    float mx = -INFINITY;
+#pragma unroll 8
+    for (int g = 0; g < G; ++g) mx = fmaxf(mx, sM[q][g]);
+    float ls = 0.f, acc = 0.f;
+    if (mx != -INFINITY) {
+#pragma unroll 8
+      for (int g = 0; g < G; ++g) {
+        const float w = exp2f(sM[q][g] - mx);  // a state that saw no allowed key: w = 0
+        ls = fmaf(sL[q][g], w, ls);
+        acc = fmaf(sO[q][g][d], w, acc);
+      }
+    }
+    rec[q * (D + 4) + d] = acc;
+    if (d == 0) {
+      rec[q * (D + 4) + D] = mx;
+      rec[q * (D + 4) + D + 1] = ls;
+    }
   }
 }
 
-// One CTA of D threads per (bh, q): merge the S partial records.
+// One CTA per (bh, q): merge the S partial records. Thread (slot, c4) adds the
+// records of splits slot, slot + SLOTS, ... for elements 4 c4 .. 4 c4 + 3; the
+// slots are summed in shared memory.
 template <int D>
-__global__ void __launch_bounds__(128)
+__global__ void __launch_bounds__(kThreads)
     decode_merge_kernel(const float *__restrict__ part, float *__restrict__ O,
                         float *__restrict__ LSE, int Lq, int S) {
+  constexpr int TPR = D / 4;
+  constexpr int SLOTS = kThreads / TPR;
+  __shared__ float sRed[kThreads / 32];
+  __shared__ float sAcc[SLOTS][D];
+  __shared__ float sL[SLOTS];
   const int bh = blockIdx.x / Lq, q = blockIdx.x % Lq;
-  const int d = threadIdx.x;
-  const float *rec = part + static_cast<size_t>(bh) * S * Lq * (D + 2) + q * (D + 2);
-  const size_t stride = static_cast<size_t>(Lq) * (D + 2);
-  float mmax = -INFINITY;
-  for (int s = 0; s < S; ++s) mmax = fmaxf(mmax, rec[s * stride]);
-  float lsum = 0.f, acc = 0.f;
-  if (mmax != -INFINITY) {
-    for (int s = 0; s < S; ++s) {
-      const float w = exp2f(rec[s * stride] - mmax);  // an empty split has m = -inf: w = 0
-      lsum = fmaf(rec[s * stride + 1], w, lsum);
-      acc = fmaf(rec[s * stride + 2 + d], w, acc);
+  const int tid = threadIdx.x, slot = tid / TPR, c4 = tid % TPR;
+  const size_t rstride = static_cast<size_t>(Lq) * (D + 4);
+  const float *rec0 = part + static_cast<size_t>(bh) * S * rstride + q * (D + 4);
+
+  float mx = -INFINITY;
+  for (int s = tid; s < S; s += kThreads) mx = fmaxf(mx, rec0[s * rstride + D]);
+  mx = warp_max(mx);
+  if ((tid & 31) == 0) sRed[tid >> 5] = mx;
+  __syncthreads();
+  mx = sRed[0];
+#pragma unroll
+  for (int w = 1; w < kThreads / 32; ++w) mx = fmaxf(mx, sRed[w]);
+
+  float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+  float ls = 0.f;
+  if (mx != -INFINITY) {
+#pragma unroll 4
+    for (int s = slot; s < S; s += SLOTS) {
+      const float *r = rec0 + s * rstride;
+      const float w = exp2f(r[D] - mx);  // a split with no allowed key has m = -inf: w = 0
+      ls = fmaf(r[D + 1], w, ls);
+      const float4 v = *reinterpret_cast<const float4 *>(r + 4 * c4);
+      acc.x = fmaf(v.x, w, acc.x);
+      acc.y = fmaf(v.y, w, acc.y);
+      acc.z = fmaf(v.z, w, acc.z);
+      acc.w = fmaf(v.w, w, acc.w);
     }
   }
+  sAcc[slot][4 * c4] = acc.x;
+  sAcc[slot][4 * c4 + 1] = acc.y;
+  sAcc[slot][4 * c4 + 2] = acc.z;
+  sAcc[slot][4 * c4 + 3] = acc.w;
+  if (c4 == 0) sL[slot] = ls;
+  __syncthreads();
   const size_t row = static_cast<size_t>(bh) * Lq + q;
-  O[row * D + d] = lsum > 0.f ? acc / lsum : 0.f;
-  if (d == 0) LSE[row] = lsum > 0.f ? (mmax + log2f(lsum)) * kLn2F : -INFINITY;
+  float lsum = 0.f;
+#pragma unroll
+  for (int k = 0; k < SLOTS; ++k) lsum += sL[k];
+  for (int d = tid; d < D; d += kThreads) {
+    float t = 0.f;
+#pragma unroll
+    for (int k = 0; k < SLOTS; ++k) t += sAcc[k][d];
+    O[row * D + d] = lsum > 0.f ? t / lsum : 0.f;
+  }
+  if (tid == 0) LSE[row] = lsum > 0.f ? (mx + log2f(lsum)) * kLn2F : -INFINITY;
 }
 
-template <int D, typename TIn>
+template <int D, int LQ, typename TIn>
 cudaError_t launch(const TIn *Q, const TIn *K, const TIn *V, float *O, float *LSE, float *part,
                    const MgProblem &p, int S, int chunk, cudaStream_t st) {
   const int BH = p.B * p.H;
-  decode_partial_kernel<D, TIn><<<static_cast<unsigned>(static_cast<long long>(BH) * S),
-                                  kThreads, 0, st>>>(Q, K, V, part, p.L, p.Lk, p.causal, p.off,
-                                                     S, chunk, p.scale * kLog2eF);
+  decode_partial_kernel<D, LQ, TIn>
+      <<<static_cast<unsigned>(static_cast<long long>(BH) * S), kThreads, 0, st>>>(
+          Q, K, V, part, p.L, p.Lk, p.causal, p.off, S, chunk, p.scale * kLog2eF);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
-  decode_merge_kernel<D><<<static_cast<unsigned>(static_cast<long long>(BH) * p.L), D, 0, st>>>(
-      part, O, LSE, p.L, S);
+  decode_merge_kernel<D><<<static_cast<unsigned>(static_cast<long long>(BH) * p.L), kThreads, 0,
+                           st>>>(part, O, LSE, p.L, S);
   return cudaGetLastError();
+}
+
+template <int D, typename TIn>
+cudaError_t launch_rows(const TIn *Q, const TIn *K, const TIn *V, float *O, float *LSE,
+                        float *part, const MgProblem &p, int S, int chunk, cudaStream_t st) {
+  if (p.L <= 1) return launch<D, 1, TIn>(Q, K, V, O, LSE, part, p, S, chunk, st);
+  if (p.L <= 2) return launch<D, 2, TIn>(Q, K, V, O, LSE, part, p, S, chunk, st);
+  if (p.L <= 4) return launch<D, 4, TIn>(Q, K, V, O, LSE, part, p, S, chunk, st);
+  return launch<D, 8, TIn>(Q, K, V, O, LSE, part, p, S, chunk, st);
 }
 
 }  // namespace
 
 int mg_decode_max_rows() { return kMaxLq; }
 
-// Splits of the key axis: about four CTAs per SM of a 152-SM GB300, at least 256
+// Splits of the key axis: about eight CTAs per SM of a 152-SM GB300, at least 256
 // keys per split. Depends only on the shape (the workspace size uses it too).
 void mg_decode_split(const MgProblem &p, int *S, int *chunk) {
   const long long BH = static_cast<long long>(p.B) * p.H;
-  const int want = static_cast<int>((4LL * 152 + BH - 1) / BH);
+  const int want = static_cast<int>((8LL * 152 + BH - 1) / BH);
   const int maxs = (p.Lk + 255) / 256;
   int s = want < 1 ? 1 : want;
   if (s > maxs) s = maxs;
@@ -251,7 +332,7 @@ void mg_decode_split(const MgProblem &p, int *S, int *chunk) {
 size_t mg_decode_workspace_floats(const MgProblem &p) {
   int S, chunk;
   mg_decode_split(p, &S, &chunk);
-  return static_cast<size_t>(p.B) * p.H * S * p.L * (p.D + 2);
+  return static_cast<size_t>(p.B) * p.H * S * p.L * (p.D + 4);
 }
 
 cudaError_t mg_launch_decode_fwd(const void *Q, const void *K, const void *V, float *O,
@@ -264,18 +345,18 @@ cudaError_t mg_launch_decode_fwd(const void *Q, const void *K, const void *V, fl
     const T *q = static_cast<const T *>(Q), *k = static_cast<const T *>(K),
             *v = static_cast<const T *>(V);
     switch (p.D) {
-      case 32: return launch<32, T>(q, k, v, O, LSE, part, p, S, chunk, st);
-      case 64: return launch<64, T>(q, k, v, O, LSE, part, p, S, chunk, st);
-      case 128: return launch<128, T>(q, k, v, O, LSE, part, p, S, chunk, st);
+      case 32: return launch_rows<32, T>(q, k, v, O, LSE, part, p, S, chunk, st);
+      case 64: return launch_rows<64, T>(q, k, v, O, LSE, part, p, S, chunk, st);
+      case 128: return launch_rows<128, T>(q, k, v, O, LSE, part, p, S, chunk, st);
       default: return cudaErrorInvalidValue;
     }
   }
   const float *q = static_cast<const float *>(Q), *k = static_cast<const float *>(K),
               *v = static_cast<const float *>(V);
   switch (p.D) {
-    case 32: return launch<32, float>(q, k, v, O, LSE, part, p, S, chunk, st);
-    case 64: return launch<64, float>(q, k, v, O, LSE, part, p, S, chunk, st);
-    case 128: return launch<128, float>(q, k, v, O, LSE, part, p, S, chunk, st);
+    case 32: return launch_rows<32, float>(q, k, v, O, LSE, part, p, S, chunk, st);
+    case 64: return launch_rows<64, float>(q, k, v, O, LSE, part, p, S, chunk, st);
+    case 128: return launch_rows<128, float>(q, k, v, O, LSE, part, p, S, chunk, st);
     default: return cudaErrorInvalidValue;
   }
 }

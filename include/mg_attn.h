@@ -177,7 +177,7 @@ int mg_attn_bwd_noalloc(const void *Q, const void *K, const void *V, const void 
                         int B, int H, int L, int D, int causal, float scale, int contract,
                         void *stream);
 
-/* Workspace bytes for mg_attn_fwd_decode (one partial record of D + 2 f32 per
+/* Workspace bytes for mg_attn_fwd_decode (one partial record of D + 4 f32 per
  * head, key split and query row, rounded up to 256 bytes). 0 for invalid
  * arguments or Lq > 8. */
 size_t mg_attn_fwd_decode_workspace_bytes(int B, int H, int Lq, int Lk, int D, int contract);

@@ -215,18 +215,21 @@ def test_fwd_decode_rejects(lib, kw, code):
 
 
 def test_decode_workspace_bytes(lib):
-    """One record of D + 2 floats per (head, key split, query row); the split
+    """One record of D + 4 floats per (head, key split, query row); the split
     count is at least one, at most one per 256 keys, and the size is a multiple
-    of 256 bytes. Worked case: B=1, H=8, Lk=32768 asks for ceil(608 / 8) = 76
-    splits of ceil(32768 / 76) = 432 -> 448 keys (whole 32-key tiles), which
-    covers the keys in 74 splits: 8 * 74 * 1 * 130 floats = 307,840 bytes,
-    rounded up to 307,968."""
-    assert lib.mg_attn_fwd_decode_workspace_bytes(1, 8, 1, 32768, 128, 1) == 307968
+    of 256 bytes. Worked cases: B=1, H=8, Lk=32768 asks for ceil(1216 / 8) = 152
+    splits, capped at 32768 / 256 = 128 splits of 256 keys: 8 * 128 * 1 * 132
+    floats = 540,672 bytes. B=1, H=8, Lk=100000 keeps 152 splits of
+    ceil(100000 / 152) = 658 -> 672 keys (whole 32-key tiles), which cover the
+    keys in 149 splits: 8 * 149 * 3 * 132 floats (Lq = 3) = 1,888,128 bytes,
+    rounded up to 1,888,256."""
+    assert lib.mg_attn_fwd_decode_workspace_bytes(1, 8, 1, 32768, 128, 1) == 540672
+    assert lib.mg_attn_fwd_decode_workspace_bytes(1, 8, 3, 100000, 128, 0) == 1888256
     for (B, H, Lq, Lk, D) in [(1, 1, 1, 1, 32), (2, 3, 8, 5000, 64), (4, 32, 3, 100000, 128),
                               (64, 64, 1, 4096, 128)]:
         for contract in (0, 1):
             n = lib.mg_attn_fwd_decode_workspace_bytes(B, H, Lq, Lk, D, contract)
-            rec = B * H * Lq * (D + 2) * 4
+            rec = B * H * Lq * (D + 4) * 4
             assert n % 256 == 0 and rec <= n < rec * max(1, -(-Lk // 256)) + 256, (B, H, Lq, Lk)
     assert lib.mg_attn_fwd_decode_workspace_bytes(1, 1, 9, 100, 64, 0) == 0
     assert lib.mg_attn_fwd_decode_workspace_bytes(1, 1, 1, 0, 64, 0) == 0
