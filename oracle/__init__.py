@@ -18,7 +18,8 @@ key-shift metamorphic relation; torch float64 SDPA + autograd on tiny shapes.
 For cross attention (Lq != Lk) and the two causal alignments: central finite
 differences for every alignment, the alignments coinciding when Lq = Lk, a
 single bottom-right query seeing every key, empty-softmax rows contributing
-nothing, and torch float64 SDPA with explicit boolean masks + autograd.
+nothing, torch float64 SDPA with explicit boolean masks + autograd, and three
+hand-derived worked examples with exact rationals (``tests/test_golden.py``).
 """
 from __future__ import annotations
 
