@@ -316,16 +316,6 @@ __global__ void __launch_bounds__(320, 1)
   }
 }
 
-uint64_t wait_limit_ns() {
-  static uint64_t v = [] {
-    const char *e = getenv("MG_WAIT_TIMEOUT_MS");
-    long long ms = e ? atoll(e) : 4000;
-    if (ms < 1) ms = 1;
-    return static_cast<uint64_t>(ms) * 1000000ull;
-  }();
-  return v;
-}
-
 template <int DP>
 cudaError_t launch(const __nv_bfloat16 *Q, const __nv_bfloat16 *K, const __nv_bfloat16 *V,
                    const __nv_bfloat16 *dO, const float *LSE, const float *Dvec, float *dQ,
@@ -347,7 +337,7 @@ cudaError_t launch(const __nv_bfloat16 *Q, const __nv_bfloat16 *K, const __nv_bf
   kern<<<static_cast<unsigned>(grid), C::NTHREADS, C::SMEM_BYTES, st>>>(
       tq, tdo, tk, tv, LSE, Dvec, dQ, BH, p.L, p.Lk, p.D, p.causal, p.off, p.scale,
       p.scale * kLog2e, err,
-      wait_limit_ns());
+      mg_wait_limit_ns());
   return cudaGetLastError();
 }
 

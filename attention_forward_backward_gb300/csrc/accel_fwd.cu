@@ -352,16 +352,6 @@ __global__ void __launch_bounds__(320, 1)
   }
 }
 
-uint64_t wait_limit_ns() {
-  static uint64_t v = [] {
-    const char *e = getenv("MG_WAIT_TIMEOUT_MS");
-    long long ms = e ? atoll(e) : 4000;
-    if (ms < 1) ms = 1;
-    return static_cast<uint64_t>(ms) * 1000000ull;
-  }();
-  return v;
-}
-
 // Test hook: MG_FAULT_INJECT=skip_k_tile makes the forward's producer skip one
 // key-tile load (read once per process; off unless the variable is set).
 int fault_mode() {
@@ -391,7 +381,7 @@ cudaError_t launch(const __nv_bfloat16 *Q, const __nv_bfloat16 *K, const __nv_bf
   const long long grid = static_cast<long long>(nqb) * BH;
   kern<<<static_cast<unsigned>(grid), C::NTHREADS, C::SMEM_BYTES, st>>>(
       tq, tk, tv, O, LSE, BH, p.L, p.Lk, p.D, p.causal, p.off, p.scale * kLog2e, err,
-      wait_limit_ns(), fault_mode());
+      mg_wait_limit_ns(), fault_mode());
   return cudaGetLastError();
 }
 

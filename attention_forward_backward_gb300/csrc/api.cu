@@ -154,6 +154,16 @@ size_t ws_bytes(int B, int H, int L) {
 
 }  // namespace
 
+uint64_t mg_wait_limit_ns() {
+  static const uint64_t v = [] {
+    const char *e = getenv("MG_WAIT_TIMEOUT_MS");
+    long long ms = e ? atoll(e) : 4000;
+    if (ms < 1) ms = 1;
+    return static_cast<uint64_t>(ms) * 1000000ull;
+  }();
+  return v;
+}
+
 cudaError_t mg_set_smem_attr(const void *func, int bytes, int slot) {
   const int dev = current_device();
   if (dev < 0) return cudaErrorNoDevice;

@@ -70,6 +70,10 @@ cudaError_t mg_launch_accel_dkdv_pp(const __nv_bfloat16 *Q, const __nv_bfloat16 
                                     const float *LSE, const float *Dvec, float *dK, float *dV,
                                     const MgProblem &p, unsigned int *err, cudaStream_t st);
 
+// Limit of every bounded wait in the tensor-core kernels, in ns: the environment
+// variable MG_WAIT_TIMEOUT_MS (read once per process, at least 1 ms), else 4 s.
+uint64_t mg_wait_limit_ns();
+
 // Split-key forward for at most mg_decode_max_rows() query rows (decoding). The
 // partial records need mg_decode_workspace_floats() floats of scratch.
 int mg_decode_max_rows();
