@@ -32,7 +32,7 @@ __device__ __forceinline__ float load_in(const __nv_bfloat16 *p, size_t i) {
 }
 
 // Eight consecutive input elements as raw registers (16-byte loads): fetched one
-// tile ahead, widened to f32 when stored to shared memory.
+// step ahead, widened to f32 registers when the step uses them.
 template <typename TIn> struct Raw8;
 template <> struct Raw8<float> {
   float4 a, b;
