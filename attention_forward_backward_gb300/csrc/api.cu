@@ -164,6 +164,24 @@ uint64_t mg_wait_limit_ns() {
   return v;
 }
 
+int mg_check_args(int B, int H, int Lq, int Lk, int D, int mask, float scale, int contract) {
+  return check_common(B, H, Lq, Lk, D, mask, scale, contract);
+}
+
+int mg_sm_count() {
+  static int cached[kMaxDevices] = {};
+  const int dev = current_device();
+  if (dev < 0 || dev >= kMaxDevices) return 152;
+  std::lock_guard<std::mutex> lk(g_mu);
+  if (!cached[dev]) {
+    int n = 0;
+    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n < 1)
+      n = 152;
+    cached[dev] = n;
+  }
+  return cached[dev];
+}
+
 cudaError_t mg_set_smem_attr(const void *func, int bytes, int slot) {
   const int dev = current_device();
   if (dev < 0) return cudaErrorNoDevice;

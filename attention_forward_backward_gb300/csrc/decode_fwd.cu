@@ -315,11 +315,12 @@ cudaError_t launch_rows(const TIn *Q, const TIn *K, const TIn *V, float *O, floa
 
 int mg_decode_max_rows() { return kMaxLq; }
 
-// Splits of the key axis: about eight CTAs per SM of a 152-SM GB300, at least 256
-// keys per split. Depends only on the shape (the workspace size uses it too).
+// Splits of the key axis: about eight CTAs per SM of the current device (its SM
+// count is read once per device), at least 256 keys per split. Depends only on
+// the shape and the device, so the workspace query and the call agree.
 void mg_decode_split(const MgProblem &p, int *S, int *chunk) {
   const long long BH = static_cast<long long>(p.B) * p.H;
-  const int want = static_cast<int>((8LL * 152 + BH - 1) / BH);
+  const int want = static_cast<int>((8LL * mg_sm_count() + BH - 1) / BH);
   const int maxs = (p.Lk + 255) / 256;
   int s = want < 1 ? 1 : want;
   if (s > maxs) s = maxs;

@@ -83,6 +83,14 @@ cudaError_t mg_launch_decode_fwd(const void *Q, const void *K, const void *V, fl
                                  float *LSE, float *part, const MgProblem &p, bool bf16,
                                  cudaStream_t st);
 
+// The argument checks every compute call starts with (sizes, mask, scale,
+// contract, head dim), in the same order: MG_OK or the mg_status_t to return.
+int mg_check_args(int B, int H, int Lq, int Lk, int D, int mask, float scale, int contract);
+
+// Number of SMs of the current device, read once per device (152 on a GB300;
+// 152 is also the answer if the device cannot be queried).
+int mg_sm_count();
+
 // Opt a kernel into more than 48 KB of dynamic shared memory once per device.
 cudaError_t mg_set_smem_attr(const void *func, int bytes, int slot);
 

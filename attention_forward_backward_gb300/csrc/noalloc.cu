@@ -20,7 +20,13 @@
 // Host code cannot use the array's name as a device pointer (it names a host
 // stand-in), so the first call on each device looks up the array's device
 // address with cudaGetSymbolAddress while that device is current and caches
-// it; that first call should therefore happen before any stream capture.
+// it; that first call should therefore happen before any stream capture. The
+// cached address belongs to the device's current context: after
+// cudaDeviceReset on that device it is stale, so the library must not be used on
+// a device that has been reset since its first call there.
+//
+// Argument errors are reported exactly as mg_attn_bwd reports them (same checks,
+// same order); only then is B*H*L compared with the array's size.
 #include <mutex>
 
 #include "../../include/mg_attn.h"
@@ -56,7 +62,14 @@ extern "C" int mg_attn_bwd_noalloc(const void *Q, const void *K, const void *V, 
                                    const void *dO, const float *LSE, void *dQ, void *dK,
                                    void *dV, int B, int H, int L, int D, int causal, float scale,
                                    int contract, void *stream) {
-  if (B < 1 || H < 1 || L < 1) return MG_ERR_INVALID_ARG;
+  // mg_attn_bwd's own checks first, in its order, so that every argument error
+  // reports the same status as there; only then the limit of the fixed array.
+  if (causal != 0 && causal != 1) return MG_ERR_INVALID_ARG;
+  int rc = mg_check_args(B, H, L, L, D, causal ? MG_MASK_CAUSAL : MG_MASK_NONE, scale, contract);
+  if (rc != MG_OK) return rc;
+  const void *ptrs[] = {Q, K, V, O, dO, LSE, dQ, dK, dV};
+  for (const void *p : ptrs)
+    if (!p || (reinterpret_cast<uintptr_t>(p) & 15u) != 0) return MG_ERR_INVALID_ARG;
   const long long rows = static_cast<long long>(B) * H * L;
   if (rows > kNoallocMaxRows) return MG_ERR_WORKSPACE;  // beyond the fixed scratch
   float *scratch = scratch_on_current_device();

@@ -316,27 +316,3 @@ __device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
 }
 
 }  // namespace mg_tc
-
-namespace mg_tc {
-
-// 2^x on the FMA/ALU pipes, for x <= 0 (x may be -inf), to relieve the MUFU
-// unit (one ex2 per attention score otherwise competes with the tensor core).
-// Range reduction in the style of Cody and Waite: x = j + f with j = round(x),
-// f in [-1/2, 1/2]; adding 1.5 * 2^23 leaves j in the low mantissa bits.
-// 2^f comes from a degree-3 polynomial fitted here by the Remez exchange
-// algorithm for minimum maximum relative error on [-1/2, 1/2] (7.5e-5, far
-// below the bf16 rounding that P gets next); 2^j is added to the exponent
-// field. Below -126 the result is 0 (this also makes masked -inf scores 0).
-__device__ __forceinline__ float exp2_poly3(float x) {
-  const float xc = fmaxf(x, -126.f);
-  const float t = xc + 12582912.f;
-  const float j = t - 12582912.f;
-  const float f = xc - j;
-  float p = fmaf(0.0551716685295105f, f, 0.2426111251115799f);
-  p = fmaf(p, f, 0.6932609677314758f);
-  p = fmaf(p, f, 0.9999280571937561f);
-  const float y = __int_as_float(__float_as_int(p) + (__float_as_int(t) << 23));
-  return x < -126.f ? 0.f : y;  // masked scores (-inf) give exactly 0
-}
-
-}  // namespace mg_tc

@@ -55,6 +55,12 @@
  * a device error word; mg_get_device_error() reports it as MG_ERR_TIMEOUT.
  * Nothing aborts the process.
  *
+ * Device state. The library looks up, once per device, the device addresses of
+ * its own module variables (the device error word, the no-allocation scratch)
+ * and caches them. They belong to the device's context: after cudaDeviceReset
+ * on a device the library has used, the cached addresses are stale, so do not
+ * call the library on a device reset since its first call there.
+ *
  * Preconditions checked: pointers non-NULL and 16-byte aligned; B, H, L >= 1;
  * B*H <= 2^24, L (Lq, Lk) <= 2^20; D in {32, 64, 128} (else
  * MG_ERR_UNSUPPORTED); causal in {0, 1} (mask one of mg_mask_t); scale finite
@@ -162,10 +168,11 @@ int mg_attn_bwd_ex(const void *Q, const void *K, const void *V, const void *O,
  * offers no scratch, a service that fixes its memory budget at start-up, a
  * caller that cannot afford cudaMalloc's implicit synchronisation). The paper
  * has no counterpart: its runtime plans every buffer itself.
- * Same arguments, results and errors as mg_attn_bwd minus the workspace. The
- * Dvec scratch is a fixed device array inside the library (4 MiB, held by every
- * GPU that loads the library until the process exits), so B*H*L must not
- * exceed 1,048,576 rows; larger problems return MG_ERR_WORKSPACE before
+ * Same arguments, results and errors as mg_attn_bwd minus the workspace (its
+ * argument checks run first, in the same order). The Dvec scratch is a fixed
+ * device array inside the library (4 MiB, held by every GPU that loads the
+ * library until the process exits), so B*H*L must not exceed 1,048,576 rows;
+ * larger problems with otherwise valid arguments return MG_ERR_WORKSPACE before
  * anything is launched. Nothing is allocated or freed.
  * The first call on each device looks up the array's device address (make it
  * before any stream capture). All calls on a device share the array: calls

@@ -1,16 +1,18 @@
 """mg_attn_bwd_noalloc: the backward for callers that cannot allocate device
 memory (its Dvec scratch is a fixed array inside the library instead of a
-caller workspace). Called through the C ABI and compared with mg_attn_bwd on
-the same inputs, twice in a row, so that the shared array's leftover contents
-from the first call cannot leak into the second. Collected last on purpose."""
+caller workspace). Called through the C ABI and compared, twice in a row (so
+that the shared array's leftover contents from the first call cannot leak into
+the second), with mg_attn_bwd on the same inputs and with the fp64 oracle.
+Collected last on purpose."""
 import ctypes
 
 import numpy as np
 import pytest
 
 import attention_forward_backward_gb300 as mg
+import oracle
 from attention_forward_backward_gb300 import synth
-from parity_util import TOL, device_inputs, rel_err
+from parity_util import TOL, compare, device_inputs, rel_err
 
 pytestmark = pytest.mark.gpu
 
@@ -34,13 +36,14 @@ def test_noalloc_matches_workspace_backward(contract):
              synth.custom_workload(1, 3, 257, 128, False, seed_cfg=871)]
     stream = torch.cuda.current_stream().cuda_stream
     for w in cases:
-        dev, _ = device_inputs(synth.inputs(w, contract), contract)
+        dev, vals = device_inputs(synth.inputs(w, contract), contract)
         B, H, L, D = w.shape
         O, LSE = mg.attention_fwd(dev["Q"], dev["K"], dev["V"], w.causal, w.scale, contract)
         ref = mg.attention_bwd(dev["Q"], dev["K"], dev["V"], O, dev["dO"], LSE, w.causal,
                                w.scale, contract)
         torch.cuda.synchronize()
         ref = [t.cpu().numpy() for t in ref]
+        exact = oracle.attn_bwd(vals["Q"], vals["K"], vals["V"], vals["dO"], w.causal, w.scale)
         for _ in range(2):
             outs = [torch.full_like(O, float("nan")) for _ in range(3)]
             rc = lib.mg_attn_bwd_noalloc(
@@ -51,8 +54,12 @@ def test_noalloc_matches_workspace_backward(contract):
             assert rc == mg.MG_OK, mg.mg_status_string(rc)
             torch.cuda.synchronize()
             assert mg.mg_get_device_error() == mg.MG_OK
-            for got, want in zip(outs, ref):
-                assert rel_err(got.cpu().numpy(), want) <= TOL[contract]
+            got = [t.cpu().numpy() for t in outs]
+            for g, want in zip(got, ref):
+                assert rel_err(g, want) <= TOL[contract]
+            errs, bad = compare(dict(zip(("dQ", "dK", "dV"), got)), exact, contract,
+                                keys=("dQ", "dK", "dV"))
+            assert not bad, (w.name, errs)
 
 
 def test_noalloc_rejects_beyond_the_fixed_scratch():
@@ -64,3 +71,17 @@ def test_noalloc_rejects_beyond_the_fixed_scratch():
     rc = lib.mg_attn_bwd_noalloc(fake, fake, fake, fake, fake, fake, fake, fake, fake,
                                  2, 32, 16385, 128, 1, 0.125, 1, None)
     assert rc == mg.MG_ERR_WORKSPACE
+
+
+def test_noalloc_reports_argument_errors_before_the_size_limit():
+    """A shape beyond the fixed array with an invalid head dim, mask flag or
+    sequence length reports the same status as mg_attn_bwd, not MG_ERR_WORKSPACE."""
+    lib = _lib()
+    fake = 1 << 40  # never dereferenced: the argument checks come first
+    args = [fake] * 9
+    big = (2, 32, 16385)
+    assert lib.mg_attn_bwd_noalloc(*args, *big, 96, 1, 0.125, 1, None) == mg.MG_ERR_UNSUPPORTED
+    assert lib.mg_attn_bwd_noalloc(*args, *big, 128, 2, 0.125, 1, None) == mg.MG_ERR_INVALID_ARG
+    assert lib.mg_attn_bwd_noalloc(*args, *big, 128, 1, 0.125, 7, None) == mg.MG_ERR_INVALID_ARG
+    assert lib.mg_attn_bwd_noalloc(*args, 1, 1, (1 << 20) + 1, 64, 1, 0.125, 0,
+                                   None) == mg.MG_ERR_INVALID_ARG
