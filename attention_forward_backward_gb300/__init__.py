@@ -13,6 +13,7 @@ The function names mirror the C ABI in ``include/mg_attn.h``:
   workspace, stream=None)``
 * ``mg_attn_fwd_ex``, ``mg_attn_bwd_workspace_bytes_ex``, ``mg_attn_bwd_ex`` (cross
   attention, Lq != Lk, with a mask)
+* ``mg_attn_fwd_padded``, ``mg_attn_bwd_padded`` (per-batch key padding lengths)
 * ``mg_attn_fwd_decode_workspace_bytes``, ``mg_attn_fwd_decode`` (split-key
   forward for at most 8 query rows)
 * ``mg_status_string(status)``, ``mg_get_device_error(stream=None)``
@@ -74,6 +75,11 @@ def load_library(path: str | None = None):
         lib.mg_attn_bwd_ex.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, i, i, i, i, i, i, f,
                                        i, vp, sz, vp]
         lib.mg_attn_bwd_ex.restype = i
+        lib.mg_attn_fwd_padded.argtypes = [vp, vp, vp, vp, vp, vp, i, i, i, i, i, i, f, i, vp]
+        lib.mg_attn_fwd_padded.restype = i
+        lib.mg_attn_bwd_padded.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, i, i, i, i,
+                                           i, i, f, i, vp, sz, vp]
+        lib.mg_attn_bwd_padded.restype = i
         lib.mg_attn_fwd_decode_workspace_bytes.argtypes = [i, i, i, i, i, i]
         lib.mg_attn_fwd_decode_workspace_bytes.restype = sz
         lib.mg_attn_fwd_decode.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, i, i, f, i, vp, sz,
@@ -189,6 +195,35 @@ def mg_attn_bwd_ex(Q, K, V, O, dO, LSE, dQ, dK, dV, mask, scale, contract, works
                                        _ptr(workspace), ws_bytes, _stream(stream))
     if rc != MG_OK:
         raise MgError(rc, "mg_attn_bwd_ex")
+    return rc
+
+
+def mg_attn_fwd_padded(Q, K, V, O, LSE, kv_len, mask, scale, contract, stream=None) -> int:
+    """Forward with per-batch key padding: kv_len is a CUDA int32 tensor of B
+    lengths (or None); shapes and mask as in mg_attn_fwd_ex."""
+    B, H, Lq, D = _dims(Q)
+    Lk = int(K.shape[2])
+    rc = load_library().mg_attn_fwd_padded(_ptr(Q), _ptr(K), _ptr(V), _ptr(O), _ptr(LSE),
+                                           _ptr(kv_len), B, H, Lq, Lk, D, _mask(mask),
+                                           float(scale), _contract(contract), _stream(stream))
+    if rc != MG_OK:
+        raise MgError(rc, "mg_attn_fwd_padded")
+    return rc
+
+
+def mg_attn_bwd_padded(Q, K, V, O, dO, LSE, dQ, dK, dV, kv_len, mask, scale, contract,
+                       workspace, stream=None) -> int:
+    """Backward with per-batch key padding (shapes as in mg_attn_bwd_ex)."""
+    B, H, Lq, D = _dims(Q)
+    Lk = int(K.shape[2])
+    ws_bytes = workspace.numel() * workspace.element_size() if workspace is not None else 0
+    rc = load_library().mg_attn_bwd_padded(_ptr(Q), _ptr(K), _ptr(V), _ptr(O), _ptr(dO),
+                                           _ptr(LSE), _ptr(dQ), _ptr(dK), _ptr(dV),
+                                           _ptr(kv_len), B, H, Lq, Lk, D, _mask(mask),
+                                           float(scale), _contract(contract), _ptr(workspace),
+                                           ws_bytes, _stream(stream))
+    if rc != MG_OK:
+        raise MgError(rc, "mg_attn_bwd_padded")
     return rc
 
 

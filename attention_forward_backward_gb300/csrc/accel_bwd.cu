@@ -1,6 +1,6 @@
 // accel_bwd.cu -- ACCEL_BF16 attention backward on tcgen05 tensor cores: one
 // fused kernel per 128-key block that accumulates dK and dV in tensor memory
-// and adds its dQ contribution into global f32 dQ with TMA bulk reductions.
+// and adds its dQ contribution into global f32 dQ.
 //
 // "Meganeura: Portable GPU Training and Inference through Vulkan and Metal"
 // splits the attention derivative into a dQ kernel and a fused dK+dV kernel
@@ -10,29 +10,40 @@
 // they enter an MMA, exactly like the forward's P.
 //
 // Per CTA: keys k0 .. k0+127 of one (b, h) head (TMEM lanes = keys). K and V
-// are loaded once; the query axis is walked in blocks of BQ rows (64 for
-// D = 128, 128 for D = 64), Q and dO by TMA through a 2-stage ring.
-// Per query block i:
-//   S^T  = K Q_i^T            (TMEM, f32)     dP^T = V dO_i^T   (TMEM, f32)
-//   P^T  = exp2(S^T scale log2e - LSE_i log2e), masked        (softmax warps)
-//   dV  += P^T dO_i           (A = P^T from TMEM, bf16)
-//   dS^T = P^T (dP^T - Dvec_i)                                (softmax warps)
-//   dK  += dS^T Q_i           (A = dS^T from TMEM, bf16)
-//   dQ_i = dS K               (dS^T also staged in smem; for D = 128 the MMA
-//                              computes dQ_i^T = K^T dS^T so that M = 128)
-// dQ_i leaves TMEM through a swizzled f32 staging tile and a TMA tensor
-// add-reduction into dQ (zeroed by the host call beforehand); bulk reductions
-// sustain far more L2 throughput than per-element f32 reductions would.
-// MMA issue order per block: dV(i), S(i+1), dP(i+1), dK(i), dQ(i), so that the
-// tensor core computes the next block's scores while the softmax warps turn
-// dP(i) into dS(i), and dK/dQ run while they turn S(i+1) into P(i+1). dP^T is
-// double-buffered in TMEM for D = 128 (for D = 64 it goes after dQ(i)); Q and
-// dO stream through a 3-stage ring so that a tile's load has two blocks of
-// lead time.
-// Warp roles: 0-3 dQ epilogue, 4 TMA producer (plus LSE/Dvec staging), 5 MMA
-// issuer, 8-15 two softmax warpgroups splitting the query columns.
-// Every wait is bounded; on a give-up the CTA sets the device error word and
-// leaves through the normal teardown (own copies and MMAs drained first).
+// are loaded once; the query axis is walked in blocks of 128 rows, Q and dO by
+// TMA through two rings of NQS stages each. Per query block j:
+//   S^T  = K Q_j^T            (TMEM, f32)     dP^T = V dO_j^T   (TMEM, f32)
+//   P^T  = exp2(S^T scale log2e - LSE_j log2e), masked        (softmax warps)
+//   dV  += P^T dO_j           (A = P^T from TMEM, bf16)
+//   dS^T = P^T (dP^T - Dvec_j)                                (softmax warps)
+//   dK  += dS^T Q_j           (A = dS^T from TMEM, bf16)
+//   dQ_j = dS K               (dS^T also staged in shared memory)
+// Every product is a 128 x 128 (D = 128) or 128 x 64 (D = 64) MMA group, so one
+// issuing thread keeps up with the tensor core and each byte an operand moves
+// through shared memory feeds twice the flops of 64-row query blocks.
+//
+// Tensor memory (512 columns) holds dV, dK, S^T and dP^T. At D = 128 that is
+// all of it, so dQ_j^T = K^T dS_j^T is accumulated over the dP^T columns once
+// dK_j has read dS_j^T from them (MMAs of one thread run in issue order), and
+// dP_{j+1} waits until the dQ warps have read dQ_j^T out. Those warps stage it
+// in dO_j's ring stage (dead once dP_j and dV_j, which precede dQ_j, are done),
+// 64 query rows at a time, each warp one 32-column box of d, and add it into
+// global dQ with TMA tensor add-reductions; the stage returns to the dO
+// producer only after those reductions have read it. (Per-element red.global
+// reductions from registers were measured about ten times slower to drain.)
+// At D = 64 dQ_j = dS K has columns and a staging tile of its own.
+//
+// MMA issue order (steady state, block j):
+//   dK(j), dQ(j), dV(j+1), dP(j+1), S(j+2)
+// dV(j+1) and S(j+2) overlap the read-out of dQ(j); the softmax turns S(j+1)
+// into P(j+1) while dK(j) and dQ(j) run, and dP(j+1) into dS(j+1) while S(j+2)
+// runs. S(j+2) overwrites P(j+1) only after dV(j+1) has read it (issue order).
+//
+// Warp roles: 0-3 dQ read-out, 4 TMA producer of K, V, Q (plus LSE and Dvec
+// staging), 5 MMA issuer, 6 TMA producer of dO, 8-15 two softmax warpgroups
+// splitting the 128 query columns. Every wait is bounded; on a give-up the CTA
+// sets the device error word and leaves through the normal teardown (own copies
+// and MMAs drained first).
 #include <climits>
 
 #include "internal.h"
@@ -45,56 +56,66 @@ using namespace mg_tc;
 
 template <int DP>
 struct BwdCfg {
-  static constexpr int BN = 128;                    // keys per CTA
-  static constexpr int BQ = DP == 128 ? 64 : 128;   // queries per block
-  static constexpr int QPW = BQ / 2;                // query columns per softmax warpgroup
-  static constexpr int ND = DP == 128 ? 2 : 1;      // dP^T buffers in TMEM
-  static constexpr int NCHUNK = DP / 64;
+  static constexpr int BN = 128;                   // keys per CTA (TMEM lanes)
+  static constexpr int BQ = 128;                   // queries per block
+  static constexpr int QPW = BQ / 2;               // query columns per softmax warpgroup
+  static constexpr int NCHUNK = DP / 64;           // 64-column boxes per row
+  static constexpr bool kDqInDp = DP == 128;       // dQ^T accumulated over dP^T's columns
+  static constexpr int NQS = DP == 128 ? 2 : 3;    // Q and dO ring stages
   static constexpr int KV_TILE = BN * DP * 2;
   static constexpr int BOX_KV = BN * 128;
   static constexpr int Q_TILE = BQ * DP * 2;
   static constexpr int BOX_Q = BQ * 128;
-  static constexpr int DS_CHUNK = BN * 128;         // [128 keys][64 q] bf16
-  static constexpr int NQC = BQ / 64;               // dS^T chunks
-  static constexpr int DS_BUF = NQC * DS_CHUNK;
-  static constexpr int NQS = 3;                     // Q/dO ring stages
-  static constexpr int NDS = DP == 128 ? 2 : 1;     // dS^T smem buffers
-  static constexpr int DQ_BOX = BQ * 128;           // [BQ][32] f32
-  static constexpr int DQ_STAGE = (DP / 32) * DQ_BOX;
-  // shared memory
+  static constexpr int DS_CHUNK = BN * 128;        // [128 keys][64 q] bf16
+  static constexpr int DS_BUF = (BQ / 64) * DS_CHUNK;
+  // dQ staging: D = 64, its own [BQ][64] f32 tile in boxes of [BQ][32] (each
+  // read-out warp reduces its 32-row slab); D = 128, half the query rows at a
+  // time ([64][128] f32 = one dO stage, boxes of [64][32]) over dO_j's stage
+  static constexpr int DQ_ROWS = kDqInDp ? 64 : BQ;
+  static constexpr int DQ_BOX = DQ_ROWS * 128;
+  static constexpr int DQ_STAGE = kDqInDp ? 0 : (DP / 32) * DQ_BOX;
+  static constexpr int DQ_TMA_ROWS = kDqInDp ? 64 : 32;  // rows per reduction box
+  // shared memory: 1024-aligned tiles first, then the small items
   static constexpr int OFF_K = 0;
   static constexpr int OFF_V = OFF_K + KV_TILE;
   static constexpr int OFF_Q = OFF_V + KV_TILE;             // NQS stages
   static constexpr int OFF_DO = OFF_Q + NQS * Q_TILE;       // NQS stages
-  static constexpr int OFF_DS = OFF_DO + NQS * Q_TILE;      // NDS dS^T tiles
-  static constexpr int OFF_DQ = OFF_DS + NDS * DS_BUF;      // dQ staging
-  static constexpr int OFF_LSE = OFF_DQ + DQ_STAGE;          // NQS stages x BQ f32
-  static constexpr int OFF_DV = OFF_LSE + NQS * BQ * 4;        // NQS stages x BQ f32
+  static constexpr int OFF_DS = OFF_DO + NQS * Q_TILE;      // dS^T tile
+  static constexpr int OFF_DQ = OFF_DS + DS_BUF;            // dQ staging (D = 64)
+  static constexpr int OFF_LSE = OFF_DQ + DQ_STAGE;         // NQS x BQ f32
+  static constexpr int OFF_DV = OFF_LSE + NQS * BQ * 4;     // NQS x BQ f32
   static constexpr int OFF_BAR = OFF_DV + NQS * BQ * 4;
   static constexpr int B_KVFULL = 0;
-  static constexpr int B_QFULL = 1;                  // NQS (Q/dO stage)
-  static constexpr int B_QEMPTY = B_QFULL + 4;       // NQS
-  static constexpr int B_SFULL = B_QEMPTY + 4;
+  static constexpr int B_QFULL = 1;                 // NQS (Q stage; also LSE, Dvec)
+  static constexpr int B_QFREE = B_QFULL + 4;       // NQS
+  static constexpr int B_DOFULL = B_QFREE + 4;      // NQS
+  static constexpr int B_DOFREE = B_DOFULL + 4;     // NQS
+  static constexpr int B_SFULL = B_DOFREE + 4;
   static constexpr int B_PREADY = B_SFULL + 1;
-  static constexpr int B_DPFULL = B_PREADY + 1;      // 2 (dP buffer)
-  static constexpr int B_DSREADY = B_DPFULL + 2;     // 2 (block parity)
-  static constexpr int B_DSMFREE = B_DSREADY + 2;    // 2 (dS smem buffer)
-  static constexpr int B_DQFULL = B_DSMFREE + 2;
+  static constexpr int B_DPFULL = B_PREADY + 1;
+  static constexpr int B_DSREADY = B_DPFULL + 1;
+  static constexpr int B_DSMFREE = B_DSREADY + 1;
+  static constexpr int B_DQFULL = B_DSMFREE + 1;
   static constexpr int B_DQEMPTY = B_DQFULL + 1;
   static constexpr int B_ACCDONE = B_DQEMPTY + 1;
   static constexpr int B_DRAIN = B_ACCDONE + 1;
   static constexpr int NBAR = B_DRAIN + 1;
   static constexpr int OFF_MISC = OFF_BAR + NBAR * 8;
-  static constexpr int SMEM_BYTES = OFF_MISC + 16 + 1024;
+  static constexpr int SMEM_USED = OFF_MISC + 16;
+  // request up to 1 KB of slack to align the base; the kernel checks the slack
+  static constexpr int SMEM_LIMIT = 227 * 1024;
+  static constexpr int SMEM_BYTES =
+      SMEM_USED + 1024 <= SMEM_LIMIT ? SMEM_USED + 1024 : SMEM_LIMIT;
   static constexpr int NTHREADS = 512;
   static constexpr int TMEM_COLS = 512;
   static constexpr int T_DV = 0;
   static constexpr int T_DK = DP;
-  static constexpr int T_S = 2 * DP;                  // BQ
-  static constexpr int T_DP = T_S + BQ;               // ND x BQ
-  static constexpr int T_DQ = T_DP + ND * BQ;         // 64
-  static_assert(T_DQ + 64 <= TMEM_COLS, "TMEM column budget");
-  static_assert(SMEM_BYTES <= 227 * 1024, "shared memory budget");
+  static constexpr int T_S = 2 * DP;                  // BQ columns
+  static constexpr int T_DP = T_S + BQ;               // BQ columns
+  static constexpr int T_DQ = kDqInDp ? T_DP : T_DP + BQ;
+  static_assert(NQS <= 4, "barrier slots");
+  static_assert(kDqInDp ? T_DP + BQ <= TMEM_COLS : T_DQ + DP <= TMEM_COLS, "TMEM budget");
+  static_assert(SMEM_USED <= SMEM_LIMIT, "shared memory budget");
 };
 
 __device__ __forceinline__ bool drain_wait(uint32_t bar, uint32_t parity, uint64_t limit_ns) {
@@ -105,16 +126,13 @@ __device__ __forceinline__ bool drain_wait(uint32_t bar, uint32_t parity, uint64
   return true;
 }
 
-__device__ __forceinline__ void named_bar_sync(int id, int count) {
-  asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(count) : "memory");
-}
-
 __device__ __forceinline__ void st_shared_v4(uint32_t addr, uint32_t a, uint32_t b, uint32_t c,
                                              uint32_t d) {
   asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(a), "r"(b), "r"(c),
                "r"(d)
                : "memory");
 }
+
 __device__ __forceinline__ void st_shared_f32(uint32_t addr, float v) {
   asm volatile("st.shared.f32 [%0], %1;" ::"r"(addr), "f"(v) : "memory");
 }
@@ -135,14 +153,21 @@ __global__ void __launch_bounds__(512, 1)
                       const __grid_constant__ CUtensorMap tmdO,
                       const __grid_constant__ CUtensorMap tmdQ, const float *__restrict__ LSE,
                       const float *__restrict__ Dvec, float *__restrict__ dQ,
-                      float *__restrict__ dK,
-                      float *__restrict__ dV, int BH, int L, int Lk, int D, int causal, int off,
-                      float scale,
-                      float scale_log2, unsigned int *err, unsigned long long timeout_ns) {
+                      float *__restrict__ dK, float *__restrict__ dV, int BH, int L,
+                      int Lk_rows, int D, int causal, int off0, float scale, float scale_log2,
+                      unsigned int *err, unsigned long long timeout_ns,
+                      const int *__restrict__ kv_len, int H, int br) {
   using C = BwdCfg<DP>;
   extern __shared__ uint8_t smem_raw[];
-  uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
-                                              ~static_cast<uintptr_t>(1023));
+  const uintptr_t raw = reinterpret_cast<uintptr_t>(smem_raw);
+  uint8_t *smem = reinterpret_cast<uint8_t *>((raw + 1023) & ~static_cast<uintptr_t>(1023));
+  // The tiles need a 1024-byte aligned base (128-byte swizzle atoms). If the
+  // alignment pad does not fit in the slack requested at launch, report and
+  // leave before any barrier or TMEM allocation (uniform over the CTA).
+  if (reinterpret_cast<uintptr_t>(smem) - raw + C::SMEM_USED > C::SMEM_BYTES) {
+    if (threadIdx.x == 0) atomicOr(err, 1u);
+    return;
+  }
   const uint32_t sbase = smem_u32(smem);
   const uint32_t bar0 = sbase + C::OFF_BAR;
   auto bar = [&](int i) { return bar0 + 8u * static_cast<uint32_t>(i); };
@@ -154,14 +179,18 @@ __global__ void __launch_bounds__(512, 1)
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   // Head-major order: CTAs that run together share a few heads' Q/dO in L2;
   // within a head the heaviest causal key block (kb = 0) goes first.
-  // L query rows, Lk key rows; causal: query i sees key j iff j <= i + off
-  const int nkb = (Lk + C::BN - 1) / C::BN;
+  // L query rows, Lk_rows key rows of which this head attends to Lk (all, or
+  // the batch element's padded length); causal: query i sees key j iff
+  // j <= i + off
+  const int nkb = (Lk_rows + C::BN - 1) / C::BN;
   const int bh = static_cast<int>(blockIdx.x / nkb);
   const int kb = static_cast<int>(blockIdx.x % nkb);
   const int k0 = kb * C::BN;
+  const MgKeys keys = mg_keys(kv_len, bh, H, L, Lk_rows, off0, br);
+  const int Lk = keys.len, off = keys.off;
   const int nqb = (L + C::BQ - 1) / C::BQ;
   const int qb0 = causal ? max(0, k0 - off) / C::BQ : 0;  // first block with a query seeing k0
-  const int n = max(0, nqb - qb0);
+  const int n = k0 >= Lk ? 0 : max(0, nqb - qb0);
 
   if (warp == 0) {
     tmem_alloc(smem_u32(tmem_slot), C::TMEM_COLS);
@@ -170,9 +199,11 @@ __global__ void __launch_bounds__(512, 1)
   if (threadIdx.x == 128) {
     for (int i = 0; i < C::NBAR; ++i) {
       uint32_t cnt = 1;
-      if (i >= C::B_QEMPTY && i < C::B_QEMPTY + 4) cnt = 1 + 8;
-      if (i == C::B_PREADY || i == C::B_DSREADY || i == C::B_DSREADY + 1) cnt = 8;
+      if (i >= C::B_QFREE && i < C::B_QFREE + 4) cnt = 1 + 8;
+      if (i == C::B_PREADY || i == C::B_DSREADY) cnt = 8;
       if (i == C::B_DQEMPTY) cnt = 4;
+      // D = 128: a dO stage is released by the four dQ warps (it stages dQ)
+      if (C::kDqInDp && i >= C::B_DOFREE && i < C::B_DOFREE + 4) cnt = 4;
       mbar_init(bar(i), cnt);
     }
     *abort_flag = 0;
@@ -191,7 +222,7 @@ __global__ void __launch_bounds__(512, 1)
   const Abort ab = make_abort(abort_flag, err, timeout_ns);
 
   if (warp == 4) {
-    // ------------------------------------------------------------ producer
+    // ------------------------------------------------------------ producer: K, V, Q, LSE, Dvec
     if (lane == 0) {
       mbar_arrive_expect_tx(bar(C::B_KVFULL), 2 * C::KV_TILE);
       for (int c = 0; c < C::NCHUNK; ++c) {
@@ -200,36 +231,57 @@ __global__ void __launch_bounds__(512, 1)
       }
     }
     int issued = 0;
-    for (int i = 0; i < n; ++i) {
-      const int st = i % C::NQS;
-      if (i >= C::NQS && !mbar_wait_warp(bar(C::B_QEMPTY + st), ((i / C::NQS) - 1) & 1, ab))
-        break;
-      const int q0 = (qb0 + i) * C::BQ;
-      // LSE (pre-scaled to base 2; +inf past L so that P = 0 there) and Dvec.
-      for (int r = lane; r < C::BQ; r += 32) {
-        const int qg = q0 + r;
+    for (int j = 0; j < n; ++j) {
+      const int st = j % C::NQS;
+      const int q0 = (qb0 + j) * C::BQ;
+      // LSE (pre-scaled to base 2; +inf past L so that P = 0 there) and Dvec,
+      // loaded before the wait for the stage so that their latency overlaps it.
+      float lse_r[C::BQ / 32], dv_r[C::BQ / 32];
+#pragma unroll
+      for (int u = 0; u < C::BQ / 32; ++u) {
+        const int qg = q0 + 32 * u + lane;
         const bool v = qg < L;
+        lse_r[u] = v ? LSE[static_cast<size_t>(bh) * L + qg] : -INFINITY;
+        dv_r[u] = v ? Dvec[static_cast<size_t>(bh) * L + qg] : 0.f;
+      }
+      if (j >= C::NQS && !mbar_wait_warp(bar(C::B_QFREE + st), ((j / C::NQS) - 1) & 1, ab))
+        break;
+#pragma unroll
+      for (int u = 0; u < C::BQ / 32; ++u) {
         // +inf also for a row with an empty softmax (LSE = -inf): its P is 0
-        const float lse = v ? LSE[static_cast<size_t>(bh) * L + qg] : -INFINITY;
-        sLse[st * C::BQ + r] = lse == -INFINITY ? INFINITY : lse * kLog2e;
-        sDv[st * C::BQ + r] = v ? Dvec[static_cast<size_t>(bh) * L + qg] : 0.f;
+        sLse[st * C::BQ + 32 * u + lane] = lse_r[u] == -INFINITY ? INFINITY : lse_r[u] * kLog2e;
+        sDv[st * C::BQ + 32 * u + lane] = dv_r[u];
       }
       __syncwarp();
       if (lane == 0) {
-        mbar_arrive_expect_tx(bar(C::B_QFULL + st), 2 * C::Q_TILE);
-        for (int c = 0; c < C::NCHUNK; ++c) {
+        mbar_arrive_expect_tx(bar(C::B_QFULL + st), C::Q_TILE);
+        for (int c = 0; c < C::NCHUNK; ++c)
           tma_load_3d(sbase + C::OFF_Q + st * C::Q_TILE + c * C::BOX_Q, &tmQ, c * 64, q0, bh,
                       bar(C::B_QFULL + st));
-          tma_load_3d(sbase + C::OFF_DO + st * C::Q_TILE + c * C::BOX_Q, &tmdO, c * 64, q0, bh,
-                      bar(C::B_QFULL + st));
-        }
       }
-      issued = i + 1;
+      issued = j + 1;
     }
     if (lane == 0) {
       drain_wait(bar(C::B_KVFULL), 0, 2000000000ull);
-      for (int i = max(0, issued - C::NQS); i < issued; ++i)
-        drain_wait(bar(C::B_QFULL + i % C::NQS), (i / C::NQS) & 1, 2000000000ull);
+      for (int j = max(0, issued - C::NQS); j < issued; ++j)
+        drain_wait(bar(C::B_QFULL + j % C::NQS), (j / C::NQS) & 1, 2000000000ull);
+    }
+  } else if (warp == 6) {
+    // ------------------------------------------------------------ producer: dO
+    if (lane == 0) {
+      int issued = 0;
+      for (int j = 0; j < n; ++j) {
+        const int st = j % C::NQS;
+        if (j >= C::NQS && !mbar_wait(bar(C::B_DOFREE + st), ((j / C::NQS) - 1) & 1, ab)) break;
+        const int q0 = (qb0 + j) * C::BQ;
+        mbar_arrive_expect_tx(bar(C::B_DOFULL + st), C::Q_TILE);
+        for (int c = 0; c < C::NCHUNK; ++c)
+          tma_load_3d(sbase + C::OFF_DO + st * C::Q_TILE + c * C::BOX_Q, &tmdO, c * 64, q0, bh,
+                      bar(C::B_DOFULL + st));
+        issued = j + 1;
+      }
+      for (int j = max(0, issued - C::NQS); j < issued; ++j)
+        drain_wait(bar(C::B_DOFULL + j % C::NQS), (j / C::NQS) & 1, 2000000000ull);
     }
   } else if (warp == 5) {
     // ------------------------------------------------------------ MMA issuer
@@ -237,7 +289,7 @@ __global__ void __launch_bounds__(512, 1)
       constexpr uint32_t idSP = idesc_bf16_f32(128, C::BQ, false, false);
       constexpr uint32_t idKV = idesc_bf16_f32(128, DP, false, true);
       constexpr uint32_t idDQ =
-          DP == 128 ? idesc_bf16_f32(128, C::BQ, true, true) : idesc_bf16_f32(128, DP, true, true);
+          C::kDqInDp ? idesc_bf16_f32(128, C::BQ, true, true) : idesc_bf16_f32(128, DP, true, true);
       bool ok = mbar_wait(bar(C::B_KVFULL), 0, ab);
       // base descriptors; each MMA adds a compile-time byte offset
       const uint32_t sb = opaque_u32(sbase);
@@ -249,13 +301,7 @@ __global__ void __launch_bounds__(512, 1)
       const uint64_t dOmn = sdesc_sw128(sb + C::OFF_DO, C::BOX_Q, 1024);
       const uint64_t dKmn = sdesc_sw128(sb + C::OFF_K, C::BOX_KV, 1024);
       const uint64_t dDSmn = sdesc_sw128(sb + C::OFF_DS, C::DS_CHUNK, 1024);
-      int qwaited = -1;
-      auto wait_q = [&](int i) -> bool {
-        if (qwaited >= i) return true;
-        qwaited = i;
-        return mbar_wait(bar(C::B_QFULL + i % C::NQS), (i / C::NQS) & 1, ab);
-      };
-      // X^T = A_tile * B_i^T with A in {K, V}, B_i in {Q_i, dO_i}; both K-major.
+      // X^T = A_tile * B_j^T with A in {K, V}, B_j in {Q_j, dO_j}; both K-major.
       auto issue_T = [&](uint64_t dA_, uint64_t dB_, uint32_t d) {
         // opaque copies: the per-step descriptors are formed here, not hoisted
         const uint64_t dA = opaque_u64(dA_), dB = opaque_u64(dB_);
@@ -266,22 +312,7 @@ __global__ void __launch_bounds__(512, 1)
           mma_ss(d, sdesc_add(dA, oa), sdesc_add(dB, ob), idSP, kk > 0 ? 1u : 0u);
         }
       };
-      auto issue_S = [&](int i) -> bool {
-        if (!wait_q(i)) return false;
-        tc_fence_after();
-        issue_T(dK0, sdesc_add(dQ0, (i % C::NQS) * C::Q_TILE), tmem + C::T_S);
-        mma_commit(bar(C::B_SFULL));
-        return true;
-      };
-      auto issue_dP = [&](int i) -> bool {
-        if (!wait_q(i)) return false;
-        tc_fence_after();
-        const int db = C::ND == 2 ? (i & 1) : 0;
-        issue_T(dV0, sdesc_add(dO0, (i % C::NQS) * C::Q_TILE), tmem + C::T_DP + db * C::BQ);
-        mma_commit(bar(C::B_DPFULL + db));
-        return true;
-      };
-      // acc (+)= X^T(tmem, bf16) * Y_i (MN-major smem), K = BQ queries.
+      // acc (+)= X^T(tmem, bf16) * Y_j (MN-major smem), K = BQ queries.
       auto issue_acc = [&](uint32_t tA, uint64_t dY_, uint32_t d, bool first) {
         const uint64_t dY = opaque_u64(dY_);
         const uint32_t acc0 = first ? 0u : 1u;
@@ -292,98 +323,167 @@ __global__ void __launch_bounds__(512, 1)
           mma_ts(d, tA + acol, sdesc_add(dY, kk * 2048), idKV, kk > 0 ? 1u : acc0);
         }
       };
-      if (ok && n > 0) ok = issue_S(0);
-      if (ok && n > 0) ok = issue_dP(0);
-      for (int i = 0; ok && i < n; ++i) {
-        const int st = i % C::NQS;
-        const int db = C::ND == 2 ? (i & 1) : 0;
-        if (!(ok = mbar_wait(bar(C::B_PREADY), i & 1, ab))) break;
+      auto issue_S = [&](int j) -> bool {
+        if (!mbar_wait(bar(C::B_QFULL + j % C::NQS), (j / C::NQS) & 1, ab)) return false;
         tc_fence_after();
-        issue_acc(tmem + C::T_S, sdesc_add(dOmn, st * C::Q_TILE), tmem + C::T_DV, i == 0);
-        if (i + 1 < n && !(ok = issue_S(i + 1))) break;
-        if (C::ND == 2 && i + 1 < n && !(ok = issue_dP(i + 1))) break;
-        if (!(ok = mbar_wait(bar(C::B_DSREADY + (i & 1)), (i >> 1) & 1, ab))) break;
+        issue_T(dK0, sdesc_add(dQ0, (j % C::NQS) * C::Q_TILE), tmem + C::T_S);
+        mma_commit(bar(C::B_SFULL));
+        return true;
+      };
+      auto issue_dP = [&](int j) -> bool {
+        if (!mbar_wait(bar(C::B_DOFULL + j % C::NQS), (j / C::NQS) & 1, ab)) return false;
         tc_fence_after();
-        issue_acc(tmem + C::T_DP + db * C::BQ, sdesc_add(dQmn, st * C::Q_TILE), tmem + C::T_DK,
-                  i == 0);
-        mma_commit(bar(C::B_QEMPTY + st));
-        if (i > 0 && !(ok = mbar_wait(bar(C::B_DQEMPTY), (i - 1) & 1, ab))) break;
+        issue_T(dV0, sdesc_add(dO0, (j % C::NQS) * C::Q_TILE), tmem + C::T_DP);
+        mma_commit(bar(C::B_DPFULL));
+        // D = 64: dO_j's last reader is dP(j), except for block 0 whose dV comes
+        // later (D = 128: the dQ warps release the stage)
+        if (!C::kDqInDp && j > 0) mma_commit(bar(C::B_DOFREE + j % C::NQS));
+        return true;
+      };
+      auto issue_dV = [&](int j) -> bool {
+        if (!mbar_wait(bar(C::B_PREADY), j & 1, ab)) return false;
+        // dO_j may not have landed yet: from block 1 on, dV(j) comes before dP(j)
+        if (!mbar_wait(bar(C::B_DOFULL + j % C::NQS), (j / C::NQS) & 1, ab)) return false;
         tc_fence_after();
-        const uint64_t dDSi = opaque_u64(sdesc_add(dDSmn, (i % C::NDS) * C::DS_BUF));
+        issue_acc(tmem + C::T_S, sdesc_add(dOmn, (j % C::NQS) * C::Q_TILE), tmem + C::T_DV,
+                  j == 0);
+        if (!C::kDqInDp && j == 0) mma_commit(bar(C::B_DOFREE));
+        return true;
+      };
+      auto issue_dK = [&](int j) -> bool {
+        if (!mbar_wait(bar(C::B_DSREADY), j & 1, ab)) return false;
+        tc_fence_after();
+        issue_acc(tmem + C::T_DP, sdesc_add(dQmn, (j % C::NQS) * C::Q_TILE), tmem + C::T_DK,
+                  j == 0);
+        mma_commit(bar(C::B_QFREE + j % C::NQS));
+        return true;
+      };
+      auto issue_dQ = [&](int j) -> bool {
+        // D = 64: dQ has columns of its own; wait until dQ(j-1) has been read out
+        if (!C::kDqInDp && j > 0 && !mbar_wait(bar(C::B_DQEMPTY), (j - 1) & 1, ab)) return false;
+        tc_fence_after();
+        const uint64_t dDS = opaque_u64(dDSmn);
         const uint64_t dKq = opaque_u64(dKmn);
 #pragma unroll
         for (int kk = 0; kk < C::BN / 16; ++kk) {
-          if (DP == 128) {
+          if (C::kDqInDp) {
             // dQ^T [d][q] = K^T [d][key] * dS^T [key][q]
-            mma_ss(tmem + C::T_DQ, sdesc_add(dKq, kk * 2048), sdesc_add(dDSi, kk * 2048), idDQ,
+            mma_ss(tmem + C::T_DQ, sdesc_add(dKq, kk * 2048), sdesc_add(dDS, kk * 2048), idDQ,
                    kk > 0 ? 1u : 0u);
           } else {
             // dQ [q][d] = dS [q][key] * K [key][d]
-            mma_ss(tmem + C::T_DQ, sdesc_add(dDSi, kk * 2048), sdesc_add(dKq, kk * 2048), idDQ,
+            mma_ss(tmem + C::T_DQ, sdesc_add(dDS, kk * 2048), sdesc_add(dKq, kk * 2048), idDQ,
                    kk > 0 ? 1u : 0u);
           }
         }
         mma_commit(bar(C::B_DQFULL));
-        mma_commit(bar(C::B_DSMFREE + i % C::NDS));
-        if (C::ND == 1 && i + 1 < n && !(ok = issue_dP(i + 1))) break;
+        mma_commit(bar(C::B_DSMFREE));
+        return true;
+      };
+      if (ok && n > 0) {
+        ok = issue_S(0) && issue_dP(0) && issue_dV(0);
+        if (ok && n > 1) ok = issue_S(1);
+      }
+      for (int i = 0; ok && i < n; ++i) {
+        if (!(ok = issue_dK(i))) break;
+        if (!(ok = issue_dQ(i))) break;
+        if (i + 1 < n) {
+          if (!(ok = issue_dV(i + 1))) break;
+          // D = 128: dP^T's columns hold dQ(i) until the dQ warps have read it
+          if (C::kDqInDp && !(ok = mbar_wait(bar(C::B_DQEMPTY), i & 1, ab))) break;
+          if (!(ok = issue_dP(i + 1))) break;
+          if (i + 2 < n && !(ok = issue_S(i + 2))) break;
+        }
       }
       mma_commit(bar(C::B_ACCDONE));
       mma_commit(bar(C::B_DRAIN));
       drain_wait(bar(C::B_DRAIN), 0, 2000000000ull);
     }
   } else if (warp < 4) {
-    // ------------------------------------------------------------ dQ epilogue
+    // ------------------------------------------------------------ dQ read-out
     const int t = threadIdx.x;  // TMEM lane: d (D = 128) or query row (D = 64)
     const uint32_t lane_off = static_cast<uint32_t>(32 * warp) << 16;
-    const uint32_t stage = sbase + C::OFF_DQ;
-    for (int i = 0; i < n; ++i) {
-      if (!mbar_wait_warp(bar(C::B_DQFULL), i & 1, ab)) break;
-      tc_fence_after();
-      uint32_t r[64];
-      {
-        uint32_t a[32], b2[32];
-        tmem_ld32(tmem + lane_off + C::T_DQ, a);
-        tmem_ld32(tmem + lane_off + C::T_DQ + 32, b2);
-        tmem_wait_ld();
+    if (C::kDqInDp) {
+      // thread t = d: dQ^T[d][q] for the block's 128 query rows, in two halves
+      // of 64 rows; warp w stages and reduces box w (d = 32w .. 32w+31)
+      for (int j = 0; j < n; ++j) {
+        if (!mbar_wait_warp(bar(C::B_DQFULL), j & 1, ab)) break;
+        tc_fence_after();
+        const int q0 = (qb0 + j) * C::BQ;
+        const uint32_t stage = sbase + C::OFF_DO + (j % C::NQS) * C::Q_TILE;
 #pragma unroll
-        for (int e = 0; e < 32; ++e) {
-          r[e] = a[e];
-          r[32 + e] = b2[e];
+        for (int h = 0; h < 2; ++h) {
+          uint32_t r[64];
+          tmem_ld32(tmem + lane_off + C::T_DQ + 64 * h, *reinterpret_cast<uint32_t(*)[32]>(r));
+          tmem_ld32(tmem + lane_off + C::T_DQ + 64 * h + 32,
+                    *reinterpret_cast<uint32_t(*)[32]>(r + 32));
+          tmem_wait_ld();
+          if (h == 1) {
+            // dQ^T's columns are read out: dP of the next block may overwrite them
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(bar(C::B_DQEMPTY));
+            // the first half's reduction must have read the tile before it is reused
+            if (lane == 0) bulk_wait_group_read0();
+            __syncwarp();
+          }
+#pragma unroll
+          for (int q = 0; q < 64; ++q)
+            st_shared_f32(stage + dq_stage_off(q, t, C::DQ_BOX), __uint_as_float(r[q]) * scale);
+          fence_proxy_async_smem();
+          __syncwarp();
+          if (lane == 0) {
+            tma_reduce_add_3d(&tmdQ, stage + warp * C::DQ_BOX, 32 * warp, q0 + 64 * h, bh);
+            bulk_commit_group();
+          }
         }
+        // the stage is the dO producer's again once both reductions have read it
+        if (lane == 0) {
+          bulk_wait_group_read0();
+          mbar_arrive(bar(C::B_DOFREE + j % C::NQS));
+        }
+        __syncwarp();
       }
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(bar(C::B_DQEMPTY));
-      // The previous reduction must have finished reading the staging tile.
-      if (t == 0) bulk_wait_group_read0();
-      __syncwarp();  // bar.sync is aligned: the whole warp arrives together
-      named_bar_sync(1, 128);
-      if (DP == 128) {
-        // thread = d; r[q] = dQ^T[d][q]
+      if (lane == 0) bulk_wait_group0();
+    } else {
+      // thread t = query row: dQ[q][d], staged in smem and added by TMA. Each
+      // warp stages and reduces its own 32 rows (a 32-row slab of the tile), so
+      // the four warps never wait on one another.
+      const uint32_t stage = sbase + C::OFF_DQ;
+      for (int j = 0; j < n; ++j) {
+        if (!mbar_wait_warp(bar(C::B_DQFULL), j & 1, ab)) break;
+        tc_fence_after();
+        uint32_t r[DP];
 #pragma unroll
-        for (int q = 0; q < 64; ++q)
-          st_shared_f32(stage + dq_stage_off(q, t, C::DQ_BOX), __uint_as_float(r[q]) * scale);
-      } else {
-        // thread = query row; r[d] = dQ[q][d]
+        for (int c = 0; c < DP / 32; ++c)
+          tmem_ld32(tmem + lane_off + C::T_DQ + 32 * c,
+                    *reinterpret_cast<uint32_t(*)[32]>(r + 32 * c));
+        tmem_wait_ld();
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(bar(C::B_DQEMPTY));
+        // This warp's previous reduction must have finished reading its slab.
+        if (lane == 0) bulk_wait_group_read0();
+        __syncwarp();
 #pragma unroll
-        for (int u = 0; u < 16; ++u) {
+        for (int u = 0; u < DP / 4; ++u) {
           const uint32_t off = dq_stage_off(t, 4 * u, C::DQ_BOX);
           st_shared_v4(stage + off, __float_as_uint(__uint_as_float(r[4 * u]) * scale),
                        __float_as_uint(__uint_as_float(r[4 * u + 1]) * scale),
                        __float_as_uint(__uint_as_float(r[4 * u + 2]) * scale),
                        __float_as_uint(__uint_as_float(r[4 * u + 3]) * scale));
         }
+        fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0) {
+          const int q0 = (qb0 + j) * C::BQ + 32 * warp;
+          for (int bx = 0; bx < (D + 31) / 32; ++bx)
+            tma_reduce_add_3d(&tmdQ, stage + bx * C::DQ_BOX + 32 * warp * 128, bx * 32, q0, bh);
+          bulk_commit_group();
+        }
       }
-      fence_proxy_async_smem();
-      named_bar_sync(1, 128);
-      if (t == 0) {
-        const int q0 = (qb0 + i) * C::BQ;
-        for (int bx = 0; bx < (D + 31) / 32; ++bx)
-          tma_reduce_add_3d(&tmdQ, stage + bx * C::DQ_BOX, bx * 32, q0, bh);
-        bulk_commit_group();
-      }
+      if (lane == 0) bulk_wait_group0();
     }
-    if (t == 0) bulk_wait_group0();
   } else if (warp >= 8) {
     // ------------------------------------------------------------ softmax warpgroups
     const int g = (warp - 8) >> 2;
@@ -395,12 +495,11 @@ __global__ void __launch_bounds__(512, 1)
     // smallest query index that may see this thread's key (past Lk: none may)
     const int qmin = kg >= Lk ? INT_MAX : (causal ? kg - off : INT_MIN);
     bool ok = true;
-    for (int i = 0; i < n; ++i) {
-      const int st = i % C::NQS;
-      const int db = C::ND == 2 ? (i & 1) : 0;
-      const int q0 = (qb0 + i) * C::BQ;
-      if (!(ok = mbar_wait_warp(bar(C::B_QFULL + st), (i / C::NQS) & 1, ab))) break;
-      if (!(ok = mbar_wait_warp(bar(C::B_SFULL), i & 1, ab))) break;
+    for (int j = 0; j < n; ++j) {
+      const int st = j % C::NQS;
+      const int q0 = (qb0 + j) * C::BQ;
+      if (!(ok = mbar_wait_warp(bar(C::B_QFULL + st), (j / C::NQS) & 1, ab))) break;
+      if (!(ok = mbar_wait_warp(bar(C::B_SFULL), j & 1, ab))) break;
       tc_fence_after();
       // query column e of this warpgroup's slice is masked iff e < lim0 (e is q - q0 - g QPW)
       const int lim0 = qmin == INT_MIN ? INT_MIN
@@ -409,68 +508,61 @@ __global__ void __launch_bounds__(512, 1)
       const float *lse = sLse + st * C::BQ + g * C::QPW;
       const float *dvq = sDv + st * C::BQ + g * C::QPW;
       const uint32_t tS = tmem + lane_off + C::T_S + g * C::QPW;
-      const uint32_t tDP = tmem + lane_off + C::T_DP + db * C::BQ + g * C::QPW;
+      const uint32_t tDP = tmem + lane_off + C::T_DP + g * C::QPW;
+      // P^T: all 64 scores of this thread's slice in flight, one wait
       float p[C::QPW];
-#pragma unroll
-      for (int c = 0; c < C::QPW / 32; ++c) {
-        uint32_t r[32];
-        tmem_ld32(tS + 32 * c, r);
+      {
+        uint32_t r[C::QPW];
+        tmem_ld32(tS, *reinterpret_cast<uint32_t(*)[32]>(r));
+        tmem_ld32(tS + 32, *reinterpret_cast<uint32_t(*)[32]>(r + 32));
         tmem_wait_ld();
-        float lv[32];
 #pragma unroll
-        for (int e = 0; e < 32; e += 4) {
-          const float4 v4 = *reinterpret_cast<const float4 *>(lse + 32 * c + e);
-          lv[e] = v4.x; lv[e + 1] = v4.y; lv[e + 2] = v4.z; lv[e + 3] = v4.w;
-        }
+        for (int e = 0; e < C::QPW; e += 4) {
+          const float4 l4 = *reinterpret_cast<const float4 *>(lse + e);
+          const float lv[4] = {l4.x, l4.y, l4.z, l4.w};
 #pragma unroll
-        for (int e = 0; e < 32; ++e) {
-          float x = ex2(fmaf(__uint_as_float(r[e]), scale_log2, -lv[e]));
-          if (need_mask && 32 * c + e < lim0) x = 0.f;
-          p[32 * c + e] = x;
+          for (int u = 0; u < 4; ++u) {
+            float x = ex2(fmaf(__uint_as_float(r[e + u]), scale_log2, -lv[u]));
+            if (need_mask && e + u < lim0) x = 0.f;
+            p[e + u] = x;
+          }
         }
       }
+      {
+        uint32_t pk[C::QPW / 2];
 #pragma unroll
-      for (int c = 0; c < C::QPW / 32; ++c) {
-        uint32_t pk[16];
-#pragma unroll
-        for (int e = 0; e < 16; ++e) pk[e] = pack_bf16(p[32 * c + 2 * e], p[32 * c + 2 * e + 1]);
-        tmem_st16(tS + 16 * c, pk);
+        for (int e = 0; e < C::QPW / 2; ++e) pk[e] = pack_bf16(p[2 * e], p[2 * e + 1]);
+        tmem_st32(tS, pk);
       }
       tmem_wait_st();
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(bar(C::B_PREADY));
 
-      if (!(ok = mbar_wait_warp(bar(C::B_DPFULL + db), (C::ND == 2 ? (i >> 1) : i) & 1, ab)))
-        break;
-      // this dS staging tile is free once dQ(i - NDS) has completed
-      if (i >= C::NDS &&
-          !(ok = mbar_wait_warp(bar(C::B_DSMFREE + i % C::NDS), ((i / C::NDS) - 1) & 1, ab)))
-        break;
+      if (!(ok = mbar_wait_warp(bar(C::B_DPFULL), j & 1, ab))) break;
+      // the dS^T staging tile is free once dQ(j - 1) has completed
+      if (j > 0 && !(ok = mbar_wait_warp(bar(C::B_DSMFREE), (j - 1) & 1, ab))) break;
       tc_fence_after();
-      const uint32_t sDSi = sDS + (i % C::NDS) * C::DS_BUF;
 #pragma unroll
       for (int c = 0; c < C::QPW / 32; ++c) {
         uint32_t r[32];
         tmem_ld32(tDP + 32 * c, r);
         tmem_wait_ld();
-        float dv[32];
-#pragma unroll
-        for (int e = 0; e < 32; e += 4) {
-          const float4 v4 = *reinterpret_cast<const float4 *>(dvq + 32 * c + e);
-          dv[e] = v4.x; dv[e + 1] = v4.y; dv[e + 2] = v4.z; dv[e + 3] = v4.w;
-        }
         uint32_t pk[16];
 #pragma unroll
-        for (int e = 0; e < 16; ++e) {
-          const float d0 = p[32 * c + 2 * e] * (__uint_as_float(r[2 * e]) - dv[2 * e]);
-          const float d1 = p[32 * c + 2 * e + 1] * (__uint_as_float(r[2 * e + 1]) - dv[2 * e + 1]);
-          pk[e] = pack_bf16(d0, d1);
+        for (int e = 0; e < 16; e += 2) {
+          const float4 d4 = *reinterpret_cast<const float4 *>(dvq + 32 * c + 2 * e);
+          const float a0 = p[32 * c + 2 * e] * (__uint_as_float(r[2 * e]) - d4.x);
+          const float a1 = p[32 * c + 2 * e + 1] * (__uint_as_float(r[2 * e + 1]) - d4.y);
+          const float a2 = p[32 * c + 2 * e + 2] * (__uint_as_float(r[2 * e + 2]) - d4.z);
+          const float a3 = p[32 * c + 2 * e + 3] * (__uint_as_float(r[2 * e + 3]) - d4.w);
+          pk[e] = pack_bf16(a0, a1);
+          pk[e + 1] = pack_bf16(a2, a3);
         }
         tmem_st16(tDP + 16 * c, pk);
         // dS^T row kr, queries ql .. ql+31 into the swizzled smem tile
         const int ql = g * C::QPW + 32 * c;
-        const uint32_t chunk = sDSi + (ql >> 6) * C::DS_CHUNK + kr * 128;
+        const uint32_t chunk = sDS + (ql >> 6) * C::DS_CHUNK + kr * 128;
 #pragma unroll
         for (int u4 = 0; u4 < 4; ++u4) {
           const int unit = ((ql & 63) >> 3) + u4;
@@ -483,15 +575,15 @@ __global__ void __launch_bounds__(512, 1)
       tc_fence_before();
       __syncwarp();
       if (lane == 0) {
-        mbar_arrive(bar(C::B_DSREADY + (i & 1)));
-        mbar_arrive(bar(C::B_QEMPTY + st));
+        mbar_arrive(bar(C::B_DSREADY));
+        mbar_arrive(bar(C::B_QFREE + st));
       }
     }
     // dK (scaled) and dV of this key block
     if (ok && n > 0) ok = mbar_wait_warp(bar(C::B_ACCDONE), 0, ab);
-    if (ok && n == 0 && kg < Lk) {
-      // no query sees this key block: dK = dV = 0 (warpgroup w writes its half)
-      const size_t row = (static_cast<size_t>(bh) * Lk + kg) * D;
+    if (ok && n == 0 && kg < Lk_rows) {
+      // no query sees this key block: dK = dV = 0 (warpgroup g writes its half)
+      const size_t row = (static_cast<size_t>(bh) * Lk_rows + kg) * D;
       for (int c = 0; c < DP / 2 && g * (DP / 2) + c < D; c += 4) {
         *reinterpret_cast<float4 *>(dV + row + g * (DP / 2) + c) = make_float4(0.f, 0.f, 0.f, 0.f);
         *reinterpret_cast<float4 *>(dK + row + g * (DP / 2) + c) = make_float4(0.f, 0.f, 0.f, 0.f);
@@ -499,8 +591,8 @@ __global__ void __launch_bounds__(512, 1)
     }
     if (ok && n > 0) {
       tc_fence_after();
-      const bool valid = kg < Lk;
-      const size_t row = (static_cast<size_t>(bh) * Lk + (valid ? kg : 0)) * D;
+      const bool valid = kg < Lk_rows;
+      const size_t row = (static_cast<size_t>(bh) * Lk_rows + (valid ? kg : 0)) * D;
 #pragma unroll
       for (int c = 0; c < DP / 64; ++c) {
         const int col = g * (DP / 2) + 32 * c;
@@ -547,7 +639,9 @@ cudaError_t launch(const __nv_bfloat16 *Q, const __nv_bfloat16 *K, const __nv_bf
   if ((e = mg_tmap_bf16(&tdo, dO, p.D, p.L, BH, C::BQ)) != cudaSuccess) return e;
   if ((e = mg_tmap_bf16(&tk, K, p.D, p.Lk, BH, C::BN)) != cudaSuccess) return e;
   if ((e = mg_tmap_bf16(&tv, V, p.D, p.Lk, BH, C::BN)) != cudaSuccess) return e;
-  if ((e = mg_tmap_f32(&tdq, dQ, p.D, p.L, BH, C::BQ)) != cudaSuccess) return e;
+  // dQ add-reductions: D = 64 in 32-row slabs (one per read-out warp), D = 128
+  // in [64 rows][32 columns] boxes (one per warp and half block)
+  if ((e = mg_tmap_f32(&tdq, dQ, p.D, p.L, BH, C::DQ_TMA_ROWS)) != cudaSuccess) return e;
   auto kern = accel_dkdv_kernel<DP>;
   if ((e = mg_set_smem_attr(reinterpret_cast<const void *>(kern), C::SMEM_BYTES,
                             DP == 64 ? 8 : 9)) != cudaSuccess)
@@ -556,7 +650,7 @@ cudaError_t launch(const __nv_bfloat16 *Q, const __nv_bfloat16 *K, const __nv_bf
   const long long grid = static_cast<long long>(nkb) * BH;
   kern<<<static_cast<unsigned>(grid), C::NTHREADS, C::SMEM_BYTES, st>>>(
       tq, tk, tv, tdo, tdq, LSE, Dvec, dQ, dK, dV, BH, p.L, p.Lk, p.D, p.causal, p.off, p.scale,
-      p.scale * kLog2e, err, mg_wait_limit_ns());
+      p.scale * kLog2e, err, mg_wait_limit_ns(), p.kv_len, p.H, p.br);
   return cudaGetLastError();
 }
 

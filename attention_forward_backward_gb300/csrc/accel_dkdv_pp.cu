@@ -89,9 +89,10 @@ __global__ void __launch_bounds__(320, 1)
                          const __grid_constant__ CUtensorMap tmV,
                          const __grid_constant__ CUtensorMap tmdO, const float *__restrict__ LSE,
                          const float *__restrict__ Dvec, float *__restrict__ dK,
-                         float *__restrict__ dV, int BH, int L, int Lk, int D, int causal,
-                         int off, float scale,
-                         float scale_log2, unsigned int *err, unsigned long long timeout_ns) {
+                         float *__restrict__ dV, int BH, int L, int Lk_rows, int D, int causal,
+                         int off0, float scale, float scale_log2, unsigned int *err,
+                         unsigned long long timeout_ns, const int *__restrict__ kv_len, int H,
+                         int br) {
   using C = PPCfg<DP>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
@@ -107,14 +108,18 @@ __global__ void __launch_bounds__(320, 1)
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   // Head-major order: CTAs that run together share a few heads' Q/dO in L2;
   // within a head the heaviest causal key block (kb = 0) goes first.
-  // L query rows, Lk key rows; causal: query i sees key j iff j <= i + off
-  const int nkb = (Lk + C::BN - 1) / C::BN;
+  // L query rows, Lk_rows key rows of which this head attends to Lk (all, or
+  // the batch element's padded length); causal: query i sees key j iff
+  // j <= i + off
+  const int nkb = (Lk_rows + C::BN - 1) / C::BN;
   const int bh = static_cast<int>(blockIdx.x / nkb);
   const int kb = static_cast<int>(blockIdx.x % nkb);
   const int k0 = kb * C::BN;
+  const MgKeys keys = mg_keys(kv_len, bh, H, L, Lk_rows, off0, br);
+  const int Lk = keys.len, off = keys.off;
   const int nqb = (L + C::BQ - 1) / C::BQ;
   const int qb0 = causal ? max(0, k0 - off) / C::BQ : 0;  // first block with a query seeing k0
-  const int n = max(0, nqb - qb0);
+  const int n = k0 >= Lk ? 0 : max(0, nqb - qb0);
 
   if (warp == 0) {
     tmem_alloc(smem_u32(tmem_slot), C::TMEM_COLS);
@@ -336,9 +341,9 @@ __global__ void __launch_bounds__(320, 1)
     }
     // dK (scaled) and dV of this key block: warpgroup w stores half the columns
     if (ok && n > 0) ok = mbar_wait_warp(bar(C::B_ACCDONE), 0, ab);
-    if (ok && n == 0 && kg < Lk) {
+    if (ok && n == 0 && kg < Lk_rows) {
       // no query sees this key block: dK = dV = 0 (warpgroup w writes its half)
-      const size_t row = (static_cast<size_t>(bh) * Lk + kg) * D;
+      const size_t row = (static_cast<size_t>(bh) * Lk_rows + kg) * D;
       for (int c = 0; c < DP / 2 && w * (DP / 2) + c < D; c += 4) {
         *reinterpret_cast<float4 *>(dV + row + w * (DP / 2) + c) = make_float4(0.f, 0.f, 0.f, 0.f);
         *reinterpret_cast<float4 *>(dK + row + w * (DP / 2) + c) = make_float4(0.f, 0.f, 0.f, 0.f);
@@ -346,8 +351,8 @@ __global__ void __launch_bounds__(320, 1)
     }
     if (ok && n > 0) {
       tc_fence_after();
-      const bool valid = kg < Lk;
-      const size_t row = (static_cast<size_t>(bh) * Lk + (valid ? kg : 0)) * D;
+      const bool valid = kg < Lk_rows;
+      const size_t row = (static_cast<size_t>(bh) * Lk_rows + (valid ? kg : 0)) * D;
 #pragma unroll
       for (int c = 0; c < DP / 64; ++c) {
         const int col = w * (DP / 2) + 32 * c;
@@ -401,8 +406,7 @@ cudaError_t launch(const __nv_bfloat16 *Q, const __nv_bfloat16 *K, const __nv_bf
   const long long grid = static_cast<long long>(nkb) * BH;
   kern<<<static_cast<unsigned>(grid), C::NTHREADS, C::SMEM_BYTES, st>>>(
       tq, tk, tv, tdo, LSE, Dvec, dK, dV, BH, p.L, p.Lk, p.D, p.causal, p.off, p.scale,
-      p.scale * kLog2e, err,
-      mg_wait_limit_ns());
+      p.scale * kLog2e, err, mg_wait_limit_ns(), p.kv_len, p.H, p.br);
   return cudaGetLastError();
 }
 

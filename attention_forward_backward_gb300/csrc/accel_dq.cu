@@ -80,8 +80,9 @@ __global__ void __launch_bounds__(320, 1)
                     const __grid_constant__ CUtensorMap tmdO,
                     const __grid_constant__ CUtensorMap tmK,
                     const __grid_constant__ CUtensorMap tmV, const float *__restrict__ LSE,
-                    const float *__restrict__ Dvec, float *__restrict__ dQ, int BH, int L, int Lk,
-                    int D, int causal, int off, float scale, float scale_log2, unsigned int *err,
+                    const float *__restrict__ Dvec, float *__restrict__ dQ, int BH, int L,
+                    int Lk_rows, int D, int causal, int off0, float scale, float scale_log2,
+                    const int *__restrict__ kv_len, int H, int br, unsigned int *err,
                     unsigned long long timeout_ns) {
   using C = DqCfg<DP>;
   extern __shared__ uint8_t smem_raw[];
@@ -99,7 +100,10 @@ __global__ void __launch_bounds__(320, 1)
   const int qb = nqb - 1 - static_cast<int>(blockIdx.x / BH);
   const int bh = static_cast<int>(blockIdx.x % BH);
   const int q0 = qb * C::BM;
-  // Lk key rows; causal: query i sees key j iff j <= i + off
+  // Lk key rows (all Lk_rows rows, or the batch element's padded length);
+  // causal: query i sees key j iff j <= i + off
+  const MgKeys keys = mg_keys(kv_len, bh, H, L, Lk_rows, off0, br);
+  const int Lk = keys.len, off = keys.off;
   const int nkt_all = (Lk + C::BN - 1) / C::BN;
   const int last = min(q0 + C::BM, L) - 1 + off;  // last key any row of the block sees
   const int n = !causal ? nkt_all : (last < 0 ? 0 : min(nkt_all, last / C::BN + 1));
@@ -336,8 +340,7 @@ cudaError_t launch(const __nv_bfloat16 *Q, const __nv_bfloat16 *K, const __nv_bf
   const long long grid = static_cast<long long>(nqb) * BH;
   kern<<<static_cast<unsigned>(grid), C::NTHREADS, C::SMEM_BYTES, st>>>(
       tq, tdo, tk, tv, LSE, Dvec, dQ, BH, p.L, p.Lk, p.D, p.causal, p.off, p.scale,
-      p.scale * kLog2e, err,
-      mg_wait_limit_ns());
+      p.scale * kLog2e, p.kv_len, p.H, p.br, err, mg_wait_limit_ns());
   return cudaGetLastError();
 }
 

@@ -25,6 +25,8 @@
 // error word and the CTA leaves through the same teardown as a normal exit.
 #include <string.h>
 
+#include <algorithm>
+
 #include "internal.h"
 #include "tc_common.cuh"
 #include "tmap.h"
@@ -82,9 +84,9 @@ __global__ void __launch_bounds__(320, 1)
     accel_fwd_kernel(const __grid_constant__ CUtensorMap tmQ,
                      const __grid_constant__ CUtensorMap tmK,
                      const __grid_constant__ CUtensorMap tmV, float *__restrict__ O,
-                     float *__restrict__ LSE, int BH, int L, int Lk, int D, int causal, int off,
-                     float scale_log2, unsigned int *err, unsigned long long timeout_ns,
-                     int fault) {
+                     float *__restrict__ LSE, int BH, int L, int Lk_rows, int D, int causal,
+                     int off0, float scale_log2, unsigned int *err, unsigned long long timeout_ns,
+                     int fault, int G, const int *__restrict__ kv_len, int H, int br) {
   using C = FwdCfg<DP>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
@@ -96,12 +98,23 @@ __global__ void __launch_bounds__(320, 1)
   volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + C::OFF_MISC + 4);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  // Heaviest causal query blocks (largest qb) of every head go first.
+  // Heads run in groups of G whose K and V fit in L2 together: all query blocks
+  // of a group's heads are scheduled before the next group, so every key tile
+  // of a head is read from HBM about once. Within a group the heaviest causal
+  // query blocks (largest qb) go first, heads alternating.
   const int nqb = (L + 255) / 256;
-  const int qb = nqb - 1 - static_cast<int>(blockIdx.x / BH);
-  const int bh = static_cast<int>(blockIdx.x % BH);
+  const long long per_group = static_cast<long long>(G) * nqb;
+  const int grp = static_cast<int>(blockIdx.x / per_group);
+  const int r_in = static_cast<int>(blockIdx.x - grp * per_group);
+  const int h0 = grp * G;
+  const int Gg = min(G, BH - h0);  // the last group may hold fewer heads
+  const int qb = nqb - 1 - r_in / Gg;
+  const int bh = h0 + r_in % Gg;
   const int q0 = qb * 256;
-  // key tiles of each query tile: Lk keys; causal: query i sees key j iff j <= i + off
+  // this head's keys: Lk (all rows, or the batch element's padded length);
+  // causal: query i sees key j iff j <= i + off
+  const MgKeys keys = mg_keys(kv_len, bh, H, L, Lk_rows, off0, br);
+  const int Lk = keys.len, off = keys.off;
   const int nkt = (Lk + C::BN - 1) / C::BN;
   int nT[2];
   for (int q = 0; q < 2; ++q) {
@@ -379,9 +392,12 @@ cudaError_t launch(const __nv_bfloat16 *Q, const __nv_bfloat16 *K, const __nv_bf
     return e;
   const int nqb = (p.L + 255) / 256;
   const long long grid = static_cast<long long>(nqb) * BH;
+  // heads per group: K and V of a group (bf16) within 32 MB of the 129 MB L2
+  const long long kv_head = 2LL * p.Lk * p.D * 2;
+  const int G = static_cast<int>(std::max(1LL, std::min<long long>(BH, (32LL << 20) / kv_head)));
   kern<<<static_cast<unsigned>(grid), C::NTHREADS, C::SMEM_BYTES, st>>>(
       tq, tk, tv, O, LSE, BH, p.L, p.Lk, p.D, p.causal, p.off, p.scale * kLog2e, err,
-      mg_wait_limit_ns(), fault_mode());
+      mg_wait_limit_ns(), fault_mode(), G, p.kv_len, p.H, p.br);
   return cudaGetLastError();
 }
 

@@ -117,10 +117,20 @@ int check_common(int B, int H, int Lq, int Lk, int D, int mask, float scale, int
   return MG_OK;
 }
 
-MgProblem make_problem(int B, int H, int Lq, int Lk, int D, int mask, float scale) {
+MgProblem make_problem(int B, int H, int Lq, int Lk, int D, int mask, float scale,
+                       const int *kv_len = nullptr) {
   MgProblem p{B, H, Lq, D, mask != MG_MASK_NONE ? 1 : 0, scale, Lk, 0};
   if (mask == MG_MASK_CAUSAL_BOTTOM_RIGHT) p.off = Lk - Lq;
+  p.kv_len = kv_len;
+  p.br = mask == MG_MASK_CAUSAL_BOTTOM_RIGHT ? 1 : 0;
   return p;
+}
+
+// kv_len (device array of B int32, may be null) must be 4-byte aligned and must
+// not overlap any output.
+int check_kv_len(const int *kv_len) {
+  return (kv_len && (reinterpret_cast<uintptr_t>(kv_len) & 3u) != 0) ? MG_ERR_INVALID_ARG
+                                                                     : MG_OK;
 }
 
 int check_ptrs(const void *const *ptrs, int n) {
@@ -213,21 +223,23 @@ const char *mg_status_string(int status) {
   }
 }
 
-int mg_attn_fwd_ex(const void *Q, const void *K, const void *V, void *O, float *LSE, int B,
-                   int H, int Lq, int Lk, int D, int mask, float scale, int contract,
-                   void *stream) {
+int mg_attn_fwd_padded(const void *Q, const void *K, const void *V, void *O, float *LSE,
+                       const int *kv_len, int B, int H, int Lq, int Lk, int D, int mask,
+                       float scale, int contract, void *stream) {
   int rc = check_common(B, H, Lq, Lk, D, mask, scale, contract);
   if (rc) return rc;
   const void *ptrs[] = {Q, K, V, O, LSE};
   if ((rc = check_ptrs(ptrs, 5))) return rc;
+  if ((rc = check_kv_len(kv_len))) return rc;
   const size_t nq = static_cast<size_t>(B) * H * Lq * D;
   const size_t nk = static_cast<size_t>(B) * H * Lk * D;
   const size_t in_el = contract == MG_CONTRACT_STRICT_F32 ? 4 : 2;
-  const Range in[] = {rng(Q, nq * in_el), rng(K, nk * in_el), rng(V, nk * in_el)};
+  const Range in[] = {rng(Q, nq * in_el), rng(K, nk * in_el), rng(V, nk * in_el),
+                      rng(kv_len, kv_len ? static_cast<size_t>(B) * 4 : 0)};
   const Range out[] = {rng(O, nq * 4), rng(LSE, static_cast<size_t>(B) * H * Lq * 4)};
-  if ((rc = check_alias(in, 3, out, 2))) return rc;
+  if ((rc = check_alias(in, 4, out, 2))) return rc;
 
-  const MgProblem p = make_problem(B, H, Lq, Lk, D, mask, scale);
+  const MgProblem p = make_problem(B, H, Lq, Lk, D, mask, scale, kv_len);
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   cudaError_t e;
   if (contract == MG_CONTRACT_STRICT_F32) {
@@ -244,6 +256,13 @@ int mg_attn_fwd_ex(const void *Q, const void *K, const void *V, void *O, float *
                             p, err, st);
   }
   return map_cuda(e);
+}
+
+int mg_attn_fwd_ex(const void *Q, const void *K, const void *V, void *O, float *LSE, int B,
+                   int H, int Lq, int Lk, int D, int mask, float scale, int contract,
+                   void *stream) {
+  return mg_attn_fwd_padded(Q, K, V, O, LSE, nullptr, B, H, Lq, Lk, D, mask, scale, contract,
+                            stream);
 }
 
 int mg_attn_fwd(const void *Q, const void *K, const void *V, void *O, float *LSE, int B, int H,
@@ -308,10 +327,20 @@ int mg_attn_bwd_ex(const void *Q, const void *K, const void *V, const void *O, c
                    const float *LSE, void *dQ, void *dK, void *dV, int B, int H, int Lq, int Lk,
                    int D, int mask, float scale, int contract, void *workspace,
                    size_t workspace_bytes, void *stream) {
+  return mg_attn_bwd_padded(Q, K, V, O, dO, LSE, dQ, dK, dV, nullptr, B, H, Lq, Lk, D, mask,
+                            scale, contract, workspace, workspace_bytes, stream);
+}
+
+int mg_attn_bwd_padded(const void *Q, const void *K, const void *V, const void *O,
+                       const void *dO, const float *LSE, void *dQ, void *dK, void *dV,
+                       const int *kv_len, int B, int H, int Lq, int Lk, int D, int mask,
+                       float scale, int contract, void *workspace, size_t workspace_bytes,
+                       void *stream) {
   int rc = check_common(B, H, Lq, Lk, D, mask, scale, contract);
   if (rc) return rc;
   const void *ptrs[] = {Q, K, V, O, dO, LSE, dQ, dK, dV};
   if ((rc = check_ptrs(ptrs, 9))) return rc;
+  if ((rc = check_kv_len(kv_len))) return rc;
   if (!workspace || !aligned16(workspace) || workspace_bytes < ws_bytes(B, H, Lq))
     return MG_ERR_WORKSPACE;
   const size_t n = static_cast<size_t>(B) * H * Lq * D;   // Q, O, dO, dQ
@@ -319,12 +348,13 @@ int mg_attn_bwd_ex(const void *Q, const void *K, const void *V, const void *O, c
   const size_t rows = static_cast<size_t>(B) * H * Lq;
   const size_t in_el = contract == MG_CONTRACT_STRICT_F32 ? 4 : 2;
   const Range in[] = {rng(Q, n * in_el), rng(K, nk * in_el), rng(V, nk * in_el),
-                      rng(dO, n * in_el), rng(O, n * 4),      rng(LSE, rows * 4)};
+                      rng(dO, n * in_el), rng(O, n * 4),      rng(LSE, rows * 4),
+                      rng(kv_len, kv_len ? static_cast<size_t>(B) * 4 : 0)};
   const Range out[] = {rng(dQ, n * 4), rng(dK, nk * 4), rng(dV, nk * 4),
                        rng(workspace, ws_bytes(B, H, Lq))};
-  if ((rc = check_alias(in, 6, out, 4))) return rc;
+  if ((rc = check_alias(in, 7, out, 4))) return rc;
 
-  const MgProblem p = make_problem(B, H, Lq, Lk, D, mask, scale);
+  const MgProblem p = make_problem(B, H, Lq, Lk, D, mask, scale, kv_len);
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   float *Dvec = static_cast<float *>(workspace);
   cudaError_t e;

@@ -15,7 +15,30 @@ struct MgProblem {
   float scale;
   int Lk;
   int off;
+  // Per-batch key padding (device array of B lengths, or null): batch element
+  // b keeps only its first kv_len[b] key rows. br marks the bottom-right causal
+  // alignment, whose offset then follows the batch element's own key count.
+  const int *kv_len = nullptr;
+  int br = 0;
 };
+
+// Key rows that one head (bh = b * H + h) attends to, and its causal offset:
+// all Lk rows and `off` without padding; with padding the first kv_len[b] rows
+// (clamped into [0, Lk]) and, for the bottom-right alignment, the offset
+// kv_len[b] - Lq. Rows past the length are masked exactly like rows past Lk.
+struct MgKeys {
+  int len;
+  int off;
+};
+#ifdef __CUDACC__
+__device__ __forceinline__ MgKeys mg_keys(const int *kv_len, int bh, int H, int Lq, int Lk,
+                                          int off, int br) {
+  if (!kv_len) return MgKeys{Lk, off};
+  int n = __ldg(kv_len + bh / H);
+  n = n < 0 ? 0 : (n > Lk ? Lk : n);
+  return MgKeys{n, br ? n - Lq : off};
+}
+#endif
 
 // Kernel ids, in the order mg_attn_kernel_name() reports them.
 enum MgKernelId {

@@ -43,8 +43,8 @@ __global__ void __launch_bounds__(256, 1)
                        const float *__restrict__ V, const float *__restrict__ dO,
                        const float *__restrict__ LSE, const float *__restrict__ Dvec,
                        float *__restrict__ dQ, float *__restrict__ dK, float *__restrict__ dV,
-                       int BH, int L, int Lk, int causal, int off, float scale,
-                       float scale_log2) {
+                       int BH, int L, int Lk_rows, int causal, int off0, float scale,
+                       float scale_log2, const int *__restrict__ kv_len, int H, int br) {
   using C = BwdCfg<D>;
   using VecV = typename VecT<C::VW>::T;
   extern __shared__ float4 smem_f4[];
@@ -61,17 +61,21 @@ __global__ void __launch_bounds__(256, 1)
   const int kt = static_cast<int>(blockIdx.x / BH);  // heaviest (kt = 0) first
   const int bh = static_cast<int>(blockIdx.x % BH);
   const int k0 = kt * C::BC;
-  // query rows L, key rows Lk; causal: query i sees key j iff j <= i + off
+  // query rows L, key rows Lk (all Lk_rows rows, or the batch element's padded
+  // length; rows past it are never staged and get dK = dV = 0); causal: query
+  // i sees key j iff j <= i + off
+  const MgKeys keys = mg_keys(kv_len, bh, H, L, Lk_rows, off0, br);
+  const int Lk = keys.len, off = keys.off;
   const size_t head = static_cast<size_t>(bh) * L * D;
-  const size_t khead = static_cast<size_t>(bh) * Lk * D;
+  const size_t khead = static_cast<size_t>(bh) * Lk_rows * D;
   const float *Qh = Q + head, *Kh = K + khead, *Vh = V + khead, *dOh = dO + head;
   const float *Lh = LSE + static_cast<size_t>(bh) * L, *Dh = Dvec + static_cast<size_t>(bh) * L;
   float *dQh = dQ + head;
 
   const int tid = threadIdx.x, tx = tid & 15, ty = tid >> 4;
-  const int nqt = (L + C::BR - 1) / C::BR;
-  // first query tile holding a query that sees key k0 (none past nqt: the key
-  // block then keeps dK = dV = 0)
+  // query tiles holding a query that sees key k0 (none when the block starts
+  // past the key count or past the last tile: dK = dV = 0 then)
+  const int nqt = k0 >= Lk ? 0 : (L + C::BR - 1) / C::BR;
   const int qt0 = causal ? max(0, k0 - off) / C::BR : 0;
 
   stage_rows<D, 64, C::NT>(sK, C::RS, Kh, k0, Lk, tid);
@@ -245,7 +249,7 @@ __global__ void __launch_bounds__(256, 1)
 #pragma unroll
   for (int a = 0; a < 4; ++a) {
     const int kg = k0 + ty + 16 * a;
-    if (kg < Lk) {
+    if (kg < Lk_rows) {
       float *krow = dK + khead + static_cast<size_t>(kg) * D;
       float *vrow = dV + khead + static_cast<size_t>(kg) * D;
 #pragma unroll
@@ -312,7 +316,7 @@ cudaError_t launch_dkdv(const float *Q, const float *K, const float *V, const fl
   const long long grid = static_cast<long long>(nkt) * BH;
   kern<<<static_cast<unsigned>(grid), C::NT, C::SMEM_BYTES, st>>>(
       Q, K, V, dO, LSE, Dvec, dQ, dK, dV, BH, p.L, p.Lk, p.causal, p.off, p.scale,
-      p.scale * kLog2e);
+      p.scale * kLog2e, p.kv_len, p.H, p.br);
   return cudaGetLastError();
 }
 

@@ -40,8 +40,8 @@ template <int D>
 __global__ void __launch_bounds__(256, 1)
     strict_fwd_kernel(const float *__restrict__ Q, const float *__restrict__ K,
                       const float *__restrict__ V, float *__restrict__ O,
-                      float *__restrict__ LSE, int BH, int L, int Lk, int causal, int off,
-                      float scale_log2) {
+                      float *__restrict__ LSE, int BH, int L, int Lk_rows, int causal, int off0,
+                      float scale_log2, const int *__restrict__ kv_len, int H, int br) {
   using C = FwdCfg<D>;
   using VecV = typename VecT<C::VW>::T;
   extern __shared__ float4 smem_f4[];
@@ -55,9 +55,13 @@ __global__ void __launch_bounds__(256, 1)
   const int qt = nqt - 1 - static_cast<int>(blockIdx.x / BH);
   const int bh = static_cast<int>(blockIdx.x % BH);
   const int q0 = qt * C::BR;
-  // query rows L, key rows Lk; causal: query i sees key j iff j <= i + off
+  // query rows L, key rows Lk (all Lk_rows rows, or the batch element's padded
+  // length; rows past it are never staged); causal: query i sees key j iff
+  // j <= i + off
+  const MgKeys keys = mg_keys(kv_len, bh, H, L, Lk_rows, off0, br);
+  const int Lk = keys.len, off = keys.off;
   const size_t head = static_cast<size_t>(bh) * L * D;
-  const size_t khead = static_cast<size_t>(bh) * Lk * D;
+  const size_t khead = static_cast<size_t>(bh) * Lk_rows * D;
   const float *Qh = Q + head, *Kh = K + khead, *Vh = V + khead;
 
   const int tid = threadIdx.x, tx = tid & 15, ty = tid >> 4;
@@ -230,7 +234,7 @@ cudaError_t launch(const float *Q, const float *K, const float *V, float *O, flo
   const int nqt = (p.L + C::BR - 1) / C::BR;
   const long long grid = static_cast<long long>(nqt) * BH;
   kern<<<static_cast<unsigned>(grid), C::NT, C::SMEM_BYTES, st>>>(
-      Q, K, V, O, LSE, BH, p.L, p.Lk, p.causal, p.off, p.scale * kLog2e);
+      Q, K, V, O, LSE, BH, p.L, p.Lk, p.causal, p.off, p.scale * kLog2e, p.kv_len, p.H, p.br);
   return cudaGetLastError();
 }
 

@@ -115,7 +115,8 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, const A
 }
 
 // Warp-uniform variant: all 32 lanes call it; the result is the same on every
-// lane, so warp-collective instructions after it stay converged.
+// lane, so warp-collective instructions after it stay converged. (Polling from
+// lane 0 alone and broadcasting the result was measured slower in every kernel.)
 __device__ __forceinline__ bool mbar_wait_warp(uint32_t bar, uint32_t parity, const Abort &ab) {
   const bool ok = mbar_wait(bar, parity, ab);
   return __all_sync(0xffffffffu, ok);

@@ -163,6 +163,39 @@ int mg_attn_bwd_ex(const void *Q, const void *K, const void *V, const void *O,
                    void *workspace, size_t workspace_bytes, void *stream);
 
 /*
+ * Per-batch key padding (cross attention of a batch whose key sequences differ
+ * in length, e.g. text conditioning padded to a common Lk; the diffusion
+ * workload's text cross-attention in "Meganeura: Portable GPU Training and
+ * Inference through Vulkan and Metal", Section 4.1 "Matched workloads"; the
+ * pages print no mask convention for it, so this is the plain reading): batch
+ * element b has kv_len[b] real key rows, 0 <= kv_len[b] <= Lk, and the rows of
+ * K and V at or past kv_len[b] are padding. Batch element b is then exactly the
+ * problem of mg_attn_fwd_ex / mg_attn_bwd_ex with Lk = kv_len[b] keys: the
+ * bottom-right causal alignment uses its own offset kv_len[b] - Lq, a query row
+ * that sees no key has an empty softmax (O row 0, LSE -inf, dQ row 0), and the
+ * padding rows of dK and dV are written as 0.
+ *   kv_len  device array of B int32 lengths, 4-byte aligned, not overlapping any
+ *           output; NULL means no padding (then these calls are mg_attn_fwd_ex
+ *           and mg_attn_bwd_ex). The kernels clamp each length into [0, Lk]:
+ *           the host cannot read device memory without synchronising, so a
+ *           length outside that range is not reported as an error.
+ * Padding rows of K and V need not hold meaningful values, but under
+ * ACCEL_BF16 they must be finite: the tensor cores read whole 128-row tiles, and
+ * a NaN or infinity there would reach the outputs through a product with a zero
+ * probability. STRICT_F32 never reads them. Layouts, contracts, workspace
+ * (mg_attn_bwd_workspace_bytes_ex), ownership and errors as the _ex calls; the
+ * backward needs the O and LSE of mg_attn_fwd_padded with the same kv_len.
+ */
+int mg_attn_fwd_padded(const void *Q, const void *K, const void *V, void *O, float *LSE,
+                       const int *kv_len, int B, int H, int Lq, int Lk, int D, int mask,
+                       float scale, int contract, void *stream);
+int mg_attn_bwd_padded(const void *Q, const void *K, const void *V, const void *O,
+                       const void *dO, const float *LSE, void *dQ, void *dK, void *dV,
+                       const int *kv_len, int B, int H, int Lq, int Lk, int D, int mask,
+                       float scale, int contract, void *workspace, size_t workspace_bytes,
+                       void *stream);
+
+/*
  * mg_attn_bwd without a workspace, for callers that cannot allocate device
  * memory at all (a plugin whose host runtime owns every device allocation and
  * offers no scratch, a service that fixes its memory budget at start-up, a

@@ -207,3 +207,51 @@ def attn_bwd(Q, K, V, dO, causal: bool, scale: float, nthreads: int = 0):
     if rc:
         raise RuntimeError(f"oracle_attn_bwd failed ({rc})")
     return {"O": O, "LSE": LSE, "Dvec": Dvec, "dQ": dQ, "dK": dK, "dV": dV}
+
+
+def attn_bwd_padded(Q, K, V, dO, kv_len, mask, scale: float, nthreads: int = 0) -> dict:
+    """Per-batch key padding: Q, dO [B, H, Lq, D], K, V [B, H, Lk, D], kv_len B
+    integers in [0, Lk]. Batch element b is the cross-attention problem with its
+    first kv_len[b] keys only (the rows past it are padding and do not exist:
+    ``attn_bwd_ex`` on the truncated K and V, so the bottom-right alignment uses
+    kv_len[b] - Lq); the padding rows of dK and dV are 0. With kv_len[b] = 0 no
+    key exists: every row of b has an empty softmax (O = 0, LSE = -inf) and all
+    of b's gradients are 0. Returns O, LSE, Dvec, dQ, dK, dV in float64."""
+    Q, K, V, dO = _f64(Q), _f64(K), _f64(V), _f64(dO)
+    if Q.ndim != 4 or K.shape != V.shape or Q.shape != dO.shape or K.shape[:2] != Q.shape[:2]:
+        raise ValueError("expected Q, dO [B, H, Lq, D] and K, V [B, H, Lk, D]")
+    B, H, Lq, D = Q.shape
+    Lk = K.shape[2]
+    lens = [int(n) for n in np.asarray(kv_len).reshape(-1)]
+    if len(lens) != B or any(n < 0 or n > Lk for n in lens):
+        raise ValueError("kv_len must hold B lengths in [0, Lk]")
+    out = {"O": np.zeros_like(Q), "LSE": np.full((B, H, Lq), -np.inf),
+           "Dvec": np.zeros((B, H, Lq)), "dQ": np.zeros_like(Q), "dK": np.zeros_like(K),
+           "dV": np.zeros_like(K)}
+    for b, n in enumerate(lens):
+        if n == 0:
+            continue
+        r = attn_bwd_ex(Q[b], K[b, :, :n], V[b, :, :n], dO[b], mask, scale, nthreads)
+        for k in ("O", "LSE", "Dvec", "dQ"):
+            out[k][b] = r[k]
+        out["dK"][b, :, :n] = r["dK"]
+        out["dV"][b, :, :n] = r["dV"]
+    return out
+
+
+def attn_fwd_padded(Q, K, V, kv_len, mask, scale: float, nthreads: int = 0):
+    """(O, LSE) of ``attn_bwd_padded`` without the backward."""
+    Q, K, V = _f64(Q), _f64(K), _f64(V)
+    if Q.ndim != 4 or K.shape != V.shape or K.shape[:2] != Q.shape[:2]:
+        raise ValueError("expected Q [B, H, Lq, D] and K, V [B, H, Lk, D]")
+    B, H, Lq, D = Q.shape
+    Lk = K.shape[2]
+    lens = [int(n) for n in np.asarray(kv_len).reshape(-1)]
+    if len(lens) != B or any(n < 0 or n > Lk for n in lens):
+        raise ValueError("kv_len must hold B lengths in [0, Lk]")
+    O = np.zeros_like(Q)
+    LSE = np.full((B, H, Lq), -np.inf)
+    for b, n in enumerate(lens):
+        if n:
+            O[b], LSE[b] = attn_fwd_ex(Q[b], K[b, :, :n], V[b, :, :n], mask, scale, nthreads)
+    return O, LSE

@@ -234,3 +234,39 @@ def test_decode_workspace_bytes(lib):
     assert lib.mg_attn_fwd_decode_workspace_bytes(1, 1, 9, 100, 64, 0) == 0
     assert lib.mg_attn_fwd_decode_workspace_bytes(1, 1, 1, 0, 64, 0) == 0
     assert lib.mg_attn_fwd_decode_workspace_bytes(1, 1, 1, 100, 96, 0) == 0
+
+
+# ---------------------------------------------------------------- key padding (_padded calls)
+def fwd_pad(lib, Q=P(0), K=P(1), V=P(2), O=P(3), LSE=P(4), kv=P(10), B=2, H=2, Lq=64, Lk=96,
+            D=64, mask=1, scale=0.125, contract=1):
+    return lib.mg_attn_fwd_padded(Q, K, V, O, LSE, kv, B, H, Lq, Lk, D, mask, scale, contract,
+                                  None)
+
+
+def bwd_pad(lib, Q=P(0), K=P(1), V=P(2), O=P(3), dO=P(4), LSE=P(5), dQ=P(6), dK=P(7), dV=P(8),
+            kv=P(10), B=2, H=2, Lq=64, Lk=96, D=64, mask=1, scale=0.125, contract=1, ws=P(9),
+            ws_bytes=1 << 20):
+    return lib.mg_attn_bwd_padded(Q, K, V, O, dO, LSE, dQ, dK, dV, kv, B, H, Lq, Lk, D, mask,
+                                  scale, contract, ws, ws_bytes, None)
+
+
+@pytest.mark.parametrize("kw,code", [
+    (dict(kv=P(10) + 2), mg.MG_ERR_INVALID_ARG),    # lengths not 4-byte aligned
+    (dict(O=P(10)), mg.MG_ERR_INVALID_ARG),         # O overlaps the lengths
+    (dict(mask=5), mg.MG_ERR_INVALID_ARG),
+    (dict(D=48), mg.MG_ERR_UNSUPPORTED),
+    (dict(Q=0), mg.MG_ERR_INVALID_ARG),
+])
+def test_fwd_padded_rejects(lib, kw, code):
+    assert fwd_pad(lib, **kw) == code
+
+
+@pytest.mark.parametrize("kw,code", [
+    (dict(kv=P(10) + 1), mg.MG_ERR_INVALID_ARG),
+    (dict(dV=P(10)), mg.MG_ERR_INVALID_ARG),        # dV overlaps the lengths
+    (dict(ws=P(10)), mg.MG_ERR_INVALID_ARG),        # workspace overlaps the lengths
+    (dict(ws_bytes=16), mg.MG_ERR_WORKSPACE),
+    (dict(B=0), mg.MG_ERR_INVALID_ARG),
+])
+def test_bwd_padded_rejects(lib, kw, code):
+    assert bwd_pad(lib, **kw) == code

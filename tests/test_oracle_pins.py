@@ -376,3 +376,110 @@ def test_torch_float64_sdpa_cross_attention(mask):
     np.testing.assert_allclose(g["dQ"], tq.grad.numpy(), rtol=1e-11, atol=1e-12)
     np.testing.assert_allclose(g["dK"], tk.grad.numpy(), rtol=1e-11, atol=1e-12)
     np.testing.assert_allclose(g["dV"], tv.grad.numpy(), rtol=1e-11, atol=1e-12)
+
+
+# ---------------------------------------------------------------- key padding
+def loss_padded(Q, K, V, dO, kv_len, mask, scale):
+    O, _ = oracle.attn_fwd_padded(Q, K, V, kv_len, mask, scale)
+    return float(np.sum(O * dO))
+
+
+@pytest.mark.parametrize("mask", MASKS_EX)
+def test_padded_finite_differences(mask):
+    """Per-batch key padding: dQ, dK, dV equal central differences of
+    sum(dO * O) over every input element, padding rows included (their exact
+    gradient is 0: perturbing a padding key changes nothing)."""
+    B, H, Lq, Lk, D, scale, h = 3, 1, 4, 5, 2, 0.7, 1e-6
+    kv_len = [5, 2, 0]
+    Q, dO = rand(B, H, Lq, D), rand(B, H, Lq, D)
+    K, V = rand(B, H, Lk, D), rand(B, H, Lk, D)
+    g = oracle.attn_bwd_padded(Q, K, V, dO, kv_len, mask, scale)
+    for name, X in (("dQ", Q), ("dK", K), ("dV", V)):
+        num = np.zeros_like(X)
+        for idx in np.ndindex(X.shape):
+            orig = X[idx]
+            X[idx] = orig + h
+            lp = loss_padded(Q, K, V, dO, kv_len, mask, scale)
+            X[idx] = orig - h
+            lm = loss_padded(Q, K, V, dO, kv_len, mask, scale)
+            X[idx] = orig
+            num[idx] = (lp - lm) / (2 * h)
+        err = np.max(np.abs(num - g[name])) / max(np.max(np.abs(num)), 1e-300)
+        assert err < 1e-6, (name, err)
+    for b, n in enumerate(kv_len):
+        assert np.all(g["dK"][b, :, n:] == 0) and np.all(g["dV"][b, :, n:] == 0)
+
+
+@pytest.mark.parametrize("mask", MASKS_EX)
+def test_torch_float64_sdpa_padded(mask):
+    """Third implementation: torch CPU float64 SDPA with the boolean mask
+    (key j < kv_len[b]) AND the alignment of the mask computed from kv_len[b],
+    + autograd, on a batch whose every row keeps at least one key."""
+    torch = pytest.importorskip("torch")
+    import torch.nn.functional as F
+    B, H, Lq, Lk, D, scale = 3, 2, 5, 9, 4, 0.5
+    kv_len = [9, 6, 5]
+    Q, dO = rand(B, H, Lq, D), rand(B, H, Lq, D)
+    K, V = rand(B, H, Lk, D), rand(B, H, Lk, D)
+    allow = np.zeros((B, 1, Lq, Lk), bool)
+    i = np.arange(Lq)[:, None]
+    j = np.arange(Lk)[None, :]
+    for b, n in enumerate(kv_len):
+        a = j < n
+        if mask == "causal":
+            a = a & (j <= i)
+        elif mask == "causal_bottom_right":
+            a = a & (j <= i + (n - Lq))
+        allow[b, 0] = a
+    tq, tk, tv = (torch.tensor(x, dtype=torch.float64, requires_grad=True) for x in (Q, K, V))
+    out = F.scaled_dot_product_attention(tq, tk, tv, attn_mask=torch.tensor(allow), scale=scale)
+    out.backward(torch.tensor(dO, dtype=torch.float64))
+    g = oracle.attn_bwd_padded(Q, K, V, dO, kv_len, mask, scale)
+    np.testing.assert_allclose(g["O"], out.detach().numpy(), rtol=1e-12, atol=1e-12)
+    np.testing.assert_allclose(g["dQ"], tq.grad.numpy(), rtol=1e-11, atol=1e-12)
+    np.testing.assert_allclose(g["dK"], tk.grad.numpy(), rtol=1e-11, atol=1e-12)
+    np.testing.assert_allclose(g["dV"], tv.grad.numpy(), rtol=1e-11, atol=1e-12)
+
+
+def test_padded_closed_forms():
+    """kv_len = Lk is the unpadded problem; kv_len = 1 leaves one key, so every
+    row that sees it has O = V_0, dQ = dK = 0 and dV_0 = the sum of those rows'
+    dO; kv_len = 0 leaves none: O = 0, LSE = -inf, every gradient 0; padding
+    rows' contents do not matter."""
+    B, H, Lq, Lk, D, scale = 3, 2, 6, 7, 3, 0.8
+    Q, dO = rand(B, H, Lq, D), rand(B, H, Lq, D)
+    K, V = rand(B, H, Lk, D), rand(B, H, Lk, D)
+    g = oracle.attn_bwd_padded(Q, K, V, dO, [Lk, 1, 0], "none", scale)
+    full = oracle.attn_bwd_ex(Q[:1], K[:1], V[:1], dO[:1], "none", scale)
+    for k in ("O", "LSE", "dQ", "dK", "dV"):
+        np.testing.assert_array_equal(g[k][:1], full[k])
+    np.testing.assert_allclose(g["O"][1], np.broadcast_to(V[1, :, :1], (H, Lq, D)), atol=1e-15)
+    assert np.all(g["dQ"][1] == 0) and np.all(g["dK"][1] == 0)
+    np.testing.assert_allclose(g["dV"][1, :, 0], dO[1].sum(axis=1), rtol=1e-13, atol=1e-14)
+    assert np.all(g["dV"][1, :, 1:] == 0)
+    assert np.all(g["O"][2] == 0) and np.all(np.isneginf(g["LSE"][2]))
+    for k in ("dQ", "dK", "dV"):
+        assert np.all(g[k][2] == 0)
+    K2, V2 = K.copy(), V.copy()
+    K2[1, :, 1:] = 1e6 * rand(H, Lk - 1, D)
+    V2[1, :, 1:] = -1e6
+    g2 = oracle.attn_bwd_padded(Q, K2, V2, dO, [Lk, 1, 0], "none", scale)
+    for k in ("O", "LSE", "dQ", "dK", "dV"):
+        np.testing.assert_array_equal(g2[k][1:], g[k][1:])
+
+
+def test_padded_bottom_right_uses_own_length():
+    """Bottom-right alignment under padding: batch element b aligns its last
+    query with its own last real key (offset kv_len[b] - Lq); with Lq > kv_len[b]
+    the first Lq - kv_len[b] rows have an empty softmax."""
+    B, H, Lq, Lk, D, scale = 2, 1, 5, 8, 4, 0.6
+    Q, dO = rand(B, H, Lq, D), rand(B, H, Lq, D)
+    K, V = rand(B, H, Lk, D), rand(B, H, Lk, D)
+    g = oracle.attn_bwd_padded(Q, K, V, dO, [8, 3], "causal_bottom_right", scale)
+    # batch 1: 3 keys, 5 queries: rows 0, 1 see nothing; row 4 sees keys 0..2
+    assert np.all(np.isneginf(g["LSE"][1, :, :2])) and np.all(g["O"][1, :, :2] == 0)
+    r = oracle.attn_fwd_ex(Q[1, :, 4:], K[1, :, :3], V[1, :, :3], "none", scale)
+    np.testing.assert_allclose(g["O"][1, :, 4:], r[0], rtol=1e-14, atol=1e-15)
+    # batch 0 (unpadded): the ordinary bottom-right problem
+    r0 = oracle.attn_bwd_ex(Q[:1], K[:1], V[:1], dO[:1], "causal_bottom_right", scale)
+    np.testing.assert_array_equal(g["dK"][:1], r0["dK"])

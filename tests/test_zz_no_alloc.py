@@ -66,7 +66,7 @@ def test_noalloc_rejects_beyond_the_fixed_scratch():
     lib = _lib()
     fake = 1 << 40  # never dereferenced: the size check comes first
     rc = lib.mg_attn_bwd_noalloc(fake, fake, fake, fake, fake, fake, fake, fake, fake,
-                                 1, 1, MAX_ROWS + 1, 64, 1, 0.125, 0, None)
+                                 2, 1, MAX_ROWS // 2 + 1, 64, 1, 0.125, 0, None)
     assert rc == mg.MG_ERR_WORKSPACE
     rc = lib.mg_attn_bwd_noalloc(fake, fake, fake, fake, fake, fake, fake, fake, fake,
                                  2, 32, 16385, 128, 1, 0.125, 1, None)
