@@ -34,10 +34,11 @@
 // At D = 64 dQ_j = dS K has columns and a staging tile of its own.
 //
 // MMA issue order (steady state, block j):
-//   dK(j), dQ(j), dV(j+1), dP(j+1), S(j+2)
-// dV(j+1) and S(j+2) overlap the read-out of dQ(j); the softmax turns S(j+1)
-// into P(j+1) while dK(j) and dQ(j) run, and dP(j+1) into dS(j+1) while S(j+2)
-// runs. S(j+2) overwrites P(j+1) only after dV(j+1) has read it (issue order).
+//   dK(j), dQ(j), dP(j+1), dV(j+1), S(j+2)
+// The softmax turns S(j+1) into P(j+1) while dK(j), dQ(j) and dP(j+1) run, and
+// dP(j+1) into dS(j+1) while dV(j+1) and S(j+2) run. S(j+2) overwrites P(j+1)
+// only after dV(j+1) has read it (issue order); at D = 128 dP(j+1) also waits
+// for the read-out of dQ(j) from the same columns.
 //
 // Warp roles: 0-3 dQ read-out, 4 TMA producer of K, V, Q (plus LSE and Dvec
 // staging), 5 MMA issuer, 6 TMA producer of dO, 8-15 two softmax warpgroups
@@ -335,19 +336,18 @@ __global__ void __launch_bounds__(512, 1)
         tc_fence_after();
         issue_T(dV0, sdesc_add(dO0, (j % C::NQS) * C::Q_TILE), tmem + C::T_DP);
         mma_commit(bar(C::B_DPFULL));
-        // D = 64: dO_j's last reader is dP(j), except for block 0 whose dV comes
-        // later (D = 128: the dQ warps release the stage)
-        if (!C::kDqInDp && j > 0) mma_commit(bar(C::B_DOFREE + j % C::NQS));
         return true;
       };
       auto issue_dV = [&](int j) -> bool {
         if (!mbar_wait(bar(C::B_PREADY), j & 1, ab)) return false;
-        // dO_j may not have landed yet: from block 1 on, dV(j) comes before dP(j)
+        // dO_j has landed (dP(j) waited for it; the wait is kept for clarity)
         if (!mbar_wait(bar(C::B_DOFULL + j % C::NQS), (j / C::NQS) & 1, ab)) return false;
         tc_fence_after();
         issue_acc(tmem + C::T_S, sdesc_add(dOmn, (j % C::NQS) * C::Q_TILE), tmem + C::T_DV,
                   j == 0);
-        if (!C::kDqInDp && j == 0) mma_commit(bar(C::B_DOFREE));
+        // D = 64: dO_j's last reader is dV(j) (D = 128: the dQ warps release the
+        // stage, which then holds dQ(j))
+        if (!C::kDqInDp) mma_commit(bar(C::B_DOFREE + j % C::NQS));
         return true;
       };
       auto issue_dK = [&](int j) -> bool {
@@ -388,10 +388,10 @@ __global__ void __launch_bounds__(512, 1)
         if (!(ok = issue_dK(i))) break;
         if (!(ok = issue_dQ(i))) break;
         if (i + 1 < n) {
-          if (!(ok = issue_dV(i + 1))) break;
           // D = 128: dP^T's columns hold dQ(i) until the dQ warps have read it
           if (C::kDqInDp && !(ok = mbar_wait(bar(C::B_DQEMPTY), i & 1, ab))) break;
           if (!(ok = issue_dP(i + 1))) break;
+          if (!(ok = issue_dV(i + 1))) break;
           if (i + 2 < n && !(ok = issue_S(i + 2))) break;
         }
       }

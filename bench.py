@@ -46,8 +46,8 @@ L2_FLUSH_BYTES = 512 << 20  # > 129 MB L2
 # profiles/ (taken on half of the heads and scaled by 2; per-head traffic is
 # identical). Remove an entry when its kernel changes.
 NCU_TRAFFIC_BYTES = {
-    ("accel_dkdv_dq", 5): 2 * (404.883968e6 + 349.094912e6),
-    ("accel_fwd", 5): 2 * (552.298752e6 + 103.339776e6),
+    ("accel_dkdv_dq", 5): 2 * (405.131008e6 + 349.366528e6),
+    ("accel_fwd", 5): 2 * (202.861312e6 + 99.704320e6),
 }
 
 
@@ -69,6 +69,8 @@ def parse():
                     help="B,H,Lq,Lk,D,mask with Lq <= 8: measure the split-key decode forward "
                          "(mg_attn_fwd_decode) beside mg_attn_fwd_ex on the same inputs")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-configs", action="store_true",
+                    help="skip the compact per-config table (configurations 1-4) of the default run")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=15.0,
                     help="target CPU seconds for the oracle sample")
@@ -354,6 +356,59 @@ def run_e2e(mg, torch, w, contract, args, host, device, stream, flops_step):
                        "while step k computes (2 input, 3 output buffer sets)"}
 
 
+def run_small_configs(mg, torch, device, stream, peaks, sm_count, steps: int, warmup: int):
+    """fwd and fwd+bwd TFLOP/s of the four smaller seeded configurations for
+    every contract each one lists (CUDA events on the call stream, L2 flushed
+    between timed steps, median step): the compact ``configs`` object of the
+    default JSON line, so that those numbers come from the same run."""
+    out = {}
+    f32 = torch.float32
+    flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=f32, device=device)
+    s = stream.cuda_stream
+    for cfg in (1, 2, 3, 4):
+        w = synth.WORKLOADS[cfg]
+        B, H, L, D = w.shape
+        row = {"workload": w.name}
+        for c in w.contracts:
+            _, dev = make_inputs(w, c, torch, device)
+            O = torch.empty((B, H, L, D), dtype=f32, device=device)
+            LSE = torch.empty((B, H, L), dtype=f32, device=device)
+            dQ, dK, dV = (torch.empty_like(O) for _ in range(3))
+            ws = torch.empty(mg.mg_attn_bwd_workspace_bytes(B, H, L, D, c), dtype=torch.uint8,
+                             device=device)
+            fwd_ms, tot_ms = [], []
+            with torch.cuda.stream(stream):
+                for i in range(warmup + steps):
+                    flush.fill_(float(i))
+                    a, b, e = (torch.cuda.Event(enable_timing=True) for _ in range(3))
+                    a.record(stream)
+                    mg.mg_attn_fwd(dev["Q"], dev["K"], dev["V"], O, LSE, w.causal, w.scale, c, s)
+                    b.record(stream)
+                    mg.mg_attn_bwd(dev["Q"], dev["K"], dev["V"], O, dev["dO"], LSE, dQ, dK, dV,
+                                   w.causal, w.scale, c, ws, s)
+                    e.record(stream)
+                    if i >= warmup:
+                        fwd_ms.append((a, b))
+                        tot_ms.append((a, e))
+                torch.cuda.synchronize()
+            if mg.mg_get_device_error(s) != mg.MG_OK:
+                raise RuntimeError(f"cfg {cfg} {c}: device error word set")
+            fm = statistics.median(x.elapsed_time(y) for x, y in fwd_ms)
+            tm = statistics.median(x.elapsed_time(y) for x, y in tot_ms)
+            if c == "accel":
+                peak = peaks["bf16_tflops"]
+            else:
+                peak = fp32_simt_peak_tflops(sm_count, peaks["sm_max_mhz"])
+            tf = (w.flops_fwd() + w.flops_bwd()) / (tm * 1e-3) / 1e12
+            row["accel_bf16" if c == "accel" else "strict_f32"] = {
+                "fwd_bwd_tflops": round(tf, 2),
+                "fwd_tflops": round(w.flops_fwd() / (fm * 1e-3) / 1e12, 2),
+                "step_ms_median": round(tm, 4), "frac_of_peak_fwd_bwd": round(tf / peak, 4)}
+        out[str(cfg)] = row
+    del flush
+    return out
+
+
 # ------------------------------------------------------------------ distributed
 _DIST = {"on": False}
 
@@ -637,6 +692,9 @@ def main():
             "step_ms_raw", "kernels", "roofline", "clocks")}
         if "e2e" in rr:
             line["contracts"][key]["e2e"] = rr["e2e"]
+    if rank() == 0 and world() == 1 and not args.shape and w.cfg == 5 and not args.no_configs:
+        line["configs"] = run_small_configs(mg, torch, device, stream, peaks, sm_count,
+                                            steps=20, warmup=3)
     if rank() == 0 and not args.no_cpu_baseline and world() == 1:
         tf, cores, sample, _ = oracle_sample(w, head, args.cpu_seconds)
         line["cpu_baseline"] = {"value": tf, "unit": UNIT, "cores": cores, "kind": "oracle",
