@@ -20,7 +20,9 @@ The function names mirror the C ABI in ``include/mg_attn.h``:
 * ``mg_attn_profile_enable``, ``mg_attn_profile_read``, ``mg_attn_kernel_name``
 
 Tensors are PyTorch CUDA tensors, contiguous [B, H, L, D] (LSE [B, H, L]); the
-shape is read from Q. ``contract`` is ``STRICT_F32`` (0) or ``ACCEL_BF16`` (1).
+shape is read from Q. ``contract`` is ``STRICT_F32`` (0), ``ACCEL_BF16`` (1) or
+``ACCEL_F16`` (2), optionally OR-ed with ``OUT_16`` (16-bit outputs), or a name
+such as ``"accel"``, ``"accel_f16+out16"``.
 ``attention_fwd`` / ``attention_bwd`` are conveniences that allocate the
 outputs with PyTorch and call the above.
 """
@@ -32,7 +34,10 @@ import threading
 
 STRICT_F32 = 0
 ACCEL_BF16 = 1
-CONTRACTS = {"strict": STRICT_F32, "accel": ACCEL_BF16}
+ACCEL_F16 = 2
+OUT_16 = 0x100  # flag: O, dQ, dK, dV in the inputs' 16-bit type
+CONTRACTS = {"strict": STRICT_F32, "accel": ACCEL_BF16, "accel_f16": ACCEL_F16}
+FLAGS = {"out16": OUT_16}
 
 MG_OK, MG_ERR_INVALID_ARG, MG_ERR_UNSUPPORTED, MG_ERR_WORKSPACE, MG_ERR_CUDA, MG_ERR_TIMEOUT = range(6)
 
@@ -125,7 +130,24 @@ def _dims(Q):
 
 
 def _contract(c) -> int:
-    return CONTRACTS[c] if isinstance(c, str) else int(c)
+    """A contract as its int value: an int, or a name such as "accel_f16+out16"
+    (base contract, then "+"-joined flags)."""
+    if not isinstance(c, str):
+        return int(c)
+    base, *flags = c.split("+")
+    v = CONTRACTS[base]
+    for f in flags:
+        v |= FLAGS[f]
+    return v
+
+
+def _out_dtype(contract):
+    """torch dtype of O, dQ, dK, dV under a contract."""
+    import torch
+    c = _contract(contract)
+    if not c & OUT_16:
+        return torch.float32
+    return torch.float16 if (c & 0xFF) == ACCEL_F16 else torch.bfloat16
 
 
 def mg_status_string(status: int) -> str:
@@ -276,10 +298,11 @@ def mg_attn_kernel_name(kernel: int) -> str:
 
 # ------------------------------------------------------------ conveniences
 def attention_fwd(Q, K, V, causal: bool, scale: float, contract, stream=None):
-    """Allocate O (f32) and LSE (f32) with PyTorch and run mg_attn_fwd."""
+    """Allocate O (f32, or 16-bit under MG_OUT_16) and LSE (f32) with PyTorch
+    and run mg_attn_fwd."""
     import torch
     B, H, L, D = _dims(Q)
-    O = torch.empty((B, H, L, D), dtype=torch.float32, device=Q.device)
+    O = torch.empty((B, H, L, D), dtype=_out_dtype(contract), device=Q.device)
     LSE = torch.empty((B, H, L), dtype=torch.float32, device=Q.device)
     mg_attn_fwd(Q, K, V, O, LSE, causal, scale, contract, stream)
     return O, LSE
@@ -287,10 +310,11 @@ def attention_fwd(Q, K, V, causal: bool, scale: float, contract, stream=None):
 
 def attention_bwd(Q, K, V, O, dO, LSE, causal: bool, scale: float, contract, stream=None,
                   workspace=None):
-    """Allocate dQ, dK, dV (f32) and the workspace with PyTorch; run mg_attn_bwd."""
+    """Allocate dQ, dK, dV (f32, or 16-bit under MG_OUT_16) and the workspace
+    with PyTorch; run mg_attn_bwd."""
     import torch
     B, H, L, D = _dims(Q)
-    dQ = torch.empty((B, H, L, D), dtype=torch.float32, device=Q.device)
+    dQ = torch.empty((B, H, L, D), dtype=_out_dtype(contract), device=Q.device)
     dK = torch.empty_like(dQ)
     dV = torch.empty_like(dQ)
     if workspace is None:

@@ -146,7 +146,7 @@ __device__ __forceinline__ uint32_t dq_stage_off(int row, int col, int box_bytes
                                ((col & 3) << 2));
 }
 
-template <int DP>
+template <int DP, bool F16>
 __global__ void __launch_bounds__(512, 1)
     accel_dkdv_kernel(const __grid_constant__ CUtensorMap tmQ,
                       const __grid_constant__ CUtensorMap tmK,
@@ -154,7 +154,7 @@ __global__ void __launch_bounds__(512, 1)
                       const __grid_constant__ CUtensorMap tmdO,
                       const __grid_constant__ CUtensorMap tmdQ, const float *__restrict__ LSE,
                       const float *__restrict__ Dvec, float *__restrict__ dQ,
-                      float *__restrict__ dK, float *__restrict__ dV, int BH, int L,
+                      void *__restrict__ dK, void *__restrict__ dV, int out16, int BH, int L,
                       int Lk_rows, int D, int causal, int off0, float scale, float scale_log2,
                       unsigned int *err, unsigned long long timeout_ns,
                       const int *__restrict__ kv_len, int H, int br) {
@@ -287,10 +287,10 @@ __global__ void __launch_bounds__(512, 1)
   } else if (warp == 5) {
     // ------------------------------------------------------------ MMA issuer
     if (lane == 0) {
-      constexpr uint32_t idSP = idesc_bf16_f32(128, C::BQ, false, false);
-      constexpr uint32_t idKV = idesc_bf16_f32(128, DP, false, true);
+      constexpr uint32_t idSP = idesc_16_f32(128, C::BQ, false, false, F16);
+      constexpr uint32_t idKV = idesc_16_f32(128, DP, false, true, F16);
       constexpr uint32_t idDQ =
-          C::kDqInDp ? idesc_bf16_f32(128, C::BQ, true, true) : idesc_bf16_f32(128, DP, true, true);
+          C::kDqInDp ? idesc_16_f32(128, C::BQ, true, true, F16) : idesc_16_f32(128, DP, true, true, F16);
       bool ok = mbar_wait(bar(C::B_KVFULL), 0, ab);
       // base descriptors; each MMA adds a compile-time byte offset
       const uint32_t sb = opaque_u32(sbase);
@@ -531,7 +531,7 @@ __global__ void __launch_bounds__(512, 1)
       {
         uint32_t pk[C::QPW / 2];
 #pragma unroll
-        for (int e = 0; e < C::QPW / 2; ++e) pk[e] = pack_bf16(p[2 * e], p[2 * e + 1]);
+        for (int e = 0; e < C::QPW / 2; ++e) pk[e] = pack16<F16>(p[2 * e], p[2 * e + 1]);
         tmem_st32(tS, pk);
       }
       tmem_wait_st();
@@ -556,8 +556,8 @@ __global__ void __launch_bounds__(512, 1)
           const float a1 = p[32 * c + 2 * e + 1] * (__uint_as_float(r[2 * e + 1]) - d4.y);
           const float a2 = p[32 * c + 2 * e + 2] * (__uint_as_float(r[2 * e + 2]) - d4.z);
           const float a3 = p[32 * c + 2 * e + 3] * (__uint_as_float(r[2 * e + 3]) - d4.w);
-          pk[e] = pack_bf16(a0, a1);
-          pk[e + 1] = pack_bf16(a2, a3);
+          pk[e] = pack16<F16>(a0, a1);
+          pk[e + 1] = pack16<F16>(a2, a3);
         }
         tmem_st16(tDP + 16 * c, pk);
         // dS^T row kr, queries ql .. ql+31 into the swizzled smem tile
@@ -585,8 +585,8 @@ __global__ void __launch_bounds__(512, 1)
       // no query sees this key block: dK = dV = 0 (warpgroup g writes its half)
       const size_t row = (static_cast<size_t>(bh) * Lk_rows + kg) * D;
       for (int c = 0; c < DP / 2 && g * (DP / 2) + c < D; c += 4) {
-        *reinterpret_cast<float4 *>(dV + row + g * (DP / 2) + c) = make_float4(0.f, 0.f, 0.f, 0.f);
-        *reinterpret_cast<float4 *>(dK + row + g * (DP / 2) + c) = make_float4(0.f, 0.f, 0.f, 0.f);
+        store4<F16>(dV, out16, row + g * (DP / 2) + c, 0.f, 0.f, 0.f, 0.f);
+        store4<F16>(dK, out16, row + g * (DP / 2) + c, 0.f, 0.f, 0.f, 0.f);
       }
     }
     if (ok && n > 0) {
@@ -603,12 +603,12 @@ __global__ void __launch_bounds__(512, 1)
         if (valid && col < D) {
 #pragma unroll
           for (int e = 0; e < 32; e += 4) {
-            *reinterpret_cast<float4 *>(dV + row + col + e) =
-                make_float4(__uint_as_float(rv[e]), __uint_as_float(rv[e + 1]),
-                            __uint_as_float(rv[e + 2]), __uint_as_float(rv[e + 3]));
-            *reinterpret_cast<float4 *>(dK + row + col + e) = make_float4(
-                __uint_as_float(rk[e]) * scale, __uint_as_float(rk[e + 1]) * scale,
-                __uint_as_float(rk[e + 2]) * scale, __uint_as_float(rk[e + 3]) * scale);
+            store4<F16>(dV, out16, row + col + e, __uint_as_float(rv[e]),
+                        __uint_as_float(rv[e + 1]), __uint_as_float(rv[e + 2]),
+                        __uint_as_float(rv[e + 3]));
+            store4<F16>(dK, out16, row + col + e, __uint_as_float(rk[e]) * scale,
+                        __uint_as_float(rk[e + 1]) * scale, __uint_as_float(rk[e + 2]) * scale,
+                        __uint_as_float(rk[e + 3]) * scale);
           }
         }
       }
@@ -626,42 +626,44 @@ __global__ void __launch_bounds__(512, 1)
   }
 }
 
-template <int DP>
-cudaError_t launch(const __nv_bfloat16 *Q, const __nv_bfloat16 *K, const __nv_bfloat16 *V,
-                   const __nv_bfloat16 *dO, const float *LSE, const float *Dvec, float *dQ,
-                   float *dK, float *dV, const MgProblem &p, unsigned int *err,
-                   cudaStream_t st) {
+template <int DP, bool F16>
+cudaError_t launch(const void *Q, const void *K, const void *V, const void *dO, const float *LSE,
+                   const float *Dvec, float *dQ, void *dK, void *dV, const MgProblem &p,
+                   unsigned int *err, cudaStream_t st) {
   using C = BwdCfg<DP>;
   const int BH = p.B * p.H;
   CUtensorMap tq, tk, tv, tdo, tdq;
   cudaError_t e;
-  if ((e = mg_tmap_bf16(&tq, Q, p.D, p.L, BH, C::BQ)) != cudaSuccess) return e;
-  if ((e = mg_tmap_bf16(&tdo, dO, p.D, p.L, BH, C::BQ)) != cudaSuccess) return e;
-  if ((e = mg_tmap_bf16(&tk, K, p.D, p.Lk, BH, C::BN)) != cudaSuccess) return e;
-  if ((e = mg_tmap_bf16(&tv, V, p.D, p.Lk, BH, C::BN)) != cudaSuccess) return e;
+  if ((e = mg_tmap_16(&tq, Q, p.D, p.L, BH, C::BQ, F16)) != cudaSuccess) return e;
+  if ((e = mg_tmap_16(&tdo, dO, p.D, p.L, BH, C::BQ, F16)) != cudaSuccess) return e;
+  if ((e = mg_tmap_16(&tk, K, p.D, p.Lk, BH, C::BN, F16)) != cudaSuccess) return e;
+  if ((e = mg_tmap_16(&tv, V, p.D, p.Lk, BH, C::BN, F16)) != cudaSuccess) return e;
   // dQ add-reductions: D = 64 in 32-row slabs (one per read-out warp), D = 128
   // in [64 rows][32 columns] boxes (one per warp and half block)
   if ((e = mg_tmap_f32(&tdq, dQ, p.D, p.L, BH, C::DQ_TMA_ROWS)) != cudaSuccess) return e;
-  auto kern = accel_dkdv_kernel<DP>;
+  auto kern = accel_dkdv_kernel<DP, F16>;
   if ((e = mg_set_smem_attr(reinterpret_cast<const void *>(kern), C::SMEM_BYTES,
-                            DP == 64 ? 8 : 9)) != cudaSuccess)
+                            (DP == 64 ? 8 : 9) + (F16 ? 12 : 0))) != cudaSuccess)
     return e;
   const int nkb = (p.Lk + C::BN - 1) / C::BN;
   const long long grid = static_cast<long long>(nkb) * BH;
   kern<<<static_cast<unsigned>(grid), C::NTHREADS, C::SMEM_BYTES, st>>>(
-      tq, tk, tv, tdo, tdq, LSE, Dvec, dQ, dK, dV, BH, p.L, p.Lk, p.D, p.causal, p.off, p.scale,
-      p.scale * kLog2e, err, mg_wait_limit_ns(), p.kv_len, p.H, p.br);
+      tq, tk, tv, tdo, tdq, LSE, Dvec, dQ, dK, dV, p.out16, BH, p.L, p.Lk, p.D, p.causal, p.off,
+      p.scale, p.scale * kLog2e, err, mg_wait_limit_ns(), p.kv_len, p.H, p.br);
   return cudaGetLastError();
 }
 
 }  // namespace
 
-cudaError_t mg_launch_accel_dkdv(const __nv_bfloat16 *Q, const __nv_bfloat16 *K,
-                                 const __nv_bfloat16 *V, const __nv_bfloat16 *dO,
-                                 const float *LSE, const float *Dvec, float *dQ, float *dK,
-                                 float *dV, const MgProblem &p, unsigned int *err,
+cudaError_t mg_launch_accel_dkdv(const void *Q, const void *K, const void *V, const void *dO,
+                                 const float *LSE, const float *Dvec, float *dQ, void *dK,
+                                 void *dV, const MgProblem &p, unsigned int *err,
                                  cudaStream_t st) {
   if (!dQ) return cudaErrorInvalidValue;  // dK/dV alone: mg_launch_accel_dkdv_pp
-  if (p.D <= 64) return launch<64>(Q, K, V, dO, LSE, Dvec, dQ, dK, dV, p, err, st);
-  return launch<128>(Q, K, V, dO, LSE, Dvec, dQ, dK, dV, p, err, st);
+  if (p.f16) {
+    if (p.D <= 64) return launch<64, true>(Q, K, V, dO, LSE, Dvec, dQ, dK, dV, p, err, st);
+    return launch<128, true>(Q, K, V, dO, LSE, Dvec, dQ, dK, dV, p, err, st);
+  }
+  if (p.D <= 64) return launch<64, false>(Q, K, V, dO, LSE, Dvec, dQ, dK, dV, p, err, st);
+  return launch<128, false>(Q, K, V, dO, LSE, Dvec, dQ, dK, dV, p, err, st);
 }

@@ -82,14 +82,14 @@ __device__ __forceinline__ bool drain_wait(uint32_t bar, uint32_t parity, uint64
   return true;
 }
 
-template <int DP>
+template <int DP, bool F16>
 __global__ void __launch_bounds__(320, 1)
     accel_dkdv_pp_kernel(const __grid_constant__ CUtensorMap tmQ,
                          const __grid_constant__ CUtensorMap tmK,
                          const __grid_constant__ CUtensorMap tmV,
                          const __grid_constant__ CUtensorMap tmdO, const float *__restrict__ LSE,
-                         const float *__restrict__ Dvec, float *__restrict__ dK,
-                         float *__restrict__ dV, int BH, int L, int Lk_rows, int D, int causal,
+                         const float *__restrict__ Dvec, void *__restrict__ dK,
+                         void *__restrict__ dV, int out16, int BH, int L, int Lk_rows, int D, int causal,
                          int off0, float scale, float scale_log2, unsigned int *err,
                          unsigned long long timeout_ns, const int *__restrict__ kv_len, int H,
                          int br) {
@@ -190,8 +190,8 @@ __global__ void __launch_bounds__(320, 1)
   } else if (warp == 9) {
     // ------------------------------------------------------------ MMA issuer
     if (lane == 0) {
-      constexpr uint32_t idSP = idesc_bf16_f32(128, C::BQ, false, false);
-      constexpr uint32_t idKV = idesc_bf16_f32(128, DP, false, true);
+      constexpr uint32_t idSP = idesc_16_f32(128, C::BQ, false, false, F16);
+      constexpr uint32_t idKV = idesc_16_f32(128, DP, false, true, F16);
       bool ok = mbar_wait(bar(C::B_KVFULL), 0, ab);
       // base descriptors; each MMA adds a compile-time byte offset
       const uint32_t sb = opaque_u32(sbase);
@@ -298,7 +298,7 @@ __global__ void __launch_bounds__(320, 1)
       for (int c = 0; c < 2; ++c) {
         uint32_t pk[16];
 #pragma unroll
-        for (int e = 0; e < 16; ++e) pk[e] = pack_bf16(p[32 * c + 2 * e], p[32 * c + 2 * e + 1]);
+        for (int e = 0; e < 16; ++e) pk[e] = pack16<F16>(p[32 * c + 2 * e], p[32 * c + 2 * e + 1]);
         tmem_st16(tS + 16 * c, pk);
       }
       tmem_wait_st();
@@ -325,8 +325,8 @@ __global__ void __launch_bounds__(320, 1)
             const float s1 = p[q + 1] * (__uint_as_float(r[q + 1]) - d4.y);
             const float s2 = p[q + 2] * (__uint_as_float(r[q + 2]) - d4.z);
             const float s3 = p[q + 3] * (__uint_as_float(r[q + 3]) - d4.w);
-            pk[e / 2] = pack_bf16(s0, s1);
-            pk[e / 2 + 1] = pack_bf16(s2, s3);
+            pk[e / 2] = pack16<F16>(s0, s1);
+            pk[e / 2 + 1] = pack16<F16>(s2, s3);
           }
           tmem_st16(tDP + 16 * c, pk);
         }
@@ -345,8 +345,8 @@ __global__ void __launch_bounds__(320, 1)
       // no query sees this key block: dK = dV = 0 (warpgroup w writes its half)
       const size_t row = (static_cast<size_t>(bh) * Lk_rows + kg) * D;
       for (int c = 0; c < DP / 2 && w * (DP / 2) + c < D; c += 4) {
-        *reinterpret_cast<float4 *>(dV + row + w * (DP / 2) + c) = make_float4(0.f, 0.f, 0.f, 0.f);
-        *reinterpret_cast<float4 *>(dK + row + w * (DP / 2) + c) = make_float4(0.f, 0.f, 0.f, 0.f);
+        store4<F16>(dV, out16, row + w * (DP / 2) + c, 0.f, 0.f, 0.f, 0.f);
+        store4<F16>(dK, out16, row + w * (DP / 2) + c, 0.f, 0.f, 0.f, 0.f);
       }
     }
     if (ok && n > 0) {
@@ -363,12 +363,12 @@ __global__ void __launch_bounds__(320, 1)
         if (valid && col < D) {
 #pragma unroll
           for (int e = 0; e < 32; e += 4) {
-            *reinterpret_cast<float4 *>(dV + row + col + e) =
-                make_float4(__uint_as_float(rv[e]), __uint_as_float(rv[e + 1]),
-                            __uint_as_float(rv[e + 2]), __uint_as_float(rv[e + 3]));
-            *reinterpret_cast<float4 *>(dK + row + col + e) = make_float4(
-                __uint_as_float(rk[e]) * scale, __uint_as_float(rk[e + 1]) * scale,
-                __uint_as_float(rk[e + 2]) * scale, __uint_as_float(rk[e + 3]) * scale);
+            store4<F16>(dV, out16, row + col + e, __uint_as_float(rv[e]),
+                        __uint_as_float(rv[e + 1]), __uint_as_float(rv[e + 2]),
+                        __uint_as_float(rv[e + 3]));
+            store4<F16>(dK, out16, row + col + e, __uint_as_float(rk[e]) * scale,
+                        __uint_as_float(rk[e + 1]) * scale, __uint_as_float(rk[e + 2]) * scale,
+                        __uint_as_float(rk[e + 3]) * scale);
           }
         }
       }
@@ -386,36 +386,39 @@ __global__ void __launch_bounds__(320, 1)
   }
 }
 
-template <int DP>
-cudaError_t launch(const __nv_bfloat16 *Q, const __nv_bfloat16 *K, const __nv_bfloat16 *V,
-                   const __nv_bfloat16 *dO, const float *LSE, const float *Dvec, float *dK,
-                   float *dV, const MgProblem &p, unsigned int *err, cudaStream_t st) {
+template <int DP, bool F16>
+cudaError_t launch(const void *Q, const void *K, const void *V, const void *dO, const float *LSE,
+                   const float *Dvec, void *dK, void *dV, const MgProblem &p, unsigned int *err,
+                   cudaStream_t st) {
   using C = PPCfg<DP>;
   const int BH = p.B * p.H;
   CUtensorMap tq, tk, tv, tdo;
   cudaError_t e;
-  if ((e = mg_tmap_bf16(&tq, Q, p.D, p.L, BH, C::BQ)) != cudaSuccess) return e;
-  if ((e = mg_tmap_bf16(&tdo, dO, p.D, p.L, BH, C::BQ)) != cudaSuccess) return e;
-  if ((e = mg_tmap_bf16(&tk, K, p.D, p.Lk, BH, C::BN)) != cudaSuccess) return e;
-  if ((e = mg_tmap_bf16(&tv, V, p.D, p.Lk, BH, C::BN)) != cudaSuccess) return e;
-  auto kern = accel_dkdv_pp_kernel<DP>;
+  if ((e = mg_tmap_16(&tq, Q, p.D, p.L, BH, C::BQ, F16)) != cudaSuccess) return e;
+  if ((e = mg_tmap_16(&tdo, dO, p.D, p.L, BH, C::BQ, F16)) != cudaSuccess) return e;
+  if ((e = mg_tmap_16(&tk, K, p.D, p.Lk, BH, C::BN, F16)) != cudaSuccess) return e;
+  if ((e = mg_tmap_16(&tv, V, p.D, p.Lk, BH, C::BN, F16)) != cudaSuccess) return e;
+  auto kern = accel_dkdv_pp_kernel<DP, F16>;
   if ((e = mg_set_smem_attr(reinterpret_cast<const void *>(kern), C::SMEM_BYTES,
-                            DP == 64 ? 16 : 17)) != cudaSuccess)
+                            (DP == 64 ? 16 : 17) + (F16 ? 12 : 0))) != cudaSuccess)
     return e;
   const int nkb = (p.Lk + C::BN - 1) / C::BN;
   const long long grid = static_cast<long long>(nkb) * BH;
   kern<<<static_cast<unsigned>(grid), C::NTHREADS, C::SMEM_BYTES, st>>>(
-      tq, tk, tv, tdo, LSE, Dvec, dK, dV, BH, p.L, p.Lk, p.D, p.causal, p.off, p.scale,
-      p.scale * kLog2e, err, mg_wait_limit_ns(), p.kv_len, p.H, p.br);
+      tq, tk, tv, tdo, LSE, Dvec, dK, dV, p.out16, BH, p.L, p.Lk, p.D, p.causal, p.off,
+      p.scale, p.scale * kLog2e, err, mg_wait_limit_ns(), p.kv_len, p.H, p.br);
   return cudaGetLastError();
 }
 
 }  // namespace
 
-cudaError_t mg_launch_accel_dkdv_pp(const __nv_bfloat16 *Q, const __nv_bfloat16 *K,
-                                    const __nv_bfloat16 *V, const __nv_bfloat16 *dO,
-                                    const float *LSE, const float *Dvec, float *dK, float *dV,
+cudaError_t mg_launch_accel_dkdv_pp(const void *Q, const void *K, const void *V, const void *dO,
+                                    const float *LSE, const float *Dvec, void *dK, void *dV,
                                     const MgProblem &p, unsigned int *err, cudaStream_t st) {
-  if (p.D <= 64) return launch<64>(Q, K, V, dO, LSE, Dvec, dK, dV, p, err, st);
-  return launch<128>(Q, K, V, dO, LSE, Dvec, dK, dV, p, err, st);
+  if (p.f16) {
+    if (p.D <= 64) return launch<64, true>(Q, K, V, dO, LSE, Dvec, dK, dV, p, err, st);
+    return launch<128, true>(Q, K, V, dO, LSE, Dvec, dK, dV, p, err, st);
+  }
+  if (p.D <= 64) return launch<64, false>(Q, K, V, dO, LSE, Dvec, dK, dV, p, err, st);
+  return launch<128, false>(Q, K, V, dO, LSE, Dvec, dK, dV, p, err, st);
 }

@@ -74,13 +74,13 @@ __device__ __forceinline__ bool drain_wait(uint32_t bar, uint32_t parity, uint64
   return true;
 }
 
-template <int DP>
+template <int DP, bool F16>
 __global__ void __launch_bounds__(320, 1)
     accel_dq_kernel(const __grid_constant__ CUtensorMap tmQ,
                     const __grid_constant__ CUtensorMap tmdO,
                     const __grid_constant__ CUtensorMap tmK,
                     const __grid_constant__ CUtensorMap tmV, const float *__restrict__ LSE,
-                    const float *__restrict__ Dvec, float *__restrict__ dQ, int BH, int L,
+                    const float *__restrict__ Dvec, void *__restrict__ dQ, int out16, int BH, int L,
                     int Lk_rows, int D, int causal, int off0, float scale, float scale_log2,
                     const int *__restrict__ kv_len, int H, int br, unsigned int *err,
                     unsigned long long timeout_ns) {
@@ -167,8 +167,8 @@ __global__ void __launch_bounds__(320, 1)
   } else if (warp == 9) {
     // ------------------------------------------------------------ MMA issuer
     if (lane == 0) {
-      constexpr uint32_t idSD = idesc_bf16_f32(128, C::BN, false, false);
-      constexpr uint32_t idQ = idesc_bf16_f32(128, DP, false, true);
+      constexpr uint32_t idSD = idesc_16_f32(128, C::BN, false, false, F16);
+      constexpr uint32_t idQ = idesc_16_f32(128, DP, false, true, F16);
       // base descriptors; each MMA adds a compile-time byte offset
       const uint32_t sb = opaque_u32(sbase);
       const uint64_t dQ0 = sdesc_sw128(sb + C::OFF_Q, 0, 1024);
@@ -273,7 +273,7 @@ __global__ void __launch_bounds__(320, 1)
         for (int e = 0; e < 16; ++e) {
           const float d0 = p[32 * c + 2 * e] * (__uint_as_float(r[2 * e]) - dvr);
           const float d1 = p[32 * c + 2 * e + 1] * (__uint_as_float(r[2 * e + 1]) - dvr);
-          pk[e] = pack_bf16(d0, d1);
+          pk[e] = pack16<F16>(d0, d1);
         }
         // dS over the S columns this warpgroup has already read
         tmem_st16(tS + 16 * c, pk);
@@ -286,13 +286,13 @@ __global__ void __launch_bounds__(320, 1)
     if (ok && n > 0) ok = mbar_wait_warp(bar(C::B_DQDONE), 0, ab);
     if (ok && n == 0 && vrow) {
       // no key tile for this query block: dQ = 0 (warpgroup g writes its half)
-      float *row = dQ + (static_cast<size_t>(bh) * L + qrow) * D;
+      const size_t row = (static_cast<size_t>(bh) * L + qrow) * D;
       for (int c = 0; c < DP / 2 && g * (DP / 2) + c < D; c += 4)
-        *reinterpret_cast<float4 *>(row + g * (DP / 2) + c) = make_float4(0.f, 0.f, 0.f, 0.f);
+        store4<F16>(dQ, out16, row + g * (DP / 2) + c, 0.f, 0.f, 0.f, 0.f);
     }
     if (ok && n > 0) {
       tc_fence_after();
-      float *row = dQ + (static_cast<size_t>(bh) * L + (vrow ? qrow : 0)) * D;
+      const size_t row = (static_cast<size_t>(bh) * L + (vrow ? qrow : 0)) * D;
 #pragma unroll
       for (int c = 0; c < DP / 64; ++c) {
         const int col = g * (DP / 2) + 32 * c;
@@ -302,9 +302,9 @@ __global__ void __launch_bounds__(320, 1)
         if (vrow && col < D) {
 #pragma unroll
           for (int e = 0; e < 32; e += 4)
-            *reinterpret_cast<float4 *>(row + col + e) = make_float4(
-                __uint_as_float(r[e]) * scale, __uint_as_float(r[e + 1]) * scale,
-                __uint_as_float(r[e + 2]) * scale, __uint_as_float(r[e + 3]) * scale);
+            store4<F16>(dQ, out16, row + col + e, __uint_as_float(r[e]) * scale,
+                        __uint_as_float(r[e + 1]) * scale, __uint_as_float(r[e + 2]) * scale,
+                        __uint_as_float(r[e + 3]) * scale);
         }
       }
     }
@@ -320,36 +320,39 @@ __global__ void __launch_bounds__(320, 1)
   }
 }
 
-template <int DP>
-cudaError_t launch(const __nv_bfloat16 *Q, const __nv_bfloat16 *K, const __nv_bfloat16 *V,
-                   const __nv_bfloat16 *dO, const float *LSE, const float *Dvec, float *dQ,
-                   const MgProblem &p, unsigned int *err, cudaStream_t st) {
+template <int DP, bool F16>
+cudaError_t launch(const void *Q, const void *K, const void *V, const void *dO, const float *LSE,
+                   const float *Dvec, void *dQ, const MgProblem &p, unsigned int *err,
+                   cudaStream_t st) {
   using C = DqCfg<DP>;
   const int BH = p.B * p.H;
   CUtensorMap tq, tdo, tk, tv;
   cudaError_t e;
-  if ((e = mg_tmap_bf16(&tq, Q, p.D, p.L, BH, C::BM)) != cudaSuccess) return e;
-  if ((e = mg_tmap_bf16(&tdo, dO, p.D, p.L, BH, C::BM)) != cudaSuccess) return e;
-  if ((e = mg_tmap_bf16(&tk, K, p.D, p.Lk, BH, C::BN)) != cudaSuccess) return e;
-  if ((e = mg_tmap_bf16(&tv, V, p.D, p.Lk, BH, C::BN)) != cudaSuccess) return e;
-  auto kern = accel_dq_kernel<DP>;
+  if ((e = mg_tmap_16(&tq, Q, p.D, p.L, BH, C::BM, F16)) != cudaSuccess) return e;
+  if ((e = mg_tmap_16(&tdo, dO, p.D, p.L, BH, C::BM, F16)) != cudaSuccess) return e;
+  if ((e = mg_tmap_16(&tk, K, p.D, p.Lk, BH, C::BN, F16)) != cudaSuccess) return e;
+  if ((e = mg_tmap_16(&tv, V, p.D, p.Lk, BH, C::BN, F16)) != cudaSuccess) return e;
+  auto kern = accel_dq_kernel<DP, F16>;
   if ((e = mg_set_smem_attr(reinterpret_cast<const void *>(kern), C::SMEM_BYTES,
-                            DP == 64 ? 10 : 11)) != cudaSuccess)
+                            (DP == 64 ? 10 : 11) + (F16 ? 12 : 0))) != cudaSuccess)
     return e;
   const int nqb = (p.L + C::BM - 1) / C::BM;
   const long long grid = static_cast<long long>(nqb) * BH;
   kern<<<static_cast<unsigned>(grid), C::NTHREADS, C::SMEM_BYTES, st>>>(
-      tq, tdo, tk, tv, LSE, Dvec, dQ, BH, p.L, p.Lk, p.D, p.causal, p.off, p.scale,
+      tq, tdo, tk, tv, LSE, Dvec, dQ, p.out16, BH, p.L, p.Lk, p.D, p.causal, p.off, p.scale,
       p.scale * kLog2e, p.kv_len, p.H, p.br, err, mg_wait_limit_ns());
   return cudaGetLastError();
 }
 
 }  // namespace
 
-cudaError_t mg_launch_accel_dq(const __nv_bfloat16 *Q, const __nv_bfloat16 *K,
-                               const __nv_bfloat16 *V, const __nv_bfloat16 *dO, const float *LSE,
-                               const float *Dvec, float *dQ, const MgProblem &p,
+cudaError_t mg_launch_accel_dq(const void *Q, const void *K, const void *V, const void *dO,
+                               const float *LSE, const float *Dvec, void *dQ, const MgProblem &p,
                                unsigned int *err, cudaStream_t st) {
-  if (p.D <= 64) return launch<64>(Q, K, V, dO, LSE, Dvec, dQ, p, err, st);
-  return launch<128>(Q, K, V, dO, LSE, Dvec, dQ, p, err, st);
+  if (p.f16) {
+    if (p.D <= 64) return launch<64, true>(Q, K, V, dO, LSE, Dvec, dQ, p, err, st);
+    return launch<128, true>(Q, K, V, dO, LSE, Dvec, dQ, p, err, st);
+  }
+  if (p.D <= 64) return launch<64, false>(Q, K, V, dO, LSE, Dvec, dQ, p, err, st);
+  return launch<128, false>(Q, K, V, dO, LSE, Dvec, dQ, p, err, st);
 }

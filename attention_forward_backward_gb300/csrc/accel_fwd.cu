@@ -79,11 +79,11 @@ __device__ __forceinline__ bool drain_wait(uint32_t bar, uint32_t parity, uint64
   return true;
 }
 
-template <int DP>
+template <int DP, bool F16>
 __global__ void __launch_bounds__(320, 1)
     accel_fwd_kernel(const __grid_constant__ CUtensorMap tmQ,
                      const __grid_constant__ CUtensorMap tmK,
-                     const __grid_constant__ CUtensorMap tmV, float *__restrict__ O,
+                     const __grid_constant__ CUtensorMap tmV, void *__restrict__ Ov, int out16,
                      float *__restrict__ LSE, int BH, int L, int Lk_rows, int D, int causal,
                      int off0, float scale_log2, unsigned int *err, unsigned long long timeout_ns,
                      int fault, int G, const int *__restrict__ kv_len, int H, int br) {
@@ -187,8 +187,8 @@ __global__ void __launch_bounds__(320, 1)
   } else if (warp == 9) {
     // ------------------------------------------------------------ MMA issuer
     if (lane == 0) {
-      constexpr uint32_t idS = idesc_bf16_f32(128, C::BN, false, false);
-      constexpr uint32_t idO = idesc_bf16_f32(128, DP, false, true);
+      constexpr uint32_t idS = idesc_16_f32(128, C::BN, false, false, F16);
+      constexpr uint32_t idO = idesc_16_f32(128, DP, false, true, F16);
       bool ok = mbar_wait(bar(C::B_QFULL), 0, ab);
       // base descriptors; each MMA adds a compile-time byte offset
       const uint32_t sb = opaque_u32(sbase);
@@ -291,7 +291,7 @@ __global__ void __launch_bounds__(320, 1)
         const float p0 = ex2(fmaf(__uint_as_float(r[2 * e]), scale_log2, -m_use));
         const float p1 = ex2(fmaf(__uint_as_float(r[2 * e + 1]), scale_log2, -m_use));
         rs += p0 + p1;
-        pk[e] = pack_bf16(p0, p1);
+        pk[e] = pack16<F16>(p0, p1);
       }
       if (warp_need) {
         const float alpha = m_new == -INFINITY ? 1.f : ex2(m_ref - m_new);
@@ -324,16 +324,21 @@ __global__ void __launch_bounds__(320, 1)
     if (ok && n > 0) ok = mbar_wait_warp(bar(C::B_ODONE + q), (n - 1) & 1, ab);
     if (ok && n == 0 && qrow < L) {
       // no key tile at all for this query tile: every row has an empty softmax
-      float *orow = O + (static_cast<size_t>(bh) * L + qrow) * D;
-      for (int c = 0; c < D; c += 4)
-        *reinterpret_cast<float4 *>(orow + c) = make_float4(0.f, 0.f, 0.f, 0.f);
+      const size_t o0 = (static_cast<size_t>(bh) * L + qrow) * D;
+      for (int c = 0; c < D; c += 4) {
+        if (out16)
+          *reinterpret_cast<uint2 *>(static_cast<uint16_t *>(Ov) + o0 + c) = make_uint2(0u, 0u);
+        else
+          *reinterpret_cast<float4 *>(static_cast<float *>(Ov) + o0 + c) =
+              make_float4(0.f, 0.f, 0.f, 0.f);
+      }
       LSE[static_cast<size_t>(bh) * L + qrow] = -INFINITY;
     }
     if (ok && n > 0) {
       tc_fence_after();
       const float inv = l > 0.f ? 1.f / l : 0.f;  // l = 0: no allowed key, O = 0
       const bool valid = qrow < L;
-      float *orow = O + (static_cast<size_t>(bh) * L + (valid ? qrow : 0)) * D;
+      const size_t o0 = (static_cast<size_t>(bh) * L + (valid ? qrow : 0)) * D;
 #pragma unroll
       for (int c = 0; c < DP / 32; ++c) {
         uint32_t r[32];
@@ -342,10 +347,14 @@ __global__ void __launch_bounds__(320, 1)
         if (valid && 32 * c < D) {
 #pragma unroll
           for (int e = 0; e < 32; e += 4) {
-            float4 v = make_float4(__uint_as_float(r[e]) * inv, __uint_as_float(r[e + 1]) * inv,
-                                   __uint_as_float(r[e + 2]) * inv,
-                                   __uint_as_float(r[e + 3]) * inv);
-            *reinterpret_cast<float4 *>(orow + 32 * c + e) = v;
+            const float a = __uint_as_float(r[e]) * inv, b = __uint_as_float(r[e + 1]) * inv;
+            const float cc = __uint_as_float(r[e + 2]) * inv, d = __uint_as_float(r[e + 3]) * inv;
+            if (out16)
+              *reinterpret_cast<uint2 *>(static_cast<uint16_t *>(Ov) + o0 + 32 * c + e) =
+                  pack16x4<F16>(a, b, cc, d);
+            else
+              *reinterpret_cast<float4 *>(static_cast<float *>(Ov) + o0 + 32 * c + e) =
+                  make_float4(a, b, cc, d);
           }
         }
       }
@@ -375,20 +384,19 @@ int fault_mode() {
   return v;
 }
 
-template <int DP>
-cudaError_t launch(const __nv_bfloat16 *Q, const __nv_bfloat16 *K, const __nv_bfloat16 *V,
-                   float *O, float *LSE, const MgProblem &p, unsigned int *err,
-                   cudaStream_t st) {
+template <int DP, bool F16>
+cudaError_t launch(const void *Q, const void *K, const void *V, void *O, float *LSE,
+                   const MgProblem &p, unsigned int *err, cudaStream_t st) {
   using C = FwdCfg<DP>;
   const int BH = p.B * p.H;
   CUtensorMap tq, tk, tv;
   cudaError_t e;
-  if ((e = mg_tmap_bf16(&tq, Q, p.D, p.L, BH, C::BM)) != cudaSuccess) return e;
-  if ((e = mg_tmap_bf16(&tk, K, p.D, p.Lk, BH, C::BN)) != cudaSuccess) return e;
-  if ((e = mg_tmap_bf16(&tv, V, p.D, p.Lk, BH, C::BN)) != cudaSuccess) return e;
-  auto kern = accel_fwd_kernel<DP>;
+  if ((e = mg_tmap_16(&tq, Q, p.D, p.L, BH, C::BM, F16)) != cudaSuccess) return e;
+  if ((e = mg_tmap_16(&tk, K, p.D, p.Lk, BH, C::BN, F16)) != cudaSuccess) return e;
+  if ((e = mg_tmap_16(&tv, V, p.D, p.Lk, BH, C::BN, F16)) != cudaSuccess) return e;
+  auto kern = accel_fwd_kernel<DP, F16>;
   if ((e = mg_set_smem_attr(reinterpret_cast<const void *>(kern), C::SMEM_BYTES,
-                            DP == 64 ? 6 : 7)) != cudaSuccess)
+                            (DP == 64 ? 6 : 7) + (F16 ? 12 : 0))) != cudaSuccess)
     return e;
   const int nqb = (p.L + 255) / 256;
   const long long grid = static_cast<long long>(nqb) * BH;
@@ -396,16 +404,19 @@ cudaError_t launch(const __nv_bfloat16 *Q, const __nv_bfloat16 *K, const __nv_bf
   const long long kv_head = 2LL * p.Lk * p.D * 2;
   const int G = static_cast<int>(std::max(1LL, std::min<long long>(BH, (32LL << 20) / kv_head)));
   kern<<<static_cast<unsigned>(grid), C::NTHREADS, C::SMEM_BYTES, st>>>(
-      tq, tk, tv, O, LSE, BH, p.L, p.Lk, p.D, p.causal, p.off, p.scale * kLog2e, err,
+      tq, tk, tv, O, p.out16, LSE, BH, p.L, p.Lk, p.D, p.causal, p.off, p.scale * kLog2e, err,
       mg_wait_limit_ns(), fault_mode(), G, p.kv_len, p.H, p.br);
   return cudaGetLastError();
 }
 
 }  // namespace
 
-cudaError_t mg_launch_accel_fwd(const __nv_bfloat16 *Q, const __nv_bfloat16 *K,
-                                const __nv_bfloat16 *V, float *O, float *LSE,
+cudaError_t mg_launch_accel_fwd(const void *Q, const void *K, const void *V, void *O, float *LSE,
                                 const MgProblem &p, unsigned int *err, cudaStream_t st) {
-  if (p.D <= 64) return launch<64>(Q, K, V, O, LSE, p, err, st);
-  return launch<128>(Q, K, V, O, LSE, p, err, st);
+  if (p.f16) {
+    if (p.D <= 64) return launch<64, true>(Q, K, V, O, LSE, p, err, st);
+    return launch<128, true>(Q, K, V, O, LSE, p, err, st);
+  }
+  if (p.D <= 64) return launch<64, false>(Q, K, V, O, LSE, p, err, st);
+  return launch<128, false>(Q, K, V, O, LSE, p, err, st);
 }

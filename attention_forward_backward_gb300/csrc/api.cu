@@ -83,7 +83,8 @@ void prof_free() {
 
 const char *const kKernelNames[MGK_COUNT] = {
     "strict_fwd", "strict_dvec", "strict_dkdv_dq", "accel_fwd",     "accel_dvec",
-    "accel_dkdv_dq", "dq_zero",  "accel_dkdv",    "accel_dq",    "decode_fwd"};
+    "accel_dkdv_dq", "dq_zero",  "accel_dkdv",    "accel_dq",    "decode_fwd",
+    "dq_round"};
 
 // How the ACCEL backward produces dQ: f32 TMA reductions from the fused dK/dV
 // kernel (default, measured faster on GB300) or a separate dQ pass that
@@ -111,20 +112,34 @@ int check_common(int B, int H, int Lq, int Lk, int D, int mask, float scale, int
   if (mask != MG_MASK_NONE && mask != MG_MASK_CAUSAL && mask != MG_MASK_CAUSAL_BOTTOM_RIGHT)
     return MG_ERR_INVALID_ARG;
   if (!(scale > 0.f) || !isfinite(scale)) return MG_ERR_INVALID_ARG;
-  if (contract != MG_CONTRACT_STRICT_F32 && contract != MG_CONTRACT_ACCEL_BF16)
+  const int base = contract & MG_CONTRACT_BASE_MASK, flags = contract & ~MG_CONTRACT_BASE_MASK;
+  if (base != MG_CONTRACT_STRICT_F32 && base != MG_CONTRACT_ACCEL_BF16 &&
+      base != MG_CONTRACT_ACCEL_F16)
     return MG_ERR_INVALID_ARG;
+  if (flags & ~MG_OUT_16) return MG_ERR_INVALID_ARG;
+  // STRICT_F32 is f32 end to end: no 16-bit outputs
+  if (flags && base == MG_CONTRACT_STRICT_F32) return MG_ERR_UNSUPPORTED;
   if (D != 32 && D != 64 && D != 128) return MG_ERR_UNSUPPORTED;
   return MG_OK;
 }
 
 MgProblem make_problem(int B, int H, int Lq, int Lk, int D, int mask, float scale,
-                       const int *kv_len = nullptr) {
+                       const int *kv_len = nullptr, int contract = 0) {
   MgProblem p{B, H, Lq, D, mask != MG_MASK_NONE ? 1 : 0, scale, Lk, 0};
   if (mask == MG_MASK_CAUSAL_BOTTOM_RIGHT) p.off = Lk - Lq;
   p.kv_len = kv_len;
   p.br = mask == MG_MASK_CAUSAL_BOTTOM_RIGHT ? 1 : 0;
+  p.f16 = (contract & MG_CONTRACT_BASE_MASK) == MG_CONTRACT_ACCEL_F16 ? 1 : 0;
+  p.out16 = (contract & MG_OUT_16) ? 1 : 0;
   return p;
 }
+
+bool is_strict(int contract) {
+  return (contract & MG_CONTRACT_BASE_MASK) == MG_CONTRACT_STRICT_F32;
+}
+// Bytes per element of the inputs Q, K, V, dO and of the outputs O, dQ, dK, dV.
+size_t in_bytes(int contract) { return is_strict(contract) ? 4 : 2; }
+size_t out_bytes(int contract) { return (contract & MG_OUT_16) ? 2 : 4; }
 
 // kv_len (device array of B int32, may be null) must be 4-byte aligned and must
 // not overlap any output.
@@ -157,9 +172,17 @@ Range rng(const void *p, size_t bytes) {
 
 int map_cuda(cudaError_t e) { return e == cudaSuccess ? MG_OK : MG_ERR_CUDA; }
 
-size_t ws_bytes(int B, int H, int L) {
-  const size_t dvec = static_cast<size_t>(B) * H * L * sizeof(float);
-  return (dvec + 255) & ~static_cast<size_t>(255);
+size_t round256(size_t x) { return (x + 255) & ~static_cast<size_t>(255); }
+
+// Backward workspace: Dvec [B][H][Lq] f32, then for 16-bit outputs an f32 dQ
+// accumulator [B][H][Lq][D] (the reductions add in f32; one pass rounds it).
+size_t dvec_ws_bytes(int B, int H, int L) {
+  return round256(static_cast<size_t>(B) * H * L * sizeof(float));
+}
+size_t ws_bytes(int B, int H, int L, int D = 0, int contract = 0) {
+  size_t b = dvec_ws_bytes(B, H, L);
+  if (contract & MG_OUT_16) b += round256(static_cast<size_t>(B) * H * L * D * sizeof(float));
+  return b;
 }
 
 }  // namespace
@@ -233,16 +256,16 @@ int mg_attn_fwd_padded(const void *Q, const void *K, const void *V, void *O, flo
   if ((rc = check_kv_len(kv_len))) return rc;
   const size_t nq = static_cast<size_t>(B) * H * Lq * D;
   const size_t nk = static_cast<size_t>(B) * H * Lk * D;
-  const size_t in_el = contract == MG_CONTRACT_STRICT_F32 ? 4 : 2;
+  const size_t in_el = in_bytes(contract), out_el = out_bytes(contract);
   const Range in[] = {rng(Q, nq * in_el), rng(K, nk * in_el), rng(V, nk * in_el),
                       rng(kv_len, kv_len ? static_cast<size_t>(B) * 4 : 0)};
-  const Range out[] = {rng(O, nq * 4), rng(LSE, static_cast<size_t>(B) * H * Lq * 4)};
+  const Range out[] = {rng(O, nq * out_el), rng(LSE, static_cast<size_t>(B) * H * Lq * 4)};
   if ((rc = check_alias(in, 4, out, 2))) return rc;
 
-  const MgProblem p = make_problem(B, H, Lq, Lk, D, mask, scale, kv_len);
+  const MgProblem p = make_problem(B, H, Lq, Lk, D, mask, scale, kv_len, contract);
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   cudaError_t e;
-  if (contract == MG_CONTRACT_STRICT_F32) {
+  if (is_strict(contract)) {
     ProfScope ps(MGK_STRICT_FWD, st);
     e = mg_launch_strict_fwd(static_cast<const float *>(Q), static_cast<const float *>(K),
                              static_cast<const float *>(V), static_cast<float *>(O), LSE, p, st);
@@ -250,10 +273,7 @@ int mg_attn_fwd_padded(const void *Q, const void *K, const void *V, void *O, flo
     unsigned int *err = device_error_word();
     if (!err) return MG_ERR_CUDA;
     ProfScope ps(MGK_ACCEL_FWD, st);
-    e = mg_launch_accel_fwd(static_cast<const __nv_bfloat16 *>(Q),
-                            static_cast<const __nv_bfloat16 *>(K),
-                            static_cast<const __nv_bfloat16 *>(V), static_cast<float *>(O), LSE,
-                            p, err, st);
+    e = mg_launch_accel_fwd(Q, K, V, O, LSE, p, err, st);
   }
   return map_cuda(e);
 }
@@ -285,13 +305,14 @@ int mg_attn_fwd_decode(const void *Q, const void *K, const void *V, void *O, flo
   int rc = check_common(B, H, Lq, Lk, D, mask, scale, contract);
   if (rc) return rc;
   if (Lq > mg_decode_max_rows()) return MG_ERR_UNSUPPORTED;
+  if (contract & MG_OUT_16) return MG_ERR_UNSUPPORTED;  // O is f32 here
   const void *ptrs[] = {Q, K, V, O, LSE};
   if ((rc = check_ptrs(ptrs, 5))) return rc;
   const size_t need = mg_attn_fwd_decode_workspace_bytes(B, H, Lq, Lk, D, contract);
   if (!workspace || !aligned16(workspace) || workspace_bytes < need) return MG_ERR_WORKSPACE;
   const size_t nq = static_cast<size_t>(B) * H * Lq * D;
   const size_t nk = static_cast<size_t>(B) * H * Lk * D;
-  const size_t in_el = contract == MG_CONTRACT_STRICT_F32 ? 4 : 2;
+  const size_t in_el = in_bytes(contract);
   const Range in[] = {rng(Q, nq * in_el), rng(K, nk * in_el), rng(V, nk * in_el)};
   const Range out[] = {rng(O, nq * 4), rng(LSE, static_cast<size_t>(B) * H * Lq * 4),
                        rng(workspace, need)};
@@ -301,12 +322,12 @@ int mg_attn_fwd_decode(const void *Q, const void *K, const void *V, void *O, flo
   ProfScope ps(MGK_DECODE_FWD, st);
   return map_cuda(mg_launch_decode_fwd(Q, K, V, static_cast<float *>(O), LSE,
                                        static_cast<float *>(workspace), p,
-                                       contract == MG_CONTRACT_ACCEL_BF16, st));
+                                       contract & MG_CONTRACT_BASE_MASK, st));
 }
 
 size_t mg_attn_bwd_workspace_bytes_ex(int B, int H, int Lq, int Lk, int D, int contract) {
   if (check_common(B, H, Lq, Lk, D, MG_MASK_NONE, 1.f, contract) != MG_OK) return 0;
-  return ws_bytes(B, H, Lq);
+  return ws_bytes(B, H, Lq, D, contract);
 }
 
 size_t mg_attn_bwd_workspace_bytes(int B, int H, int L, int D, int contract) {
@@ -341,24 +362,24 @@ int mg_attn_bwd_padded(const void *Q, const void *K, const void *V, const void *
   const void *ptrs[] = {Q, K, V, O, dO, LSE, dQ, dK, dV};
   if ((rc = check_ptrs(ptrs, 9))) return rc;
   if ((rc = check_kv_len(kv_len))) return rc;
-  if (!workspace || !aligned16(workspace) || workspace_bytes < ws_bytes(B, H, Lq))
-    return MG_ERR_WORKSPACE;
+  const size_t need = ws_bytes(B, H, Lq, D, contract);
+  if (!workspace || !aligned16(workspace) || workspace_bytes < need) return MG_ERR_WORKSPACE;
   const size_t n = static_cast<size_t>(B) * H * Lq * D;   // Q, O, dO, dQ
   const size_t nk = static_cast<size_t>(B) * H * Lk * D;  // K, V, dK, dV
   const size_t rows = static_cast<size_t>(B) * H * Lq;
-  const size_t in_el = contract == MG_CONTRACT_STRICT_F32 ? 4 : 2;
+  const size_t in_el = in_bytes(contract), out_el = out_bytes(contract);
   const Range in[] = {rng(Q, n * in_el), rng(K, nk * in_el), rng(V, nk * in_el),
-                      rng(dO, n * in_el), rng(O, n * 4),      rng(LSE, rows * 4),
+                      rng(dO, n * in_el), rng(O, n * out_el), rng(LSE, rows * 4),
                       rng(kv_len, kv_len ? static_cast<size_t>(B) * 4 : 0)};
-  const Range out[] = {rng(dQ, n * 4), rng(dK, nk * 4), rng(dV, nk * 4),
-                       rng(workspace, ws_bytes(B, H, Lq))};
+  const Range out[] = {rng(dQ, n * out_el), rng(dK, nk * out_el), rng(dV, nk * out_el),
+                       rng(workspace, need)};
   if ((rc = check_alias(in, 7, out, 4))) return rc;
 
-  const MgProblem p = make_problem(B, H, Lq, Lk, D, mask, scale, kv_len);
+  const MgProblem p = make_problem(B, H, Lq, Lk, D, mask, scale, kv_len, contract);
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   float *Dvec = static_cast<float *>(workspace);
   cudaError_t e;
-  if (contract == MG_CONTRACT_STRICT_F32) {
+  if (is_strict(contract)) {
     {
       ProfScope ps(MGK_STRICT_DVEC, st);
       e = mg_launch_dvec_f32(static_cast<const float *>(O), static_cast<const float *>(dO), Dvec,
@@ -380,32 +401,35 @@ int mg_attn_bwd_padded(const void *Q, const void *K, const void *V, const void *
     if (!err) return MG_ERR_CUDA;
     {
       ProfScope ps(MGK_ACCEL_DVEC, st);
-      e = mg_launch_dvec_bf16(static_cast<const float *>(O),
-                              static_cast<const __nv_bfloat16 *>(dO), Dvec, p, st);
+      e = mg_launch_dvec_16(O, dO, Dvec, p, st);
     }
     if (e != cudaSuccess) return MG_ERR_CUDA;
-    const __nv_bfloat16 *q = static_cast<const __nv_bfloat16 *>(Q);
-    const __nv_bfloat16 *k = static_cast<const __nv_bfloat16 *>(K);
-    const __nv_bfloat16 *v = static_cast<const __nv_bfloat16 *>(V);
-    const __nv_bfloat16 *d = static_cast<const __nv_bfloat16 *>(dO);
     if (accel_dq_atomic()) {
+      // the reductions add into f32: the caller's dQ, or for 16-bit outputs an
+      // f32 accumulator in the workspace that one pass rounds into dQ at the end
+      float *dq_acc = p.out16 ? reinterpret_cast<float *>(static_cast<char *>(workspace) +
+                                                          dvec_ws_bytes(B, H, Lq))
+                              : static_cast<float *>(dQ);
       {
         ProfScope ps(MGK_DQ_ZERO, st);
-        e = cudaMemsetAsync(dQ, 0, n * 4, st);
+        e = cudaMemsetAsync(dq_acc, 0, n * 4, st);
       }
       if (e != cudaSuccess) return MG_ERR_CUDA;
-      ProfScope ps(MGK_ACCEL_DKDV_DQ, st);
-      e = mg_launch_accel_dkdv(q, k, v, d, LSE, Dvec, static_cast<float *>(dQ),
-                               static_cast<float *>(dK), static_cast<float *>(dV), p, err, st);
+      {
+        ProfScope ps(MGK_ACCEL_DKDV_DQ, st);
+        e = mg_launch_accel_dkdv(Q, K, V, dO, LSE, Dvec, dq_acc, dK, dV, p, err, st);
+      }
+      if (e != cudaSuccess || !p.out16) return map_cuda(e);
+      ProfScope ps(MGK_DQ_ROUND, st);
+      e = mg_launch_f32_to_16(dq_acc, dQ, n, p.f16 != 0, st);
     } else {
       {
         ProfScope ps(MGK_ACCEL_DKDV, st);
-        e = mg_launch_accel_dkdv_pp(q, k, v, d, LSE, Dvec, static_cast<float *>(dK),
-                                    static_cast<float *>(dV), p, err, st);
+        e = mg_launch_accel_dkdv_pp(Q, K, V, dO, LSE, Dvec, dK, dV, p, err, st);
       }
       if (e != cudaSuccess) return MG_ERR_CUDA;
       ProfScope ps(MGK_ACCEL_DQ, st);
-      e = mg_launch_accel_dq(q, k, v, d, LSE, Dvec, static_cast<float *>(dQ), p, err, st);
+      e = mg_launch_accel_dq(Q, K, V, dO, LSE, Dvec, dQ, p, err, st);
     }
   }
   return map_cuda(e);

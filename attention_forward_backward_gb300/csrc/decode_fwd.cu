@@ -16,6 +16,8 @@
 //   LSE = ln 2 (m + log2 l);  a row with no allowed key gets O = 0, LSE = -inf.
 #include <math.h>
 
+#include <cuda_fp16.h>
+
 #include "internal.h"
 
 namespace {
@@ -30,6 +32,7 @@ __device__ __forceinline__ float load_in(const float *p, size_t i) { return p[i]
 __device__ __forceinline__ float load_in(const __nv_bfloat16 *p, size_t i) {
   return __bfloat162float(p[i]);
 }
+__device__ __forceinline__ float load_in(const __half *p, size_t i) { return __half2float(p[i]); }
 
 // Eight consecutive input elements as raw registers (16-byte loads): fetched one
 // step ahead, widened to f32 registers when the step uses them.
@@ -58,6 +61,21 @@ template <> struct Raw8<__nv_bfloat16> {
     for (int k = 0; k < 4; ++k) {  // bf16 -> f32 is a 16-bit shift
       dst[2 * k] = __uint_as_float(w[k] << 16);
       dst[2 * k + 1] = __uint_as_float(w[k] & 0xffff0000u);
+    }
+  }
+};
+
+template <> struct Raw8<__half> {
+  uint4 u;
+  __device__ __forceinline__ void load(const __half *p) { u = *reinterpret_cast<const uint4 *>(p); }
+  __device__ __forceinline__ void zero() { u = make_uint4(0u, 0u, 0u, 0u); }
+  __device__ __forceinline__ void put(float *dst) const {
+    const unsigned w[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+      const float2 f = __half22float2(*reinterpret_cast<const __half2 *>(&w[k]));
+      dst[2 * k] = f.x;
+      dst[2 * k + 1] = f.y;
     }
   }
 };
@@ -336,28 +354,25 @@ size_t mg_decode_workspace_floats(const MgProblem &p) {
   return static_cast<size_t>(p.B) * p.H * S * p.L * (p.D + 4);
 }
 
+template <typename T>
+cudaError_t dispatch_d(const void *Q, const void *K, const void *V, float *O, float *LSE,
+                       float *part, const MgProblem &p, int S, int chunk, cudaStream_t st) {
+  const T *q = static_cast<const T *>(Q), *k = static_cast<const T *>(K),
+          *v = static_cast<const T *>(V);
+  switch (p.D) {
+    case 32: return launch_rows<32, T>(q, k, v, O, LSE, part, p, S, chunk, st);
+    case 64: return launch_rows<64, T>(q, k, v, O, LSE, part, p, S, chunk, st);
+    case 128: return launch_rows<128, T>(q, k, v, O, LSE, part, p, S, chunk, st);
+    default: return cudaErrorInvalidValue;
+  }
+}
+
 cudaError_t mg_launch_decode_fwd(const void *Q, const void *K, const void *V, float *O,
-                                 float *LSE, float *part, const MgProblem &p, bool bf16,
+                                 float *LSE, float *part, const MgProblem &p, int in_type,
                                  cudaStream_t st) {
   int S, chunk;
   mg_decode_split(p, &S, &chunk);
-  if (bf16) {
-    using T = __nv_bfloat16;
-    const T *q = static_cast<const T *>(Q), *k = static_cast<const T *>(K),
-            *v = static_cast<const T *>(V);
-    switch (p.D) {
-      case 32: return launch_rows<32, T>(q, k, v, O, LSE, part, p, S, chunk, st);
-      case 64: return launch_rows<64, T>(q, k, v, O, LSE, part, p, S, chunk, st);
-      case 128: return launch_rows<128, T>(q, k, v, O, LSE, part, p, S, chunk, st);
-      default: return cudaErrorInvalidValue;
-    }
-  }
-  const float *q = static_cast<const float *>(Q), *k = static_cast<const float *>(K),
-              *v = static_cast<const float *>(V);
-  switch (p.D) {
-    case 32: return launch_rows<32, float>(q, k, v, O, LSE, part, p, S, chunk, st);
-    case 64: return launch_rows<64, float>(q, k, v, O, LSE, part, p, S, chunk, st);
-    case 128: return launch_rows<128, float>(q, k, v, O, LSE, part, p, S, chunk, st);
-    default: return cudaErrorInvalidValue;
-  }
+  if (in_type == 1) return dispatch_d<__nv_bfloat16>(Q, K, V, O, LSE, part, p, S, chunk, st);
+  if (in_type == 2) return dispatch_d<__half>(Q, K, V, O, LSE, part, p, S, chunk, st);
+  return dispatch_d<float>(Q, K, V, O, LSE, part, p, S, chunk, st);
 }

@@ -20,6 +20,11 @@ struct MgProblem {
   // alignment, whose offset then follows the batch element's own key count.
   const int *kv_len = nullptr;
   int br = 0;
+  // ACCEL precision variants: f16 = 1 for f16 Q, K, V, dO (P and dS rounded to
+  // f16 as MMA operands) instead of bf16; out16 = 1 to store O, dQ, dK, dV in that
+  // 16-bit type instead of f32 (LSE stays f32).
+  int f16 = 0;
+  int out16 = 0;
 };
 
 // Key rows that one head (bh = b * H + h) attends to, and its causal offset:
@@ -52,7 +57,8 @@ enum MgKernelId {
   MGK_ACCEL_DKDV = 7,     // dK/dV kernel of the two-pass backward
   MGK_ACCEL_DQ = 8,       // dQ pass of the two-pass backward
   MGK_DECODE_FWD = 9,     // split-key forward for a few query rows (partials + merge)
-  MGK_COUNT = 10
+  MGK_DQ_ROUND = 10,      // f32 dQ accumulator rounded to the 16-bit output type
+  MGK_COUNT = 11
 };
 
 // Device error codes written into the device error word by bounded waits.
@@ -69,28 +75,29 @@ cudaError_t mg_launch_strict_dkdv(const float *Q, const float *K, const float *V
                                   float *dQ, float *dK, float *dV, const MgProblem &p,
                                   cudaStream_t st);
 
-// Dvec = rowsum(dO * O), dO in f32 or bf16.
+// Dvec = rowsum(dO * O): STRICT (f32 O and dO).
 cudaError_t mg_launch_dvec_f32(const float *O, const float *dO, float *Dvec, const MgProblem &p,
                                cudaStream_t st);
-cudaError_t mg_launch_dvec_bf16(const float *O, const __nv_bfloat16 *dO, float *Dvec,
-                                const MgProblem &p, cudaStream_t st);
+// ACCEL variants: dO bf16 or f16 (p.f16), O f32 or of dO's 16-bit type (p.out16).
+cudaError_t mg_launch_dvec_16(const void *O, const void *dO, float *Dvec, const MgProblem &p,
+                              cudaStream_t st);
 
 // ACCEL_BF16 (tcgen05 / TMEM / TMA) kernels. `err` is the device error word.
 // mg_launch_accel_dkdv: the fused kernel; it computes dK and dV and adds dQ
 // into a zeroed dQ (dQ must not be null).
-cudaError_t mg_launch_accel_fwd(const __nv_bfloat16 *Q, const __nv_bfloat16 *K,
-                                const __nv_bfloat16 *V, float *O, float *LSE,
+// Q, K, V (and dO) are bf16 or f16 (p.f16); O is f32 or 16-bit (p.out16).
+cudaError_t mg_launch_accel_fwd(const void *Q, const void *K, const void *V, void *O, float *LSE,
                                 const MgProblem &p, unsigned int *err, cudaStream_t st);
-cudaError_t mg_launch_accel_dkdv(const __nv_bfloat16 *Q, const __nv_bfloat16 *K,
-                                 const __nv_bfloat16 *V, const __nv_bfloat16 *dO,
-                                 const float *LSE, const float *Dvec, float *dQ, float *dK,
-                                 float *dV, const MgProblem &p, unsigned int *err,
+// dQ is always f32 here (the caller's dQ, or an f32 accumulator for 16-bit
+// outputs); dK, dV are f32 or 16-bit (p.out16).
+cudaError_t mg_launch_accel_dkdv(const void *Q, const void *K, const void *V, const void *dO,
+                                 const float *LSE, const float *Dvec, float *dQ, void *dK,
+                                 void *dV, const MgProblem &p, unsigned int *err,
                                  cudaStream_t st);
 
 // dK/dV kernel of the two-pass backward: two query blocks in flight per CTA.
-cudaError_t mg_launch_accel_dkdv_pp(const __nv_bfloat16 *Q, const __nv_bfloat16 *K,
-                                    const __nv_bfloat16 *V, const __nv_bfloat16 *dO,
-                                    const float *LSE, const float *Dvec, float *dK, float *dV,
+cudaError_t mg_launch_accel_dkdv_pp(const void *Q, const void *K, const void *V, const void *dO,
+                                    const float *LSE, const float *Dvec, void *dK, void *dV,
                                     const MgProblem &p, unsigned int *err, cudaStream_t st);
 
 // Limit of every bounded wait in the tensor-core kernels, in ns: the environment
@@ -102,8 +109,9 @@ uint64_t mg_wait_limit_ns();
 int mg_decode_max_rows();
 void mg_decode_split(const MgProblem &p, int *S, int *chunk);
 size_t mg_decode_workspace_floats(const MgProblem &p);
+// in_type: 0 f32, 1 bf16, 2 f16 inputs (the contract's base value).
 cudaError_t mg_launch_decode_fwd(const void *Q, const void *K, const void *V, float *O,
-                                 float *LSE, float *part, const MgProblem &p, bool bf16,
+                                 float *LSE, float *part, const MgProblem &p, int in_type,
                                  cudaStream_t st);
 
 // The argument checks every compute call starts with (sizes, mask, scale,
@@ -117,8 +125,12 @@ int mg_sm_count();
 // Opt a kernel into more than 48 KB of dynamic shared memory once per device.
 cudaError_t mg_set_smem_attr(const void *func, int bytes, int slot);
 
-// ACCEL_BF16 dQ pass (one CTA per 128-row query block; dQ stored, not reduced).
-cudaError_t mg_launch_accel_dq(const __nv_bfloat16 *Q, const __nv_bfloat16 *K,
-                               const __nv_bfloat16 *V, const __nv_bfloat16 *dO, const float *LSE,
-                               const float *Dvec, float *dQ, const MgProblem &p,
+// ACCEL dQ pass (one CTA per 128-row query block; dQ stored, not reduced: f32
+// or 16-bit by p.out16).
+cudaError_t mg_launch_accel_dq(const void *Q, const void *K, const void *V, const void *dO,
+                               const float *LSE, const float *Dvec, void *dQ, const MgProblem &p,
                                unsigned int *err, cudaStream_t st);
+
+// dst (16-bit, bf16 or f16 by `f16`) = src (f32), n elements (n % 4 == 0).
+cudaError_t mg_launch_f32_to_16(const float *src, void *dst, size_t n, bool f16,
+                                cudaStream_t st);

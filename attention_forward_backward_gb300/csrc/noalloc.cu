@@ -67,6 +67,8 @@ extern "C" int mg_attn_bwd_noalloc(const void *Q, const void *K, const void *V, 
   if (causal != 0 && causal != 1) return MG_ERR_INVALID_ARG;
   int rc = mg_check_args(B, H, L, L, D, causal ? MG_MASK_CAUSAL : MG_MASK_NONE, scale, contract);
   if (rc != MG_OK) return rc;
+  // the fixed array holds Dvec only, not the f32 dQ accumulator of 16-bit outputs
+  if (contract & MG_OUT_16) return MG_ERR_UNSUPPORTED;
   const void *ptrs[] = {Q, K, V, O, dO, LSE, dQ, dK, dV};
   for (const void *p : ptrs)
     if (!p || (reinterpret_cast<uintptr_t>(p) & 15u) != 0) return MG_ERR_INVALID_ARG;

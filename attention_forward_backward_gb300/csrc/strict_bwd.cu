@@ -18,6 +18,10 @@
 // in registers; dQ_tile = scale dS K is added to global dQ. Thread (ty, tx)
 // owns keys ty + 16 a (a < 4), queries tx + 16 b (b < 4) of the score tiles and
 // output columns VW*tx + 16*VW*v of dK, dV and the dQ tile.
+#include <cuda_fp16.h>
+
+#include <type_traits>
+
 #include "internal.h"
 #include "strict_common.cuh"
 
@@ -269,9 +273,27 @@ __global__ void __launch_bounds__(256, 1)
   }
 }
 
-// Dvec_i = sum_d dO_id O_id. G = D/4 threads per row, float4 loads of O.
-template <int D, typename TdO>
-__global__ void __launch_bounds__(256) dvec_kernel(const float *__restrict__ O,
+// Four consecutive elements widened to f32 (8- or 16-byte loads).
+__device__ __forceinline__ void load4(const float *p, float (&g)[4]) {
+  const float4 d = *reinterpret_cast<const float4 *>(p);
+  g[0] = d.x; g[1] = d.y; g[2] = d.z; g[3] = d.w;
+}
+__device__ __forceinline__ void load4(const __nv_bfloat16 *p, float (&g)[4]) {
+  const uint2 raw = *reinterpret_cast<const uint2 *>(p);
+  const float2 a = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(&raw.x));
+  const float2 b = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(&raw.y));
+  g[0] = a.x; g[1] = a.y; g[2] = b.x; g[3] = b.y;
+}
+__device__ __forceinline__ void load4(const __half *p, float (&g)[4]) {
+  const uint2 raw = *reinterpret_cast<const uint2 *>(p);
+  const float2 a = __half22float2(*reinterpret_cast<const __half2 *>(&raw.x));
+  const float2 b = __half22float2(*reinterpret_cast<const __half2 *>(&raw.y));
+  g[0] = a.x; g[1] = a.y; g[2] = b.x; g[3] = b.y;
+}
+
+// Dvec_i = sum_d dO_id O_id. G = D/4 threads per row, 4 elements per thread.
+template <int D, typename TO, typename TdO>
+__global__ void __launch_bounds__(256) dvec_kernel(const TO *__restrict__ O,
                                                    const TdO *__restrict__ dO,
                                                    float *__restrict__ Dvec, long long rows) {
   constexpr int G = D / 4;
@@ -279,27 +301,34 @@ __global__ void __launch_bounds__(256) dvec_kernel(const float *__restrict__ O,
   const int lane = threadIdx.x % G;
   float acc = 0.f;
   if (row < rows) {
-    const float4 o = *reinterpret_cast<const float4 *>(O + row * D + lane * 4);
-    float g[4];
-    if constexpr (sizeof(TdO) == 4) {
-      const float4 d = *reinterpret_cast<const float4 *>(
-          reinterpret_cast<const float *>(dO) + row * D + lane * 4);
-      g[0] = d.x; g[1] = d.y; g[2] = d.z; g[3] = d.w;
-    } else {
-      const uint2 raw = *reinterpret_cast<const uint2 *>(
-          reinterpret_cast<const __nv_bfloat16 *>(dO) + row * D + lane * 4);
-      const __nv_bfloat162 lo = *reinterpret_cast<const __nv_bfloat162 *>(&raw.x);
-      const __nv_bfloat162 hi = *reinterpret_cast<const __nv_bfloat162 *>(&raw.y);
-      const float2 a = __bfloat1622float2(lo), b = __bfloat1622float2(hi);
-      g[0] = a.x; g[1] = a.y; g[2] = b.x; g[3] = b.y;
-    }
-    acc = o.x * g[0];
-    acc = fmaf(o.y, g[1], acc);
-    acc = fmaf(o.z, g[2], acc);
-    acc = fmaf(o.w, g[3], acc);
+    float o[4], g[4];
+    load4(O + row * D + lane * 4, o);
+    load4(dO + row * D + lane * 4, g);
+    acc = o[0] * g[0];
+    acc = fmaf(o[1], g[1], acc);
+    acc = fmaf(o[2], g[2], acc);
+    acc = fmaf(o[3], g[3], acc);
   }
   acc = group_sum<G>(acc);
   if (row < rows && lane == 0) Dvec[row] = acc;
+}
+
+// dst = src rounded (RNE) to a 16-bit type, 4 elements per thread.
+template <typename T16>
+__global__ void __launch_bounds__(256) f32_to_16_kernel(const float *__restrict__ src,
+                                                        T16 *__restrict__ dst, size_t n4) {
+  const size_t i = static_cast<size_t>(blockIdx.x) * 256 + threadIdx.x;
+  if (i >= n4) return;
+  const float4 v = reinterpret_cast<const float4 *>(src)[i];
+  uint2 out;
+  if constexpr (sizeof(T16) == 2 && std::is_same<T16, __half>::value) {
+    __half2 a = __floats2half2_rn(v.x, v.y), b = __floats2half2_rn(v.z, v.w);
+    out = make_uint2(*reinterpret_cast<uint32_t *>(&a), *reinterpret_cast<uint32_t *>(&b));
+  } else {
+    __nv_bfloat162 a = __floats2bfloat162_rn(v.x, v.y), b = __floats2bfloat162_rn(v.z, v.w);
+    out = make_uint2(*reinterpret_cast<uint32_t *>(&a), *reinterpret_cast<uint32_t *>(&b));
+  }
+  reinterpret_cast<uint2 *>(dst)[i] = out;
 }
 
 template <int D>
@@ -320,18 +349,18 @@ cudaError_t launch_dkdv(const float *Q, const float *K, const float *V, const fl
   return cudaGetLastError();
 }
 
-template <int D, typename TdO>
-cudaError_t launch_dvec(const float *O, const TdO *dO, float *Dvec, const MgProblem &p,
+template <int D, typename TO, typename TdO>
+cudaError_t launch_dvec(const TO *O, const TdO *dO, float *Dvec, const MgProblem &p,
                         cudaStream_t st) {
   const long long rows = static_cast<long long>(p.B) * p.H * p.L;
   const long long threads = rows * (D / 4);
   const long long blocks = (threads + 255) / 256;
-  dvec_kernel<D, TdO><<<static_cast<unsigned>(blocks), 256, 0, st>>>(O, dO, Dvec, rows);
+  dvec_kernel<D, TO, TdO><<<static_cast<unsigned>(blocks), 256, 0, st>>>(O, dO, Dvec, rows);
   return cudaGetLastError();
 }
 
-template <typename TdO>
-cudaError_t dvec_dispatch(const float *O, const TdO *dO, float *Dvec, const MgProblem &p,
+template <typename TO, typename TdO>
+cudaError_t dvec_dispatch(const TO *O, const TdO *dO, float *Dvec, const MgProblem &p,
                           cudaStream_t st) {
   switch (p.D) {
     case 32: return launch_dvec<32>(O, dO, Dvec, p, st);
@@ -357,10 +386,32 @@ cudaError_t mg_launch_strict_dkdv(const float *Q, const float *K, const float *V
 
 cudaError_t mg_launch_dvec_f32(const float *O, const float *dO, float *Dvec, const MgProblem &p,
                                cudaStream_t st) {
-  return dvec_dispatch<float>(O, dO, Dvec, p, st);
+  return dvec_dispatch(O, dO, Dvec, p, st);
 }
 
-cudaError_t mg_launch_dvec_bf16(const float *O, const __nv_bfloat16 *dO, float *Dvec,
-                                const MgProblem &p, cudaStream_t st) {
-  return dvec_dispatch<__nv_bfloat16>(O, dO, Dvec, p, st);
+
+cudaError_t mg_launch_dvec_16(const void *O, const void *dO, float *Dvec, const MgProblem &p,
+                              cudaStream_t st) {
+  if (p.f16) {
+    const __half *d = static_cast<const __half *>(dO);
+    if (p.out16) return dvec_dispatch(static_cast<const __half *>(O), d, Dvec, p, st);
+    return dvec_dispatch(static_cast<const float *>(O), d, Dvec, p, st);
+  }
+  const __nv_bfloat16 *d = static_cast<const __nv_bfloat16 *>(dO);
+  if (p.out16) return dvec_dispatch(static_cast<const __nv_bfloat16 *>(O), d, Dvec, p, st);
+  return dvec_dispatch(static_cast<const float *>(O), d, Dvec, p, st);
+}
+
+cudaError_t mg_launch_f32_to_16(const float *src, void *dst, size_t n, bool f16,
+                                cudaStream_t st) {
+  if (n % 4) return cudaErrorInvalidValue;
+  const size_t n4 = n / 4;
+  if (n4 == 0) return cudaSuccess;
+  const unsigned blocks = static_cast<unsigned>((n4 + 255) / 256);
+  if (f16)
+    f32_to_16_kernel<__half><<<blocks, 256, 0, st>>>(src, static_cast<__half *>(dst), n4);
+  else
+    f32_to_16_kernel<__nv_bfloat16>
+        <<<blocks, 256, 0, st>>>(src, static_cast<__nv_bfloat16 *>(dst), n4);
+  return cudaGetLastError();
 }

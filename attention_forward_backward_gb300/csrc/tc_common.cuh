@@ -13,6 +13,7 @@
 
 #include <cuda.h>
 #include <cuda_bf16.h>
+#include <cuda_fp16.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
 
@@ -297,12 +298,17 @@ __device__ __forceinline__ uint64_t sdesc_add(uint64_t desc, uint32_t byte_off) 
   return desc + (byte_off >> 4);
 }
 
-// Instruction descriptor of kind::f16 with bf16 A and B, f32 accumulator.
+// Instruction descriptor of kind::f16 with an f32 accumulator and A, B both
+// bf16 (f16 = false) or both f16 (f16 = true; one MMA never mixes the two).
 // a_mn / b_mn select MN-major (transposed) operands; M in {64,128}, N % 16 == 0.
+__host__ __device__ constexpr uint32_t idesc_16_f32(int M, int N, bool a_mn, bool b_mn,
+                                                    bool f16) {
+  return (1u << 4) | ((f16 ? 0u : 1u) << 7) | ((f16 ? 0u : 1u) << 10) |
+         ((a_mn ? 1u : 0u) << 15) | ((b_mn ? 1u : 0u) << 16) |
+         (static_cast<uint32_t>(N >> 3) << 17) | (static_cast<uint32_t>(M >> 4) << 24);
+}
 __host__ __device__ constexpr uint32_t idesc_bf16_f32(int M, int N, bool a_mn, bool b_mn) {
-  return (1u << 4) | (1u << 7) | (1u << 10) | ((a_mn ? 1u : 0u) << 15) |
-         ((b_mn ? 1u : 0u) << 16) | (static_cast<uint32_t>(N >> 3) << 17) |
-         (static_cast<uint32_t>(M >> 4) << 24);
+  return idesc_16_f32(M, N, a_mn, b_mn, false);
 }
 
 __device__ __forceinline__ float ex2(float x) {
@@ -314,6 +320,30 @@ __device__ __forceinline__ float ex2(float x) {
 __device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
   __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
   return *reinterpret_cast<uint32_t *>(&v);
+}
+__device__ __forceinline__ uint32_t pack_f16(float lo, float hi) {
+  __half2 v = __floats2half2_rn(lo, hi);
+  return *reinterpret_cast<uint32_t *>(&v);
+}
+// Two f32 values rounded (RNE) to the MMA operand type and packed low-first.
+template <bool F16>
+__device__ __forceinline__ uint32_t pack16(float lo, float hi) {
+  return F16 ? pack_f16(lo, hi) : pack_bf16(lo, hi);
+}
+// Four f32 values rounded to the 16-bit output type, as 8 bytes (low first).
+template <bool F16>
+__device__ __forceinline__ uint2 pack16x4(float a, float b, float c, float d) {
+  return make_uint2(pack16<F16>(a, b), pack16<F16>(c, d));
+}
+// Four consecutive values to element idx (a multiple of 4) of a row-major
+// output that is f32 (out16 = 0) or of the 16-bit operand type (out16 = 1).
+template <bool F16>
+__device__ __forceinline__ void store4(void *out, int out16, size_t idx, float a, float b,
+                                       float c, float d) {
+  if (out16)
+    *reinterpret_cast<uint2 *>(static_cast<uint16_t *>(out) + idx) = pack16x4<F16>(a, b, c, d);
+  else
+    *reinterpret_cast<float4 *>(static_cast<float *>(out) + idx) = make_float4(a, b, c, d);
 }
 
 }  // namespace mg_tc

@@ -47,6 +47,12 @@ cudaError_t mg_tmap_bf16(CUtensorMap *m, const void *ptr, int D, int L, int BH, 
   return encode(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, ptr, D, L, BH, 64, box_rows);
 }
 
+cudaError_t mg_tmap_16(CUtensorMap *m, const void *ptr, int D, int L, int BH, int box_rows,
+                       bool f16) {
+  return encode(m, f16 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2,
+                ptr, D, L, BH, 64, box_rows);
+}
+
 cudaError_t mg_tmap_f32(CUtensorMap *m, const void *ptr, int D, int L, int BH, int box_rows) {
   return encode(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, ptr, D, L, BH, 32, box_rows);
 }

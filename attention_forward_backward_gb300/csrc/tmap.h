@@ -12,5 +12,9 @@
 
 // bf16 tensor, boxes of 64 columns x box_rows rows, 128-byte swizzle.
 cudaError_t mg_tmap_bf16(CUtensorMap *m, const void *ptr, int D, int L, int BH, int box_rows);
+// bf16 (f16 = false) or f16 tensor, boxes of 64 columns x box_rows rows,
+// 128-byte swizzle.
+cudaError_t mg_tmap_16(CUtensorMap *m, const void *ptr, int D, int L, int BH, int box_rows,
+                       bool f16);
 // f32 tensor, boxes of 32 columns x box_rows rows, 128-byte swizzle (dQ reduce).
 cudaError_t mg_tmap_f32(CUtensorMap *m, const void *ptr, int D, int L, int BH, int box_rows);

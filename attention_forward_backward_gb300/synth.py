@@ -75,6 +75,38 @@ def bf16_bits_to_f32(bits: np.ndarray) -> np.ndarray:
     return (np.asarray(bits, dtype=np.uint16).astype(np.uint32) << np.uint32(16)).view(np.float32)
 
 
+def round_to_f16(x: np.ndarray) -> np.ndarray:
+    """Round float32 to the nearest IEEE half (ties to even, numpy's conversion);
+    returns the uint16 bit patterns."""
+    return np.ascontiguousarray(x, dtype=np.float32).astype(np.float16).view(np.uint16)
+
+
+def f16_bits_to_f32(bits: np.ndarray) -> np.ndarray:
+    return np.asarray(bits, dtype=np.uint16).view(np.float16).astype(np.float32)
+
+
+def base_contract(contract: str) -> str:
+    """"strict", "accel" or "accel_f16": the input format of a contract name
+    ("+out16" and other suffixes name output options, not input formats)."""
+    return contract.split("+")[0]
+
+
+def encode(x: np.ndarray, contract: str):
+    """Host input in the contract's format: f32 array (strict), or the 16-bit bit
+    patterns (key "bits") with their exact float32 values (key "values") that the
+    oracle consumes: bf16 (accel) or f16 (accel_f16), rounded to nearest even."""
+    c = base_contract(contract)
+    if c == "strict":
+        return x
+    if c == "accel":
+        bits = round_to_bf16(x)
+        return {"bits": bits, "values": bf16_bits_to_f32(bits)}
+    if c == "accel_f16":
+        bits = round_to_f16(x)
+        return {"bits": bits, "values": f16_bits_to_f32(bits)}
+    raise ValueError(contract)
+
+
 @dataclass(frozen=True)
 class Workload:
     """One seeded attention workload. Shapes are [B, H, L, D] row-major."""
@@ -135,20 +167,11 @@ def tensor_f32(w: Workload, which: str) -> np.ndarray:
 def inputs(w: Workload, contract: str):
     """Dict of host inputs for a contract.
 
-    strict -> float32 arrays. accel -> uint16 bf16 bit patterns (key "bits")
-    plus their exact float32 values (key "values"), which the oracle consumes.
+    strict -> float32 arrays. accel (accel_f16) -> uint16 bf16 (f16) bit
+    patterns (key "bits") plus their exact float32 values (key "values"), which
+    the oracle consumes.
     """
-    out = {}
-    for t in ("Q", "K", "V", "dO"):
-        x = tensor_f32(w, t)
-        if contract == "strict":
-            out[t] = x
-        elif contract == "accel":
-            bits = round_to_bf16(x)
-            out[t] = {"bits": bits, "values": bf16_bits_to_f32(bits)}
-        else:
-            raise ValueError(contract)
-    return out
+    return {t: encode(tensor_f32(w, t), contract) for t in ("Q", "K", "V", "dO")}
 
 
 def custom_workload(B, H, L, D, causal, seed_cfg=900, qk_gain=1.0) -> Workload:
@@ -165,11 +188,5 @@ def cross_inputs(B, H, Lq, Lk, D, contract: str, seed_cfg: int = 950):
     for t in ("Q", "K", "V", "dO"):
         rows = Lq if t in ("Q", "dO") else Lk
         x = normal_f32(1000 * seed_cfg + TENSOR_IDS[t], B * H * rows * D).reshape(B, H, rows, D)
-        if contract == "strict":
-            out[t] = x
-        elif contract == "accel":
-            bits = round_to_bf16(x)
-            out[t] = {"bits": bits, "values": bf16_bits_to_f32(bits)}
-        else:
-            raise ValueError(contract)
+        out[t] = encode(x, contract)
     return out

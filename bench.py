@@ -159,13 +159,14 @@ def summarize_clocks(lines):
 def make_inputs(w, contract, torch, device):
     host = {}
     dev = {}
+    base = synth.base_contract(contract)
     for t in ("Q", "K", "V", "dO"):
-        x = synth.tensor_f32(w, t)
-        if contract == "strict":
+        x = synth.encode(synth.tensor_f32(w, t), contract)
+        if base == "strict":
             h = torch.from_numpy(x)
         else:
-            bits = synth.round_to_bf16(x).view(np.int16)
-            h = torch.from_numpy(bits).view(torch.bfloat16)
+            dt = torch.float16 if base == "accel_f16" else torch.bfloat16
+            h = torch.from_numpy(np.ascontiguousarray(x["bits"]).view(np.int16)).view(dt)
         host[t] = h.pin_memory()
         dev[t] = host[t].to(device, non_blocking=False)
     return host, dev
@@ -358,20 +359,25 @@ def run_e2e(mg, torch, w, contract, args, host, device, stream, flops_step):
 
 def run_small_configs(mg, torch, device, stream, peaks, sm_count, steps: int, warmup: int):
     """fwd and fwd+bwd TFLOP/s of the four smaller seeded configurations for
-    every contract each one lists (CUDA events on the call stream, L2 flushed
-    between timed steps, median step): the compact ``configs`` object of the
-    default JSON line, so that those numbers come from the same run."""
+    every contract each one lists, and of the accelerated contract's precision
+    variants (f16 inputs, 16-bit outputs) on the benchmark workload (CUDA events
+    on the call stream, L2 flushed between timed steps, median step): the compact
+    ``configs`` object of the default JSON line, so that those numbers come from
+    the same run."""
     out = {}
     f32 = torch.float32
     flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=f32, device=device)
     s = stream.cuda_stream
-    for cfg in (1, 2, 3, 4):
+    plan = [(cfg, synth.WORKLOADS[cfg].contracts) for cfg in (1, 2, 3, 4)]
+    # the precision variants of the accelerated contract on the benchmark workload
+    plan.append((5, ("accel_f16", "accel+out16", "accel_f16+out16")))
+    for cfg, contracts in plan:
         w = synth.WORKLOADS[cfg]
         B, H, L, D = w.shape
-        row = {"workload": w.name}
-        for c in w.contracts:
+        row = out.get(str(cfg), {"workload": w.name})
+        for c in contracts:
             _, dev = make_inputs(w, c, torch, device)
-            O = torch.empty((B, H, L, D), dtype=f32, device=device)
+            O = torch.empty((B, H, L, D), dtype=mg._out_dtype(c), device=device)
             LSE = torch.empty((B, H, L), dtype=f32, device=device)
             dQ, dK, dV = (torch.empty_like(O) for _ in range(3))
             ws = torch.empty(mg.mg_attn_bwd_workspace_bytes(B, H, L, D, c), dtype=torch.uint8,
@@ -395,12 +401,13 @@ def run_small_configs(mg, torch, device, stream, peaks, sm_count, steps: int, wa
                 raise RuntimeError(f"cfg {cfg} {c}: device error word set")
             fm = statistics.median(x.elapsed_time(y) for x, y in fwd_ms)
             tm = statistics.median(x.elapsed_time(y) for x, y in tot_ms)
-            if c == "accel":
-                peak = peaks["bf16_tflops"]
+            if c != "strict":
+                peak = peaks["bf16_tflops"]  # f16 and bf16 share the dense tensor rate
             else:
                 peak = fp32_simt_peak_tflops(sm_count, peaks["sm_max_mhz"])
             tf = (w.flops_fwd() + w.flops_bwd()) / (tm * 1e-3) / 1e12
-            row["accel_bf16" if c == "accel" else "strict_f32"] = {
+            key = {"accel": "accel_bf16", "strict": "strict_f32"}.get(c, c.replace("+", "_"))
+            row[key] = {
                 "fwd_bwd_tflops": round(tf, 2),
                 "fwd_tflops": round(w.flops_fwd() / (fm * 1e-3) / 1e12, 2),
                 "step_ms_median": round(tm, 4), "frac_of_peak_fwd_bwd": round(tf / peak, 4)}

@@ -30,6 +30,23 @@
  *                           accumulation in tensor memory; P (forward and dV)
  *                           and dS (dK, dQ) are rounded to bf16 (RNE) as MMA
  *                           operands, everything else stays f32.
+ *   MG_CONTRACT_ACCEL_F16   the same with f16 in place of bf16: the 16-bit
+ *                           format the pages' accelerated path rounds its matrix
+ *                           inputs to (Section 4.2). f16 has 10 mantissa bits
+ *                           (bf16: 7) but a narrow range: P and dS below 2^-24
+ *                           round to zero as MMA operands, the underflow that
+ *                           the pages' precision bit guards derivative regions
+ *                           against (Section 3.1); ACCEL_BF16, with f32's
+ *                           range, cannot underflow there.
+ * Flag OR-ed into an ACCEL contract:
+ *   MG_OUT_16               O, dQ, dK, dV are stored in the inputs' 16-bit type
+ *                           (bf16 or f16, RNE) instead of f32; LSE stays f32, and
+ *                           every accumulation stays f32 (dQ's reductions add
+ *                           into an f32 accumulator in the backward's workspace,
+ *                           rounded once at the end). The backward then reads
+ *                           O in that 16-bit type. Not valid with STRICT_F32
+ *                           (MG_ERR_UNSUPPORTED), the decode forward or the
+ *                           no-allocation backward.
  *
  * Layout. Q, K, V, O, dO, dQ, dK, dV are dense row-major [B][H][L][D] (D
  * innermost, no padding, no strides). LSE (and the workspace's Dvec) are
@@ -78,7 +95,10 @@ extern "C" {
 
 typedef enum {
   MG_CONTRACT_STRICT_F32 = 0,
-  MG_CONTRACT_ACCEL_BF16 = 1
+  MG_CONTRACT_ACCEL_BF16 = 1,
+  MG_CONTRACT_ACCEL_F16 = 2,
+  MG_CONTRACT_BASE_MASK = 0xff, /* the base contract is contract & MG_CONTRACT_BASE_MASK */
+  MG_OUT_16 = 0x100             /* flag: 16-bit O, dQ, dK, dV (see above) */
 } mg_contract_t;
 
 typedef enum {
@@ -99,8 +119,8 @@ typedef enum {
 /*
  * Forward: O = softmax(scale * Q K^T + causal mask) V and LSE (natural log).
  * Tiled attention forward archetype (Section 3.3 of the paper).
- *   Q, K, V  in   [B][H][L][D]; f32 (STRICT) or bf16 (ACCEL)
- *   O        out  [B][H][L][D] f32 (both contracts), overwritten
+ *   Q, K, V  in   [B][H][L][D]; f32 (STRICT), bf16 or f16 (ACCEL_BF16, ACCEL_F16)
+ *   O        out  [B][H][L][D] f32 (16-bit with MG_OUT_16), overwritten
  *   LSE      out  [B][H][L] f32, overwritten; the backward requires it
  */
 int mg_attn_fwd(const void *Q, const void *K, const void *V, void *O, float *LSE,
@@ -117,18 +137,21 @@ int mg_attn_fwd_ex(const void *Q, const void *K, const void *V, void *O, float *
                    int B, int H, int Lq, int Lk, int D, int mask, float scale, int contract,
                    void *stream);
 
-/* Bytes of device workspace mg_attn_bwd needs for this shape (holds Dvec,
- * [B][H][L] f32, rounded up to 256 bytes). 0 for invalid arguments. */
+/* Bytes of device workspace mg_attn_bwd needs for this shape and contract:
+ * Dvec, [B][H][L] f32, rounded up to 256 bytes; with MG_OUT_16 also an f32 dQ
+ * accumulator [B][H][L][D], rounded up to 256 bytes. 0 for invalid arguments. */
 size_t mg_attn_bwd_workspace_bytes(int B, int H, int L, int D, int contract);
 
 /*
  * Backward: dQ, dK, dV of loss = sum(dO * O), given the forward's O and LSE.
  * dQ and fused dK+dV archetypes (Sections 3.3 and 8 of the paper); the
  * derivative region keeps f32 accumulation (Sections 3.1 and 4.2).
- *   Q, K, V, dO  in   [B][H][L][D]; f32 (STRICT) or bf16 (ACCEL)
- *   O            in   [B][H][L][D] f32, as written by mg_attn_fwd
+ *   Q, K, V, dO  in   [B][H][L][D]; f32 (STRICT), bf16 or f16 (ACCEL_BF16, ACCEL_F16)
+ *   O            in   [B][H][L][D] as written by mg_attn_fwd (f32, or 16-bit with
+ *                     MG_OUT_16)
  *   LSE          in   [B][H][L] f32, as written by mg_attn_fwd
- *   dQ, dK, dV   out  [B][H][L][D] f32, overwritten (never accumulated into)
+ *   dQ, dK, dV   out  [B][H][L][D] f32 (16-bit with MG_OUT_16), overwritten (never
+ *                     accumulated into)
  *   workspace    scratch of at least mg_attn_bwd_workspace_bytes() bytes,
  *                16-byte aligned; its contents on entry do not matter
  * Steps on the stream: Dvec = rowsum(dO * O) into the workspace; then one
@@ -144,8 +167,9 @@ int mg_attn_bwd(const void *Q, const void *K, const void *V, const void *O,
                 int B, int H, int L, int D, int causal, float scale, int contract,
                 void *workspace, size_t workspace_bytes, void *stream);
 
-/* Workspace bytes for mg_attn_bwd_ex (Dvec is [B][H][Lq] f32, rounded up to
- * 256 bytes). 0 for invalid arguments. */
+/* Workspace bytes for mg_attn_bwd_ex (Dvec is [B][H][Lq] f32, and with
+ * MG_OUT_16 a [B][H][Lq][D] f32 dQ accumulator, each rounded up to 256 bytes).
+ * 0 for invalid arguments. */
 size_t mg_attn_bwd_workspace_bytes_ex(int B, int H, int Lq, int Lk, int D, int contract);
 
 /*

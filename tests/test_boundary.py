@@ -76,7 +76,9 @@ def bwd(lib, Q=P(0), K=P(1), V=P(2), O=P(3), dO=P(4), LSE=P(5), dQ=P(6), dK=P(7)
     (dict(scale=-1.0), mg.MG_ERR_INVALID_ARG),
     (dict(scale=float("nan")), mg.MG_ERR_INVALID_ARG),
     (dict(scale=float("inf")), mg.MG_ERR_INVALID_ARG),
-    (dict(contract=2), mg.MG_ERR_INVALID_ARG),
+    (dict(contract=3), mg.MG_ERR_INVALID_ARG),
+    (dict(contract=0x200 | 1), mg.MG_ERR_INVALID_ARG),  # unknown flag
+    (dict(contract=0x100), mg.MG_ERR_UNSUPPORTED),      # 16-bit outputs under STRICT_F32
     (dict(O=P(0)), mg.MG_ERR_INVALID_ARG),          # output aliases Q
     (dict(LSE=P(3) + 1024), mg.MG_ERR_INVALID_ARG),  # LSE inside O
 ])
@@ -202,7 +204,8 @@ def fwd_decode(lib, Q=P(0), K=P(1), V=P(2), O=P(3), LSE=P(4), B=1, H=2, Lq=4, Lk
     (dict(D=48), mg.MG_ERR_UNSUPPORTED),
     (dict(mask=3), mg.MG_ERR_INVALID_ARG),
     (dict(scale=0.0), mg.MG_ERR_INVALID_ARG),
-    (dict(contract=2), mg.MG_ERR_INVALID_ARG),
+    (dict(contract=3), mg.MG_ERR_INVALID_ARG),
+    (dict(contract=0x100 | 1), mg.MG_ERR_UNSUPPORTED),  # decode writes O in f32 only
     (dict(ws=None), mg.MG_ERR_WORKSPACE),
     (dict(ws=P(5) + 8), mg.MG_ERR_WORKSPACE),        # misaligned workspace
     (dict(ws_bytes=16), mg.MG_ERR_WORKSPACE),
@@ -270,3 +273,35 @@ def test_fwd_padded_rejects(lib, kw, code):
 ])
 def test_bwd_padded_rejects(lib, kw, code):
     assert bwd_pad(lib, **kw) == code
+
+
+def test_workspace_bytes_with_16_bit_outputs(lib):
+    """MG_OUT_16 adds an f32 dQ accumulator [B][H][Lq][D] after Dvec, each part
+    rounded up to 256 bytes: B=1, H=2, Lq=100, D=64 -> 1024 + 51200 bytes."""
+    dvec = lib.mg_attn_bwd_workspace_bytes_ex(1, 2, 100, 70, 64, 1)
+    assert dvec == 1024
+    assert lib.mg_attn_bwd_workspace_bytes_ex(1, 2, 100, 70, 64, 0x100 | 1) == 1024 + 51200
+    assert lib.mg_attn_bwd_workspace_bytes_ex(1, 2, 100, 70, 64, 0x100 | 2) == 1024 + 51200
+    assert lib.mg_attn_bwd_workspace_bytes_ex(1, 2, 100, 70, 64, 0x100) == 0  # STRICT
+
+
+def test_16_bit_outputs_size_their_buffers(lib):
+    """With 16-bit outputs O (and dQ, dK, dV) take 2 bytes per element: an LSE
+    placed right after a 16-bit O is no overlap, one placed inside it is; in the
+    backward a dK right after a 16-bit dQ likewise."""
+    n = 1 * 2 * 64 * 64
+    assert fwd(lib, O=P(3), LSE=P(3) + 2 * n, contract=0x100 | 1) != mg.MG_ERR_INVALID_ARG
+    assert fwd(lib, O=P(3), LSE=P(3) + 2 * n - 16, contract=0x100 | 1) == mg.MG_ERR_INVALID_ARG
+    assert fwd(lib, O=P(3), LSE=P(3) + 2 * n, contract=1) == mg.MG_ERR_INVALID_ARG  # f32 O
+    assert bwd(lib, dQ=P(6), dK=P(6) + 2 * n, contract=0x100 | 1) != mg.MG_ERR_INVALID_ARG
+    assert bwd(lib, dQ=P(6), dK=P(6) + 2 * n - 16, contract=0x100 | 1) == mg.MG_ERR_INVALID_ARG
+
+
+def test_noalloc_rejects_16_bit_outputs(lib):
+    import ctypes
+    f = lib.mg_attn_bwd_noalloc
+    vp, i, fl = ctypes.c_void_p, ctypes.c_int, ctypes.c_float
+    f.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, i, i, i, i, i, fl, i, vp]
+    f.restype = i
+    args = [P(k) for k in range(9)]
+    assert f(*args, 1, 2, 64, 64, 1, 0.125, 0x100 | 1, None) == mg.MG_ERR_UNSUPPORTED
