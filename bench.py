@@ -90,6 +90,32 @@ def load_peaks():
             "sm_max_mhz": 2070.0, "source": "fallback"}
 
 
+def bind_to_gpu_numa(torch, device) -> list | None:
+    """Restrict this process to the CPUs local to `device` (sysfs local_cpulist
+    of its PCI function), so that pinned host buffers, placed on first touch,
+    sit on the GPU's own memory node: the end-to-end leg copies about 1.6 GB per
+    step between host and device. Returns the CPU list, or None where the
+    topology cannot be read (nothing is changed then)."""
+    try:
+        prop = torch.cuda.get_device_properties(device)
+        bus = "%04x:%02x:%02x.0" % (prop.pci_domain_id, prop.pci_bus_id, prop.pci_device_id)
+        with open(f"/sys/bus/pci/devices/{bus}/local_cpulist") as f:
+            spec = f.read().strip()
+        cpus = []
+        for part in spec.split(","):
+            if "-" in part:
+                a, b = part.split("-")
+                cpus.extend(range(int(a), int(b) + 1))
+            elif part:
+                cpus.append(int(part))
+        if not cpus:
+            return None
+        os.sched_setaffinity(0, cpus)
+        return cpus
+    except Exception:
+        return None
+
+
 def fp32_simt_peak_tflops(sm_count: int, mhz: float) -> float:
     """FP32 CUDA-core peak: SMs x 128 FP32 lanes x 2 flops (FFMA) x clock."""
     return sm_count * 128 * 2 * mhz * 1e6 / 1e12
@@ -656,6 +682,7 @@ def main():
     local = int(os.environ.get("LOCAL_RANK", "0"))
     torch.cuda.set_device(local)
     device = torch.device("cuda", local)
+    numa_cpus = bind_to_gpu_numa(torch, device)
     mg.load_library()
     props = torch.cuda.get_device_properties(device)
     sm_count = props.multi_processor_count
@@ -684,6 +711,8 @@ def main():
                    "flops_convention": "fwd 4BHL^2D, bwd 2.5x fwd, causal x1/2",
                    "l2": "flushed between timed steps (512 MiB write outside the events)",
                    "dq_mode": os.environ.get("MG_DQ_MODE", "atomic"),
+                   "host_cpus": (f"{len(numa_cpus)} GPU-local CPUs" if numa_cpus
+                                 else "unbound (topology not readable)"),
                    "parallelism": f"replica per GPU x{world()} (heads independent)"},
         "roofline": r["roofline"],
         "clocks": r["clocks"],
