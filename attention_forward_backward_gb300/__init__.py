@@ -21,8 +21,9 @@ The function names mirror the C ABI in ``include/mg_attn.h``:
 
 Tensors are PyTorch CUDA tensors, contiguous [B, H, L, D] (LSE [B, H, L]); the
 shape is read from Q. ``contract`` is ``STRICT_F32`` (0), ``ACCEL_BF16`` (1) or
-``ACCEL_F16`` (2), optionally OR-ed with ``OUT_16`` (16-bit outputs), or a name
-such as ``"accel"``, ``"accel_f16+out16"``.
+``ACCEL_F16`` (2), optionally OR-ed with ``OUT_16`` (16-bit outputs) and
+``DS_HILO`` (hi/lo split of dS in the backward), or a name such as ``"accel"``,
+``"accel_f16+out16"``, ``"accel+hilo"``.
 ``attention_fwd`` / ``attention_bwd`` are conveniences that allocate the
 outputs with PyTorch and call the above.
 """
@@ -37,7 +38,8 @@ ACCEL_BF16 = 1
 ACCEL_F16 = 2
 OUT_16 = 0x100  # flag: O, dQ, dK, dV in the inputs' 16-bit type
 CONTRACTS = {"strict": STRICT_F32, "accel": ACCEL_BF16, "accel_f16": ACCEL_F16}
-FLAGS = {"out16": OUT_16}
+DS_HILO = 0x200  # flag: hi/lo split of dS in the backward (derivative precision)
+FLAGS = {"out16": OUT_16, "hilo": DS_HILO}
 
 MG_OK, MG_ERR_INVALID_ARG, MG_ERR_UNSUPPORTED, MG_ERR_WORKSPACE, MG_ERR_CUDA, MG_ERR_TIMEOUT = range(6)
 

@@ -92,7 +92,7 @@ __global__ void __launch_bounds__(320, 1)
                          void *__restrict__ dV, int out16, int BH, int L, int Lk_rows, int D, int causal,
                          int off0, float scale, float scale_log2, unsigned int *err,
                          unsigned long long timeout_ns, const int *__restrict__ kv_len, int H,
-                         int br) {
+                         int br, int hilo) {
   using C = PPCfg<DP>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
@@ -242,6 +242,8 @@ __global__ void __launch_bounds__(320, 1)
         if (!(ok = mbar_wait(bar(C::B_DSREADY + w), (i >> 1) & 1, ab))) break;
         tc_fence_after();
         issue_acc(tw + 64, sdesc_add(dQmn, st * C::Q_TILE), tmem + C::T_DK, i == 0);
+        // hi/lo policy: dK also accumulates the lo part of dS^T (dP^T columns 32..63)
+        if (hilo) issue_acc(tw + 96, sdesc_add(dQmn, st * C::Q_TILE), tmem + C::T_DK, false);
         mma_commit(bar(C::B_QEMPTY + st));
       }
       mma_commit(bar(C::B_ACCDONE));
@@ -313,7 +315,8 @@ __global__ void __launch_bounds__(320, 1)
         tmem_ld32(tDP, *reinterpret_cast<uint32_t(*)[32]>(r));
         tmem_ld32(tDP + 32, *reinterpret_cast<uint32_t(*)[32]>(r + 32));
         tmem_wait_ld();
-        // dS^T over the first 32 columns of dP^T, 16 columns (32 queries) at a time
+        // dS^T over the first 32 columns of dP^T, 16 columns (32 queries) at a time;
+        // under the hi/lo policy its lo part over columns 32..63
 #pragma unroll
         for (int c = 0; c < 2; ++c) {
           uint32_t pk[16];
@@ -329,6 +332,20 @@ __global__ void __launch_bounds__(320, 1)
             pk[e / 2 + 1] = pack16<F16>(s2, s3);
           }
           tmem_st16(tDP + 16 * c, pk);
+          if (hilo) {
+            // the same dS values again (same arithmetic, same result), split
+#pragma unroll
+            for (int e = 0; e < 32; e += 4) {
+              const int q = 32 * c + e;
+              const float4 d4 = *reinterpret_cast<const float4 *>(dvq + q);
+              uint32_t h;
+              pack16_hilo<F16>(p[q] * (__uint_as_float(r[q]) - d4.x),
+                               p[q + 1] * (__uint_as_float(r[q + 1]) - d4.y), h, pk[e / 2]);
+              pack16_hilo<F16>(p[q + 2] * (__uint_as_float(r[q + 2]) - d4.z),
+                               p[q + 3] * (__uint_as_float(r[q + 3]) - d4.w), h, pk[e / 2 + 1]);
+            }
+            tmem_st16(tDP + 32 + 16 * c, pk);
+          }
         }
       }
       tmem_wait_st();
@@ -406,7 +423,7 @@ cudaError_t launch(const void *Q, const void *K, const void *V, const void *dO, 
   const long long grid = static_cast<long long>(nkb) * BH;
   kern<<<static_cast<unsigned>(grid), C::NTHREADS, C::SMEM_BYTES, st>>>(
       tq, tk, tv, tdo, LSE, Dvec, dK, dV, p.out16, BH, p.L, p.Lk, p.D, p.causal, p.off,
-      p.scale, p.scale * kLog2e, err, mg_wait_limit_ns(), p.kv_len, p.H, p.br);
+      p.scale, p.scale * kLog2e, err, mg_wait_limit_ns(), p.kv_len, p.H, p.br, p.hilo);
   return cudaGetLastError();
 }
 

@@ -83,7 +83,7 @@ __global__ void __launch_bounds__(320, 1)
                     const float *__restrict__ Dvec, void *__restrict__ dQ, int out16, int BH, int L,
                     int Lk_rows, int D, int causal, int off0, float scale, float scale_log2,
                     const int *__restrict__ kv_len, int H, int br, unsigned int *err,
-                    unsigned long long timeout_ns) {
+                    unsigned long long timeout_ns, int hilo) {
   using C = DqCfg<DP>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
@@ -219,6 +219,14 @@ __global__ void __launch_bounds__(320, 1)
           const uint32_t acol = (kk >> 2) * 64 + (kk & 3) * 8;
           mma_ts(tmem + C::T_DQ, aS + acol, sdesc_add(dk, kk * 2048), idQ, kk > 0 ? 1u : acc0);
         }
+        // hi/lo policy: dQ also accumulates dS's lo part (columns 64g+32 .. 64g+63)
+        if (hilo) {
+#pragma unroll
+          for (int kk = 0; kk < C::BN / 16; ++kk) {
+            const uint32_t acol = (kk >> 2) * 64 + 32 + (kk & 3) * 8;
+            mma_ts(tmem + C::T_DQ, aS + acol, sdesc_add(dk, kk * 2048), idQ, 1u);
+          }
+        }
         mma_commit(bar(C::B_KEMPTY + s));
         if (j + 1 < n && !(ok = issue_dP(j + 1))) break;
         if (j + 2 < n && !(ok = issue_S(j + 2))) break;
@@ -268,15 +276,20 @@ __global__ void __launch_bounds__(320, 1)
         uint32_t r[32];
         tmem_ld32(tDP + 32 * c, r);
         tmem_wait_ld();
-        uint32_t pk[16];
+        uint32_t pk[16], pl[16];
 #pragma unroll
         for (int e = 0; e < 16; ++e) {
           const float d0 = p[32 * c + 2 * e] * (__uint_as_float(r[2 * e]) - dvr);
           const float d1 = p[32 * c + 2 * e + 1] * (__uint_as_float(r[2 * e + 1]) - dvr);
-          pk[e] = pack16<F16>(d0, d1);
+          if (hilo)
+            pack16_hilo<F16>(d0, d1, pk[e], pl[e]);
+          else
+            pk[e] = pack16<F16>(d0, d1);
         }
-        // dS over the S columns this warpgroup has already read
+        // dS over the S columns this warpgroup has already read (its lo part, under
+        // the hi/lo policy, 32 columns further on)
         tmem_st16(tS + 16 * c, pk);
+        if (hilo) tmem_st16(tS + 32 + 16 * c, pl);
       }
       tmem_wait_st();
       tc_fence_before();
@@ -340,7 +353,7 @@ cudaError_t launch(const void *Q, const void *K, const void *V, const void *dO, 
   const long long grid = static_cast<long long>(nqb) * BH;
   kern<<<static_cast<unsigned>(grid), C::NTHREADS, C::SMEM_BYTES, st>>>(
       tq, tdo, tk, tv, LSE, Dvec, dQ, p.out16, BH, p.L, p.Lk, p.D, p.causal, p.off, p.scale,
-      p.scale * kLog2e, p.kv_len, p.H, p.br, err, mg_wait_limit_ns());
+      p.scale * kLog2e, p.kv_len, p.H, p.br, err, mg_wait_limit_ns(), p.hilo);
   return cudaGetLastError();
 }
 

@@ -116,8 +116,8 @@ int check_common(int B, int H, int Lq, int Lk, int D, int mask, float scale, int
   if (base != MG_CONTRACT_STRICT_F32 && base != MG_CONTRACT_ACCEL_BF16 &&
       base != MG_CONTRACT_ACCEL_F16)
     return MG_ERR_INVALID_ARG;
-  if (flags & ~MG_OUT_16) return MG_ERR_INVALID_ARG;
-  // STRICT_F32 is f32 end to end: no 16-bit outputs
+  if (flags & ~(MG_OUT_16 | MG_DS_HILO)) return MG_ERR_INVALID_ARG;
+  // STRICT_F32 is f32 end to end: no 16-bit outputs, no 16-bit dS to split
   if (flags && base == MG_CONTRACT_STRICT_F32) return MG_ERR_UNSUPPORTED;
   if (D != 32 && D != 64 && D != 128) return MG_ERR_UNSUPPORTED;
   return MG_OK;
@@ -131,6 +131,7 @@ MgProblem make_problem(int B, int H, int Lq, int Lk, int D, int mask, float scal
   p.br = mask == MG_MASK_CAUSAL_BOTTOM_RIGHT ? 1 : 0;
   p.f16 = (contract & MG_CONTRACT_BASE_MASK) == MG_CONTRACT_ACCEL_F16 ? 1 : 0;
   p.out16 = (contract & MG_OUT_16) ? 1 : 0;
+  p.hilo = (contract & MG_DS_HILO) ? 1 : 0;
   return p;
 }
 
@@ -404,7 +405,9 @@ int mg_attn_bwd_padded(const void *Q, const void *K, const void *V, const void *
       e = mg_launch_dvec_16(O, dO, Dvec, p, st);
     }
     if (e != cudaSuccess) return MG_ERR_CUDA;
-    if (accel_dq_atomic()) {
+    // the hi/lo dS policy runs in the two-pass backward, where both parts of dS
+    // are tensor-memory operands of the dK and dQ products
+    if (accel_dq_atomic() && !p.hilo) {
       // the reductions add into f32: the caller's dQ, or for 16-bit outputs an
       // f32 accumulator in the workspace that one pass rounds into dQ at the end
       float *dq_acc = p.out16 ? reinterpret_cast<float *>(static_cast<char *>(workspace) +

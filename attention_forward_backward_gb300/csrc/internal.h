@@ -25,6 +25,9 @@ struct MgProblem {
   // 16-bit type instead of f32 (LSE stays f32).
   int f16 = 0;
   int out16 = 0;
+  // Derivative-precision policy: hilo = 1 splits dS into a 16-bit hi part and
+  // a 16-bit lo part (dS - hi) and accumulates both products for dK and dQ.
+  int hilo = 0;
 };
 
 // Key rows that one head (bh = b * H + h) attends to, and its causal offset:

@@ -330,6 +330,22 @@ template <bool F16>
 __device__ __forceinline__ uint32_t pack16(float lo, float hi) {
   return F16 ? pack_f16(lo, hi) : pack_bf16(lo, hi);
 }
+// The two 16-bit values of a packed pair back in f32 (exact).
+template <bool F16>
+__device__ __forceinline__ float2 unpack16(uint32_t v) {
+  if (F16) return __half22float2(*reinterpret_cast<const __half2 *>(&v));
+  return make_float2(__uint_as_float(v << 16), __uint_as_float(v & 0xffff0000u));
+}
+// hi/lo split of two f32 values into 16-bit MMA operands: hi = round(x) and
+// lo = round(x - hi), so that hi + lo carries about twice the operand type's
+// mantissa (x - hi is exact in f32). With f16 the split widens the mantissa but
+// not the exponent range: values below f16's subnormals still flush.
+template <bool F16>
+__device__ __forceinline__ void pack16_hilo(float a, float b, uint32_t &hi, uint32_t &lo) {
+  hi = pack16<F16>(a, b);
+  const float2 h = unpack16<F16>(hi);
+  lo = pack16<F16>(a - h.x, b - h.y);
+}
 // Four f32 values rounded to the 16-bit output type, as 8 bytes (low first).
 template <bool F16>
 __device__ __forceinline__ uint2 pack16x4(float a, float b, float c, float d) {

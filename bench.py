@@ -386,7 +386,8 @@ def run_e2e(mg, torch, w, contract, args, host, device, stream, flops_step):
 def run_small_configs(mg, torch, device, stream, peaks, sm_count, steps: int, warmup: int):
     """fwd and fwd+bwd TFLOP/s of the four smaller seeded configurations for
     every contract each one lists, and of the accelerated contract's precision
-    variants (f16 inputs, 16-bit outputs) on the benchmark workload (CUDA events
+    variants (f16 inputs, 16-bit outputs, the hi/lo dS split, whose extra dK and
+    dQ products are not credited as flops) on the benchmark workload (CUDA events
     on the call stream, L2 flushed between timed steps, median step): the compact
     ``configs`` object of the default JSON line, so that those numbers come from
     the same run."""
@@ -396,7 +397,7 @@ def run_small_configs(mg, torch, device, stream, peaks, sm_count, steps: int, wa
     s = stream.cuda_stream
     plan = [(cfg, synth.WORKLOADS[cfg].contracts) for cfg in (1, 2, 3, 4)]
     # the precision variants of the accelerated contract on the benchmark workload
-    plan.append((5, ("accel_f16", "accel+out16", "accel_f16+out16")))
+    plan.append((5, ("accel_f16", "accel+out16", "accel_f16+out16", "accel+hilo")))
     for cfg, contracts in plan:
         w = synth.WORKLOADS[cfg]
         B, H, L, D = w.shape

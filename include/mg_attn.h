@@ -38,7 +38,7 @@
  *                           the pages' precision bit guards derivative regions
  *                           against (Section 3.1); ACCEL_BF16, with f32's
  *                           range, cannot underflow there.
- * Flag OR-ed into an ACCEL contract:
+ * Flags OR-ed into an ACCEL contract:
  *   MG_OUT_16               O, dQ, dK, dV are stored in the inputs' 16-bit type
  *                           (bf16 or f16, RNE) instead of f32; LSE stays f32, and
  *                           every accumulation stays f32 (dQ's reductions add
@@ -47,6 +47,21 @@
  *                           O in that 16-bit type. Not valid with STRICT_F32
  *                           (MG_ERR_UNSUPPORTED), the decode forward or the
  *                           no-allocation backward.
+ *   MG_DS_HILO              derivative-precision policy of the backward (the
+ *                           pages attach a precision bit to derivative regions
+ *                           so that the 16-bit promotion does not round small
+ *                           gradient operands, Section 3.1): dS is split into
+ *                           hi = round16(dS) and lo = round16(dS - hi), and dK
+ *                           and dQ accumulate both products (dS_hi + dS_lo)
+ *                           with f32 accumulation, so that the dS operand keeps
+ *                           about twice the 16-bit type's mantissa (bf16: 16
+ *                           bits, f16: 22) at twice the dK and dQ tensor work.
+ *                           The split widens the mantissa, not the exponent
+ *                           range (with f16, dS below 2^-24 still flushes). P
+ *                           (forward, dV) stays one 16-bit operand. Runs in
+ *                           the two-pass backward (a dK/dV kernel and a dQ
+ *                           pass). No effect on the forward calls; not valid
+ *                           with STRICT_F32 (MG_ERR_UNSUPPORTED).
  *
  * Layout. Q, K, V, O, dO, dQ, dK, dV are dense row-major [B][H][L][D] (D
  * innermost, no padding, no strides). LSE (and the workspace's Dvec) are
@@ -98,7 +113,8 @@ typedef enum {
   MG_CONTRACT_ACCEL_BF16 = 1,
   MG_CONTRACT_ACCEL_F16 = 2,
   MG_CONTRACT_BASE_MASK = 0xff, /* the base contract is contract & MG_CONTRACT_BASE_MASK */
-  MG_OUT_16 = 0x100             /* flag: 16-bit O, dQ, dK, dV (see above) */
+  MG_OUT_16 = 0x100,            /* flag: 16-bit O, dQ, dK, dV (see above) */
+  MG_DS_HILO = 0x200            /* flag: hi/lo split of dS in the backward (see above) */
 } mg_contract_t;
 
 typedef enum {

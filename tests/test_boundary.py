@@ -77,8 +77,9 @@ def bwd(lib, Q=P(0), K=P(1), V=P(2), O=P(3), dO=P(4), LSE=P(5), dQ=P(6), dK=P(7)
     (dict(scale=float("nan")), mg.MG_ERR_INVALID_ARG),
     (dict(scale=float("inf")), mg.MG_ERR_INVALID_ARG),
     (dict(contract=3), mg.MG_ERR_INVALID_ARG),
-    (dict(contract=0x200 | 1), mg.MG_ERR_INVALID_ARG),  # unknown flag
+    (dict(contract=0x400 | 1), mg.MG_ERR_INVALID_ARG),  # unknown flag
     (dict(contract=0x100), mg.MG_ERR_UNSUPPORTED),      # 16-bit outputs under STRICT_F32
+    (dict(contract=0x200), mg.MG_ERR_UNSUPPORTED),      # hi/lo dS split under STRICT_F32
     (dict(O=P(0)), mg.MG_ERR_INVALID_ARG),          # output aliases Q
     (dict(LSE=P(3) + 1024), mg.MG_ERR_INVALID_ARG),  # LSE inside O
 ])
@@ -97,6 +98,8 @@ def test_fwd_rejects(lib, kw, code):
     (dict(dK=P(6)), mg.MG_ERR_INVALID_ARG),          # dK aliases dQ
     (dict(ws=P(8)), mg.MG_ERR_INVALID_ARG),          # workspace aliases dV
     (dict(contract=1, ws=P(4)), mg.MG_ERR_INVALID_ARG),  # workspace aliases dO
+    (dict(contract=0x200), mg.MG_ERR_UNSUPPORTED),      # hi/lo dS split under STRICT_F32
+    (dict(contract=0x200 | 0x100 | 3), mg.MG_ERR_INVALID_ARG),  # no such base contract
 ])
 def test_bwd_rejects(lib, kw, code):
     assert bwd(lib, **kw) == code
@@ -283,6 +286,9 @@ def test_workspace_bytes_with_16_bit_outputs(lib):
     assert lib.mg_attn_bwd_workspace_bytes_ex(1, 2, 100, 70, 64, 0x100 | 1) == 1024 + 51200
     assert lib.mg_attn_bwd_workspace_bytes_ex(1, 2, 100, 70, 64, 0x100 | 2) == 1024 + 51200
     assert lib.mg_attn_bwd_workspace_bytes_ex(1, 2, 100, 70, 64, 0x100) == 0  # STRICT
+    # the hi/lo dS policy needs no workspace of its own
+    assert lib.mg_attn_bwd_workspace_bytes_ex(1, 2, 100, 70, 64, 0x200 | 1) == 1024
+    assert lib.mg_attn_bwd_workspace_bytes_ex(1, 2, 100, 70, 64, 0x200 | 0x100 | 1) == 1024 + 51200
 
 
 def test_16_bit_outputs_size_their_buffers(lib):

@@ -4,7 +4,10 @@ by element at the ACCEL gate (2e-2, max-abs error over max-abs reference):
 * ACCEL_F16 ("accel_f16"): f16 Q, K, V, dO, with P and dS rounded to f16 as MMA
   operands; the pages' own accelerated format ("Meganeura: Portable GPU Training
   and Inference through Vulkan and Metal", Section 4.2);
-* MG_OUT_16 ("+out16"): O, dQ, dK, dV stored in the inputs' 16-bit type.
+* MG_OUT_16 ("+out16"): O, dQ, dK, dV stored in the inputs' 16-bit type;
+* MG_DS_HILO ("+hilo"): the backward's derivative-precision policy, dS split
+  into a 16-bit hi and lo part (Section 3.1's precision bit on derivative
+  regions), with bf16 and with f16 inputs and 16-bit outputs.
 
 The oracle consumes the 16-bit-rounded inputs exactly, so only the kernels' own
 arithmetic and the final rounding of 16-bit outputs are measured. Covered: the
@@ -22,7 +25,7 @@ from parity_util import TOL, compare, compare_ex, device_inputs, run_gpu, run_gp
 
 pytestmark = pytest.mark.gpu
 
-VARIANTS = ["accel_f16", "accel+out16", "accel_f16+out16"]
+VARIANTS = ["accel_f16", "accel+out16", "accel_f16+out16", "accel+hilo", "accel_f16+hilo+out16"]
 
 
 def _full(w, contract, bwd=True):
