@@ -16,6 +16,9 @@ The function names mirror the C ABI in ``include/mg_attn.h``:
 * ``mg_attn_fwd_padded``, ``mg_attn_bwd_padded`` (per-batch key padding lengths)
 * ``mg_attn_fwd_decode_workspace_bytes``, ``mg_attn_fwd_decode`` (split-key
   forward for at most 8 query rows)
+* ``mg_conv2d_grad_input(dY, Wt, dX, stride, pad, contract)``,
+  ``mg_conv2d_grad_weight(X, dY, dW, stride, pad, contract)`` (derivatives of a
+  channels-last 2-D convolution: X [N, H, W, C], Wt [K, R, S, C], dY [N, P, Q, K])
 * ``mg_status_string(status)``, ``mg_get_device_error(stream=None)``
 * ``mg_attn_profile_enable``, ``mg_attn_profile_read``, ``mg_attn_kernel_name``
 
@@ -104,6 +107,10 @@ def load_library(path: str | None = None):
         lib.mg_attn_kernel_count.restype = i
         lib.mg_attn_kernel_name.argtypes = [i]
         lib.mg_attn_kernel_name.restype = ctypes.c_char_p
+        for name in ("mg_conv2d_grad_input", "mg_conv2d_grad_weight"):
+            fn = getattr(lib, name)
+            fn.argtypes = [vp, vp, vp] + [i] * 10 + [vp]
+            fn.restype = i
         _lib = lib
         return lib
 
@@ -268,6 +275,47 @@ def mg_attn_fwd_decode(Q, K, V, O, LSE, mask, scale, contract, workspace, stream
                                            _stream(stream))
     if rc != MG_OK:
         raise MgError(rc, "mg_attn_fwd_decode")
+    return rc
+
+
+def _conv_dims(X_shape, Wt_shape, stride: int, pad: int):
+    N, H, W, C = (int(x) for x in X_shape)
+    K, R, S, C2 = (int(x) for x in Wt_shape)
+    if C2 != C:
+        raise ValueError("X [N,H,W,C] and Wt [K,R,S,C] must share C")
+    return N, H, W, C, K, R, S
+
+
+def conv_out_size(H: int, W: int, R: int, S: int, stride: int, pad: int):
+    """(P, Q): output rows and columns of the convolution."""
+    return (H + 2 * pad - R) // stride + 1, (W + 2 * pad - S) // stride + 1
+
+
+def mg_conv2d_grad_input(dY, Wt, dX, stride: int, pad: int, contract="accel",
+                         stream=None) -> int:
+    """dX [N,H,W,C] (f32, overwritten) from dY [N,P,Q,K] and Wt [K,R,S,C] (16-bit)."""
+    N, H, W, C, K, R, S = _conv_dims(dX.shape, Wt.shape, stride, pad)
+    if tuple(dY.shape) != (N,) + conv_out_size(H, W, R, S, stride, pad) + (K,):
+        raise ValueError("dY does not match the convolution's output shape")
+    rc = load_library().mg_conv2d_grad_input(_ptr(dY), _ptr(Wt), _ptr(dX), N, H, W, C, K, R, S,
+                                             int(stride), int(pad), _contract(contract),
+                                             _stream(stream))
+    if rc != MG_OK:
+        raise MgError(rc, "mg_conv2d_grad_input")
+    return rc
+
+
+def mg_conv2d_grad_weight(X, dY, dW, stride: int, pad: int, contract="accel",
+                          stream=None) -> int:
+    """dW [K,R,S,C] (f32, overwritten) from X [N,H,W,C] and dY [N,P,Q,K] (16-bit)."""
+    N, H, W, C, K, R, S = _conv_dims(X.shape, dW.shape, stride, pad)
+    if tuple(dY.shape) != (N,) + conv_out_size(H, W, R, S, stride, pad) + (K,):
+        raise ValueError("dY does not match the convolution's output shape")
+    rc = load_library().mg_conv2d_grad_weight(_ptr(X), _ptr(dY), _ptr(dW), N, H, W, C, K, R, S,
+                                              int(stride), int(pad), _contract(contract),
+                                              _stream(stream))
+    if rc != MG_OK:
+        raise MgError(rc, "mg_conv2d_grad_weight")
     return rc
 
 

@@ -18,7 +18,7 @@
 namespace {
 
 constexpr int kMaxDevices = 64;
-constexpr int kMaxSlots = 32;
+constexpr int kMaxSlots = 48;
 
 // Device error word: bounded waits in the ACCEL kernels write a code here
 // instead of trapping. One copy per device (module globals are per context).
@@ -84,7 +84,7 @@ void prof_free() {
 const char *const kKernelNames[MGK_COUNT] = {
     "strict_fwd", "strict_dvec", "strict_dkdv_dq", "accel_fwd",     "accel_dvec",
     "accel_dkdv_dq", "dq_zero",  "accel_dkdv",    "accel_dq",    "decode_fwd",
-    "dq_round"};
+    "dq_round", "conv_dgrad", "conv_wgrad"};
 
 // How the ACCEL backward produces dQ: f32 TMA reductions from the fused dK/dV
 // kernel (default, measured faster on GB300) or a separate dQ pass that
@@ -232,6 +232,39 @@ cudaError_t mg_set_smem_attr(const void *func, int bytes, int slot) {
   }
   return e;
 }
+
+// ---------------------------------------------------------------- convolution derivatives
+namespace {
+
+// Shape and contract checks shared by both convolution derivatives.
+int conv_problem(int N, int H, int W, int C, int K, int R, int S, int stride, int pad,
+                 int contract, MgConvProblem *p) {
+  if (N < 1 || H < 1 || W < 1 || C < 1 || K < 1 || R < 1 || S < 1 || pad < 0)
+    return MG_ERR_INVALID_ARG;
+  if (H > 65535 || W > 65535 || R > 64 || S > 64 || pad > 64) return MG_ERR_INVALID_ARG;
+  if (stride != 1 && stride != 2) return (stride < 1) ? MG_ERR_INVALID_ARG : MG_ERR_UNSUPPORTED;
+  if (H + 2 * pad < R || W + 2 * pad < S) return MG_ERR_INVALID_ARG;
+  const int base = contract & MG_CONTRACT_BASE_MASK, flags = contract & ~MG_CONTRACT_BASE_MASK;
+  if (base != MG_CONTRACT_STRICT_F32 && base != MG_CONTRACT_ACCEL_BF16 &&
+      base != MG_CONTRACT_ACCEL_F16)
+    return MG_ERR_INVALID_ARG;
+  if (flags & ~(MG_OUT_16 | MG_DS_HILO)) return MG_ERR_INVALID_ARG;
+  // tensor cores only, f32 results; channel counts in whole 16-byte rows
+  if (base == MG_CONTRACT_STRICT_F32 || flags) return MG_ERR_UNSUPPORTED;
+  if (C % 8 != 0 || K % 8 != 0) return MG_ERR_UNSUPPORTED;
+  const int P = (H + 2 * pad - R) / stride + 1, Q = (W + 2 * pad - S) / stride + 1;
+  const long long lim = 0x7fffffffLL;
+  if (static_cast<long long>(N) * H * W * C > lim || static_cast<long long>(N) * P * Q * K > lim ||
+      static_cast<long long>(K) * R * S * C > lim)
+    return MG_ERR_INVALID_ARG;
+  // grid limits of the weight gradient (R*S taps, K/128 x C/64 channel blocks)
+  if (static_cast<long long>((K + 127) / 128) * ((C + 63) / 64) > 65535) return MG_ERR_UNSUPPORTED;
+  *p = MgConvProblem{N, H, W, C, K, R, S, stride, pad, P, Q,
+                     base == MG_CONTRACT_ACCEL_F16 ? 1 : 0};
+  return MG_OK;
+}
+
+}  // namespace
 
 extern "C" {
 
@@ -488,6 +521,46 @@ int mg_attn_profile_read(int kernel, int *launches, double *total_ms) {
   *launches = cnt;
   *total_ms = ms;
   return MG_OK;
+}
+
+// ---------------------------------------------------------------- convolution derivatives
+int mg_conv2d_grad_input(const void *dY, const void *Wt, float *dX, int N, int H, int W, int C,
+                         int K, int R, int S, int stride, int pad, int contract, void *stream) {
+  MgConvProblem p;
+  int rc = conv_problem(N, H, W, C, K, R, S, stride, pad, contract, &p);
+  if (rc) return rc;
+  const void *ptrs[] = {dY, Wt, dX};
+  if ((rc = check_ptrs(ptrs, 3))) return rc;
+  const Range in[] = {rng(dY, static_cast<size_t>(N) * p.P * p.Q * K * 2),
+                      rng(Wt, static_cast<size_t>(K) * R * S * C * 2)};
+  const Range out[] = {rng(dX, static_cast<size_t>(N) * H * W * C * 4)};
+  if ((rc = check_alias(in, 2, out, 1))) return rc;
+  unsigned int *err = device_error_word();
+  if (!err) return MG_ERR_CUDA;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  ProfScope ps(MGK_CONV_DGRAD, st);
+  return map_cuda(mg_launch_conv_dgrad(dY, Wt, dX, p, err, st));
+}
+
+int mg_conv2d_grad_weight(const void *X, const void *dY, float *dW, int N, int H, int W, int C,
+                          int K, int R, int S, int stride, int pad, int contract, void *stream) {
+  MgConvProblem p;
+  int rc = conv_problem(N, H, W, C, K, R, S, stride, pad, contract, &p);
+  if (rc) return rc;
+  const void *ptrs[] = {X, dY, dW};
+  if ((rc = check_ptrs(ptrs, 3))) return rc;
+  const size_t nw = static_cast<size_t>(K) * R * S * C;
+  const Range in[] = {rng(X, static_cast<size_t>(N) * H * W * C * 2),
+                      rng(dY, static_cast<size_t>(N) * p.P * p.Q * K * 2)};
+  const Range out[] = {rng(dW, nw * 4)};
+  if ((rc = check_alias(in, 2, out, 1))) return rc;
+  unsigned int *err = device_error_word();
+  if (!err) return MG_ERR_CUDA;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  ProfScope ps(MGK_CONV_WGRAD, st);
+  cudaError_t e = cudaMemsetAsync(dW, 0, nw * 4, st);
+  if (e == cudaSuccess) e = mg_launch_conv_wgrad(X, dY, dW, p, err, st);
+  return map_cuda(e);
 }
 
 int mg_attn_kernel_count(void) { return MGK_COUNT; }

@@ -61,7 +61,9 @@ enum MgKernelId {
   MGK_ACCEL_DQ = 8,       // dQ pass of the two-pass backward
   MGK_DECODE_FWD = 9,     // split-key forward for a few query rows (partials + merge)
   MGK_DQ_ROUND = 10,      // f32 dQ accumulator rounded to the 16-bit output type
-  MGK_COUNT = 11
+  MGK_CONV_DGRAD = 11,    // convolution input gradient
+  MGK_CONV_WGRAD = 12,    // convolution weight gradient (after zeroing dW)
+  MGK_COUNT = 13
 };
 
 // Device error codes written into the device error word by bounded waits.
@@ -137,3 +139,18 @@ cudaError_t mg_launch_accel_dq(const void *Q, const void *K, const void *V, cons
 // dst (16-bit, bf16 or f16 by `f16`) = src (f32), n elements (n % 4 == 0).
 cudaError_t mg_launch_f32_to_16(const float *src, void *dst, size_t n, bool f16,
                                 cudaStream_t st);
+
+// A channels-last 2-D convolution: X [N][H][W][C], Wt [K][R][S][C], Y and dY
+// [N][P][Q][K] with P = (H + 2 pad - R) / stride + 1, Q likewise; f16 = 1 for f16
+// operands (else bf16). Shapes are validated by the caller.
+struct MgConvProblem {
+  int N, H, W, C, K, R, S, stride, pad, P, Q;
+  int f16;
+};
+
+// dX (f32, overwritten) from dY and Wt.
+cudaError_t mg_launch_conv_dgrad(const void *dY, const void *Wt, float *dX,
+                                 const MgConvProblem &p, unsigned int *err, cudaStream_t st);
+// dW += the weight gradient from X and dY (f32; the caller zeroes dW first).
+cudaError_t mg_launch_conv_wgrad(const void *X, const void *dY, float *dW,
+                                 const MgConvProblem &p, unsigned int *err, cudaStream_t st);

@@ -138,6 +138,16 @@ __device__ __forceinline__ void tma_load_3d(uint32_t dst, const void *tmap, int 
       : "memory");
 }
 
+// 4-D tiled load (coordinates innermost first) completing on `bar`.
+__device__ __forceinline__ void tma_load_4d(uint32_t dst, const void *tmap, int c0, int c1,
+                                            int c2, int c3, uint32_t bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.4d.shared::cluster.global.mbarrier::complete_tx::bytes"
+      " [%0], [%1, {%2, %3, %4, %5}], [%6];" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(tmap)), "r"(c0), "r"(c1), "r"(c2), "r"(c3), "r"(bar)
+      : "memory");
+}
+
 // 3-D tiled f32 add-reduction from shared memory into global memory.
 __device__ __forceinline__ void tma_reduce_add_3d(const void *tmap, uint32_t src, int c0, int c1,
                                                   int c2) {

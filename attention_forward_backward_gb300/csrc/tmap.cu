@@ -56,3 +56,23 @@ cudaError_t mg_tmap_16(CUtensorMap *m, const void *ptr, int D, int L, int BH, in
 cudaError_t mg_tmap_f32(CUtensorMap *m, const void *ptr, int D, int L, int BH, int box_rows) {
   return encode(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, ptr, D, L, BH, 32, box_rows);
 }
+
+cudaError_t mg_tmap_16_4d(CUtensorMap *m, const void *ptr, const long long dims[4],
+                          const long long strides_bytes[3], const int box[4], bool f16) {
+  EncodeTiledFn fn = encode_fn();
+  if (!fn) return cudaErrorNotSupported;
+  cuuint64_t d[4], st[3];
+  cuuint32_t b[4];
+  const cuuint32_t estr[4] = {1, 1, 1, 1};
+  for (int i = 0; i < 4; ++i) {
+    if (dims[i] < 1 || box[i] < 1 || box[i] > 256) return cudaErrorInvalidValue;
+    d[i] = static_cast<cuuint64_t>(dims[i]);
+    b[i] = static_cast<cuuint32_t>(box[i]);
+  }
+  for (int i = 0; i < 3; ++i) st[i] = static_cast<cuuint64_t>(strides_bytes[i]);
+  CUresult r = fn(m, f16 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4,
+                  const_cast<void *>(ptr), d, st, b, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                  CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                  CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
+}

@@ -18,3 +18,8 @@ cudaError_t mg_tmap_16(CUtensorMap *m, const void *ptr, int D, int L, int BH, in
                        bool f16);
 // f32 tensor, boxes of 32 columns x box_rows rows, 128-byte swizzle (dQ reduce).
 cudaError_t mg_tmap_f32(CUtensorMap *m, const void *ptr, int D, int L, int BH, int box_rows);
+// 16-bit 4-D tensor (dims[0] innermost, contiguous; strides in bytes of dims
+// 1..3, multiples of 16), boxes of 64 x box1 x box2 x box3 elements, 128-byte
+// swizzle, zero fill out of bounds (channels-last convolution operands).
+cudaError_t mg_tmap_16_4d(CUtensorMap *m, const void *ptr, const long long dims[4],
+                          const long long strides_bytes[3], const int box[4], bool f16);

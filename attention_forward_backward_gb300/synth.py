@@ -190,3 +190,93 @@ def cross_inputs(B, H, Lq, Lk, D, contract: str, seed_cfg: int = 950):
         x = normal_f32(1000 * seed_cfg + TENSOR_IDS[t], B * H * rows * D).reshape(B, H, rows, D)
         out[t] = encode(x, contract)
     return out
+
+
+# ---------------------------------------------------------------- convolution layers
+CONV_TENSOR_IDS = {"X": 4, "Wt": 5, "dY": 6}
+
+
+@dataclass(frozen=True)
+class ConvWorkload:
+    """One seeded 2-D convolution layer, channels last: X [N, H, W, C], Wt
+    [K, R, S, C], dY [N, P, Q, K] with P = (H + 2 pad - R) // stride + 1."""
+    cid: int
+    N: int
+    H: int
+    W: int
+    C: int
+    K: int
+    R: int
+    S: int
+    stride: int
+    pad: int
+    name: str = ""
+
+    @property
+    def P(self) -> int:
+        return (self.H + 2 * self.pad - self.R) // self.stride + 1
+
+    @property
+    def Q(self) -> int:
+        return (self.W + 2 * self.pad - self.S) // self.stride + 1
+
+    def shapes(self):
+        return {"X": (self.N, self.H, self.W, self.C), "Wt": (self.K, self.R, self.S, self.C),
+                "dY": (self.N, self.P, self.Q, self.K)}
+
+    def flops(self) -> float:
+        """2 N P Q K C R S: one derivative (input or weight gradient)."""
+        return 2.0 * self.N * self.P * self.Q * self.K * self.C * self.R * self.S
+
+    def with_batch(self, N: int) -> "ConvWorkload":
+        return ConvWorkload(self.cid, N, self.H, self.W, self.C, self.K, self.R, self.S,
+                            self.stride, self.pad, self.name.replace(f"N{self.N}", f"N{N}"))
+
+
+def _resnet(cid, H, C, K, R, stride, pad, what, N=32):
+    P = (H + 2 * pad - R) // stride + 1
+    return ConvWorkload(cid, N, H, H, C, K, R, R, stride, pad,
+                        name=f"{what} {R}x{R}/{stride} {C}->{K} {H}->{P} N{N}")
+
+
+# The distinct convolution shapes of a ResNet-50 (v1.5: stride on the 3x3 of the
+# first block of a stage) on 224 x 224 images, batch 32; the stem (C = 3) is
+# left out (see the derivative functions' channel rule).
+CONV_WORKLOADS = {
+    1: _resnet(1, 56, 64, 64, 3, 1, 1, "res2 3x3"),
+    2: _resnet(2, 56, 256, 64, 1, 1, 0, "res2 reduce"),
+    3: _resnet(3, 56, 64, 256, 1, 1, 0, "res2 expand"),
+    4: _resnet(4, 56, 128, 128, 3, 2, 1, "res3 3x3 strided"),
+    5: _resnet(5, 28, 128, 128, 3, 1, 1, "res3 3x3"),
+    6: _resnet(6, 56, 256, 512, 1, 2, 0, "res3 downsample"),
+    7: _resnet(7, 14, 256, 256, 3, 1, 1, "res4 3x3"),
+    8: _resnet(8, 14, 1024, 256, 1, 1, 0, "res4 reduce"),
+    9: _resnet(9, 7, 512, 512, 3, 1, 1, "res5 3x3"),
+    10: _resnet(10, 7, 512, 2048, 1, 1, 0, "res5 expand"),
+}
+
+
+def conv_tensor_f32(w: ConvWorkload, which: str) -> np.ndarray:
+    """Seeded float32 tensor ``which`` in {X, Wt, dY}: X = |normal| (activations
+    after a ReLU), Wt = normal * sqrt(2 / (C R S)) (He initialisation), dY =
+    normal."""
+    shape = w.shapes()[which]
+    seed = 1000 * (100 + w.cid) + CONV_TENSOR_IDS[which]
+    x = normal_f32(seed, int(np.prod(shape))).reshape(shape)
+    if which == "X":
+        x = np.abs(x)
+    elif which == "Wt":
+        x *= np.float32(math.sqrt(2.0 / (w.C * w.R * w.S)))
+    return x
+
+
+def conv_inputs(w: ConvWorkload, contract: str = "accel"):
+    """Host inputs X, Wt, dY of a convolution layer in a 16-bit contract's format
+    (bit patterns and their exact float32 values, as ``encode``)."""
+    return {t: encode(conv_tensor_f32(w, t), contract) for t in ("X", "Wt", "dY")}
+
+
+def custom_conv(N, H, W, C, K, R, S, stride, pad, cid=200) -> ConvWorkload:
+    """An ad-hoc convolution (edge cases in tests) with its own seed block."""
+    return ConvWorkload(cid, N, H, W, C, K, R, S, stride, pad,
+                        name=f"custom N{N} {H}x{W} {C}->{K} {R}x{S}/{stride} pad{pad}")

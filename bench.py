@@ -68,6 +68,8 @@ def parse():
     ap.add_argument("--decode", default=None,
                     help="B,H,Lq,Lk,D,mask with Lq <= 8: measure the split-key decode forward "
                          "(mg_attn_fwd_decode) beside mg_attn_fwd_ex on the same inputs")
+    ap.add_argument("--conv", action="store_true",
+                    help="time the convolution derivatives on the ResNet-50 layer set instead")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-configs", action="store_true",
                     help="skip the compact per-config table (configurations 1-4) of the default run")
@@ -659,12 +661,124 @@ def run_decode(args):
     return 0
 
 
+def conv_layers(mg, torch, device, stream, peaks, steps: int, warmup: int, batch: int = 0):
+    """Both convolution derivatives of every seeded ResNet-50 layer shape (batch
+    32 unless `batch`), each timed alone with CUDA events on the call stream, L2
+    flushed before every timed call (the median of `steps` calls). Returns per
+    layer and derivative the median ms and TFLOP/s (2 N P Q K C R S per
+    derivative), and the set's total TFLOP/s."""
+    s = stream.cuda_stream
+    flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=device)
+    layers, tot_f, tot_ms = {}, 0.0, 0.0
+    for cid, w in synth.CONV_WORKLOADS.items():
+        if batch:
+            w = w.with_batch(batch)
+        host = synth.conv_inputs(w, "accel")
+        dev = {k: torch.from_numpy(np.ascontiguousarray(v["bits"]).view(np.int16)).view(
+            torch.bfloat16).to(device) for k, v in host.items()}
+        dX = torch.empty((w.N, w.H, w.W, w.C), dtype=torch.float32, device=device)
+        dW = torch.empty((w.K, w.R, w.S, w.C), dtype=torch.float32, device=device)
+        calls = {
+            "dgrad": lambda: mg.mg_conv2d_grad_input(dev["dY"], dev["Wt"], dX, w.stride, w.pad,
+                                                     "accel", s),
+            "wgrad": lambda: mg.mg_conv2d_grad_weight(dev["X"], dev["dY"], dW, w.stride, w.pad,
+                                                      "accel", s)}
+        row = {"layer": w.name}
+        for name, call in calls.items():
+            ev = []
+            with torch.cuda.stream(stream):
+                for i in range(warmup + steps):
+                    flush.fill_(float(i))
+                    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                    a.record(stream)
+                    call()
+                    b.record(stream)
+                    if i >= warmup:
+                        ev.append((a, b))
+                torch.cuda.synchronize()
+            if mg.mg_get_device_error(s) != mg.MG_OK:
+                raise RuntimeError(f"conv {w.name} {name}: device error word set")
+            ms = statistics.median(a.elapsed_time(b) for a, b in ev)
+            tf = w.flops() / (ms * 1e-3) / 1e12
+            row[name] = {"ms": round(ms, 5), "tflops": round(tf, 2),
+                         "frac_of_peak": round(tf / peaks["bf16_tflops"], 4)}
+            tot_f += w.flops()
+            tot_ms += ms
+        layers[str(cid)] = row
+    total = tot_f / (tot_ms * 1e-3) / 1e12
+    return {"layers": layers, "total_tflops": round(total, 2),
+            "total_frac_of_peak": round(total / peaks["bf16_tflops"], 4),
+            "total_ms": round(tot_ms, 4), "total_gflop": round(tot_f / 1e9, 3)}
+
+
+def conv_oracle_sample(seconds: float):
+    """The fp64 oracle's two derivatives on the first layer shape (res2 3x3) at
+    growing batch until about `seconds` of CPU work: TFLOP/s, threads, sample."""
+    from oracle import conv as oc
+    import oracle
+    w = synth.CONV_WORKLOADS[1]
+    n, el = 1, 0.0
+    while True:
+        ww = w.with_batch(n)
+        v = {k: x["values"] for k, x in synth.conv_inputs(ww, "accel").items()}
+        t0 = time.perf_counter()
+        oc.conv2d_grad_input(v["dY"], v["Wt"], ww.H, ww.W, ww.stride, ww.pad)
+        oc.conv2d_grad_weight(v["X"], v["dY"], ww.R, ww.S, ww.stride, ww.pad)
+        el = time.perf_counter() - t0
+        if el >= seconds / 3 or n >= 32:
+            break
+        n *= 2
+    return (2 * ww.flops() / el / 1e12, oracle.max_threads(),
+            f"both derivatives of {ww.name} ({el:.1f} s)")
+
+
+def run_conv(args):
+    """Convolution derivatives on one GB300: the ResNet-50 layer set at batch 32
+    (one JSON line; roofline against the measured dense bf16 rate)."""
+    import torch
+    import attention_forward_backward_gb300 as mg
+    device = torch.device("cuda", 0)
+    torch.cuda.set_device(0)
+    mg.load_library()
+    stream = torch.cuda.Stream(device)
+    peaks = load_peaks()
+    clocks = ClockSampler(0)
+    clocks.start()
+    res = conv_layers(mg, torch, device, stream, peaks, args.steps, args.warmup)
+    clk = clocks.stop()
+    line = {
+        "metric": "convolution derivative TFLOP/s on 1 GB300 (input + weight gradients, "
+                  "ResNet-50 layer set)",
+        "value": res["total_tflops"], "unit": "TFLOP/s", "n_gpus": 1, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": res["total_ms"], "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "config": {"workload": "ResNet-50 convolution shapes (10 layers, 224x224, batch 32), "
+                               "dX and dW of each", "layout": "NHWC / KRSC",
+                   "l2": "flushed before every timed call",
+                   "flops_convention": "2 N P Q K C R S per derivative"},
+        "roofline": {"bound": "tensor", "achieved": res["total_tflops"],
+                     "peak": peaks["bf16_tflops"], "unit": "TFLOP/s",
+                     "frac": res["total_frac_of_peak"], "traffic": None,
+                     "peak_source": peaks["source"]},
+        "clocks": clk, "layers": res["layers"],
+        "gpu_launches": (args.steps + args.warmup) * 2 * len(res["layers"]),
+    }
+    if not args.no_cpu_baseline:
+        tf, cores, sample = conv_oracle_sample(args.cpu_seconds)
+        line["cpu_baseline"] = {"value": tf, "unit": "TFLOP/s", "cores": cores,
+                                "kind": "oracle", "sample": sample}
+    print(json.dumps(line))
+    return 0
+
+
 def main():
     args = parse()
     if args.cross:
         return run_cross(args)
     if args.decode:
         return run_decode(args)
+    if args.conv:
+        return run_conv(args)
     if args.shape:
         B, H, L, D, causal = (int(x) for x in args.shape.split(","))
         w = synth.custom_workload(B, H, L, D, bool(causal), seed_cfg=800)
@@ -732,6 +846,12 @@ def main():
     if rank() == 0 and world() == 1 and not args.shape and w.cfg == 5 and not args.no_configs:
         line["configs"] = run_small_configs(mg, torch, device, stream, peaks, sm_count,
                                             steps=20, warmup=3)
+        conv = conv_layers(mg, torch, device, stream, peaks, steps=10, warmup=3)
+        line["conv"] = {"workload": "ResNet-50 convolution shapes, batch 32 (dX and dW)",
+                        "total_tflops": conv["total_tflops"],
+                        "total_frac_of_peak": conv["total_frac_of_peak"],
+                        "layers": {k: {"dgrad": v["dgrad"]["tflops"], "wgrad": v["wgrad"]["tflops"]}
+                                   for k, v in conv["layers"].items()}}
     if rank() == 0 and not args.no_cpu_baseline and world() == 1:
         tf, cores, sample, _ = oracle_sample(w, head, args.cpu_seconds)
         line["cpu_baseline"] = {"value": tf, "unit": UNIT, "cores": cores, "kind": "oracle",

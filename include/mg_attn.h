@@ -286,6 +286,41 @@ int mg_attn_fwd_decode(const void *Q, const void *K, const void *V, void *O, flo
                        int B, int H, int Lq, int Lk, int D, int mask, float scale,
                        int contract, void *workspace, size_t workspace_bytes, void *stream);
 
+/*
+ * Convolution derivatives ("Meganeura: Portable GPU Training and Inference
+ * through Vulkan and Metal", Section 3.1 lists convolution input and weight
+ * derivatives among the backward nodes; Section 7.3, "Convolution derivatives
+ * own the ResNet gap", names the input-gradient GEMM and the weight-gradient
+ * GEMM with its small-output variant). The forward is a 2-D convolution as
+ * deep-learning frameworks define it (cross-correlation, zero padding, the same
+ * stride and padding on both spatial axes, no dilation, one group), channels
+ * last:
+ *   X [N][H][W][C], Wt [K][R][S][C], Y and dY [N][P][Q][K],
+ *   P = (H + 2 pad - R) / stride + 1,  Q = (W + 2 pad - S) / stride + 1,
+ *   Y[n,p,q,k] = sum_{r,s,c} X[n, p*stride - pad + r, q*stride - pad + s, c] Wt[k,r,s,c]
+ * and its derivatives are
+ *   dX[n,h,w,c] = sum over p*stride - pad + r = h, q*stride - pad + s = w of
+ *                 dY[n,p,q,k] Wt[k,r,s,c]
+ *   dW[k,r,s,c] = sum_{n,p,q} dY[n,p,q,k] X[n, p*stride - pad + r, q*stride - pad + s, c]
+ * Contract: ACCEL_BF16 (X, Wt, dY bf16) or ACCEL_F16 (f16); products on the
+ * tcgen05 tensor cores with f32 accumulation; dX and dW are f32 and are
+ * overwritten. Only the order of the f32 additions differs from exact
+ * arithmetic on the 16-bit inputs; dW adds per-CTA partial sums with f32
+ * atomics, so it is not bitwise reproducible across runs.
+ * Preconditions checked: pointers non-NULL, 16-byte aligned, outputs not
+ * overlapping inputs; N, H, W, C, K, R, S >= 1; H, W <= 65535; R, S, pad in
+ * [0, 64] with H + 2 pad >= R and W + 2 pad >= S; every tensor below 2^31
+ * elements (else MG_ERR_INVALID_ARG); stride 1 or 2, C and K multiples of 8,
+ * ceil(K/128) * ceil(C/64) <= 65535, contract ACCEL_BF16 or ACCEL_F16 without
+ * flags (else MG_ERR_UNSUPPORTED: STRICT_F32 has no convolution derivatives).
+ * Asynchronous on `stream`; no allocation. Kernel names in the profile:
+ * "conv_dgrad", "conv_wgrad".
+ */
+int mg_conv2d_grad_input(const void *dY, const void *Wt, float *dX, int N, int H, int W, int C,
+                         int K, int R, int S, int stride, int pad, int contract, void *stream);
+int mg_conv2d_grad_weight(const void *X, const void *dY, float *dW, int N, int H, int W, int C,
+                          int K, int R, int S, int stride, int pad, int contract, void *stream);
+
 /* Static, human-readable name of a status code. Never NULL. */
 const char *mg_status_string(int status);
 

@@ -311,3 +311,36 @@ def test_noalloc_rejects_16_bit_outputs(lib):
     f.restype = i
     args = [P(k) for k in range(9)]
     assert f(*args, 1, 2, 64, 64, 1, 0.125, 0x100 | 1, None) == mg.MG_ERR_UNSUPPORTED
+
+
+# ---------------------------------------------------------------- convolution derivatives
+def conv(lib, which, a=P(0), b=P(1), out=P(2), N=2, H=8, W=8, C=64, K=64, R=3, S=3, stride=1,
+         pad=1, contract=1):
+    fn = lib.mg_conv2d_grad_input if which == "dgrad" else lib.mg_conv2d_grad_weight
+    return fn(a, b, out, N, H, W, C, K, R, S, stride, pad, contract, None)
+
+
+@pytest.mark.parametrize("which", ["dgrad", "wgrad"])
+@pytest.mark.parametrize("kw,code", [
+    (dict(a=None), mg.MG_ERR_INVALID_ARG),
+    (dict(out=None), mg.MG_ERR_INVALID_ARG),
+    (dict(b=P(1) + 8), mg.MG_ERR_INVALID_ARG),           # misaligned
+    (dict(out=P(0)), mg.MG_ERR_INVALID_ARG),             # output aliases an input
+    (dict(out=P(1) + 1024), mg.MG_ERR_INVALID_ARG),      # output inside an input
+    (dict(N=0), mg.MG_ERR_INVALID_ARG),
+    (dict(C=-8), mg.MG_ERR_INVALID_ARG),
+    (dict(R=11, pad=1), mg.MG_ERR_INVALID_ARG),          # kernel larger than the padded image
+    (dict(pad=-1), mg.MG_ERR_INVALID_ARG),
+    (dict(stride=0), mg.MG_ERR_INVALID_ARG),
+    (dict(H=70000), mg.MG_ERR_INVALID_ARG),
+    (dict(N=1 << 16, H=256, W=256, C=64), mg.MG_ERR_INVALID_ARG),  # X beyond 2^31 elements
+    (dict(stride=3), mg.MG_ERR_UNSUPPORTED),
+    (dict(C=12), mg.MG_ERR_UNSUPPORTED),                 # channels not in 16-byte rows
+    (dict(K=20), mg.MG_ERR_UNSUPPORTED),
+    (dict(contract=0), mg.MG_ERR_UNSUPPORTED),           # STRICT_F32: tensor cores only
+    (dict(contract=0x100 | 1), mg.MG_ERR_UNSUPPORTED),   # no 16-bit outputs
+    (dict(contract=3), mg.MG_ERR_INVALID_ARG),
+    (dict(contract=0x400 | 1), mg.MG_ERR_INVALID_ARG),
+])
+def test_conv_rejects(lib, which, kw, code):
+    assert conv(lib, which, **kw) == code
