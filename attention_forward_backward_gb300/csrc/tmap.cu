@@ -76,3 +76,23 @@ cudaError_t mg_tmap_16_4d(CUtensorMap *m, const void *ptr, const long long dims[
                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
 }
+
+cudaError_t mg_tmap_f32_nd(CUtensorMap *m, const void *ptr, int rank, const long long *dims,
+                           const long long *strides_bytes, const int *box) {
+  EncodeTiledFn fn = encode_fn();
+  if (!fn) return cudaErrorNotSupported;
+  if (rank < 2 || rank > 5 || box[0] != 32) return cudaErrorInvalidValue;
+  cuuint64_t d[5], st[4];
+  cuuint32_t b[5], estr[5];
+  for (int i = 0; i < rank; ++i) {
+    if (dims[i] < 1 || box[i] < 1 || box[i] > 256) return cudaErrorInvalidValue;
+    d[i] = static_cast<cuuint64_t>(dims[i]);
+    b[i] = static_cast<cuuint32_t>(box[i]);
+    estr[i] = 1;
+  }
+  for (int i = 0; i + 1 < rank; ++i) st[i] = static_cast<cuuint64_t>(strides_bytes[i]);
+  CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, rank, const_cast<void *>(ptr), d, st, b,
+                  estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                  CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
+}

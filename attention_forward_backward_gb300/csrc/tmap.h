@@ -23,3 +23,8 @@ cudaError_t mg_tmap_f32(CUtensorMap *m, const void *ptr, int D, int L, int BH, i
 // swizzle, zero fill out of bounds (channels-last convolution operands).
 cudaError_t mg_tmap_16_4d(CUtensorMap *m, const void *ptr, const long long dims[4],
                           const long long strides_bytes[3], const int box[4], bool f16);
+// f32 tensor of rank 3 or 4 (dims[0] innermost, contiguous; strides in bytes of
+// dims 1.., multiples of 16), boxes of 32 x box[1] x ... elements, 128-byte
+// swizzle (accumulator tiles staged in shared memory and stored or add-reduced).
+cudaError_t mg_tmap_f32_nd(CUtensorMap *m, const void *ptr, int rank, const long long *dims,
+                           const long long *strides_bytes, const int *box);

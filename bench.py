@@ -70,6 +70,8 @@ def parse():
                          "(mg_attn_fwd_decode) beside mg_attn_fwd_ex on the same inputs")
     ap.add_argument("--conv", action="store_true",
                     help="time the convolution derivatives on the ResNet-50 layer set instead")
+    ap.add_argument("--conv-layers", default=None,
+                    help="with --conv: comma-separated layer ids of the ResNet-50 set")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-configs", action="store_true",
                     help="skip the compact per-config table (configurations 1-4) of the default run")
@@ -661,7 +663,8 @@ def run_decode(args):
     return 0
 
 
-def conv_layers(mg, torch, device, stream, peaks, steps: int, warmup: int, batch: int = 0):
+def conv_layers(mg, torch, device, stream, peaks, steps: int, warmup: int, batch: int = 0,
+                only=None):
     """Both convolution derivatives of every seeded ResNet-50 layer shape (batch
     32 unless `batch`), each timed alone with CUDA events on the call stream, L2
     flushed before every timed call (the median of `steps` calls). Returns per
@@ -671,6 +674,8 @@ def conv_layers(mg, torch, device, stream, peaks, steps: int, warmup: int, batch
     flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=device)
     layers, tot_f, tot_ms = {}, 0.0, 0.0
     for cid, w in synth.CONV_WORKLOADS.items():
+        if only and cid not in only:
+            continue
         if batch:
             w = w.with_batch(batch)
         host = synth.conv_inputs(w, "accel")
@@ -744,7 +749,8 @@ def run_conv(args):
     peaks = load_peaks()
     clocks = ClockSampler(0)
     clocks.start()
-    res = conv_layers(mg, torch, device, stream, peaks, args.steps, args.warmup)
+    only = [int(x) for x in args.conv_layers.split(",")] if args.conv_layers else None
+    res = conv_layers(mg, torch, device, stream, peaks, args.steps, args.warmup, only=only)
     clk = clocks.stop()
     line = {
         "metric": "convolution derivative TFLOP/s on 1 GB300 (input + weight gradients, "
