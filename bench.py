@@ -717,24 +717,24 @@ def conv_layers(mg, torch, device, stream, peaks, steps: int, warmup: int, batch
 
 
 def conv_oracle_sample(seconds: float):
-    """The fp64 oracle's two derivatives on the first layer shape (res2 3x3) at
-    growing batch until about `seconds` of CPU work: TFLOP/s, threads, sample."""
+    """The fp64 oracle's two derivatives of the layer set at batch 32, layer after
+    layer (cycling) until about `seconds` of CPU work: TFLOP/s, threads, sample."""
     from oracle import conv as oc
     import oracle
-    w = synth.CONV_WORKLOADS[1]
-    n, el = 1, 0.0
-    while True:
-        ww = w.with_batch(n)
-        v = {k: x["values"] for k, x in synth.conv_inputs(ww, "accel").items()}
+    flops, el, done = 0.0, 0.0, []
+    ids = sorted(synth.CONV_WORKLOADS)
+    while el < seconds and len(done) < 4 * len(ids):
+        w = synth.CONV_WORKLOADS[ids[len(done) % len(ids)]]
+        v = {k: x["values"] for k, x in synth.conv_inputs(w, "accel").items()}
         t0 = time.perf_counter()
-        oc.conv2d_grad_input(v["dY"], v["Wt"], ww.H, ww.W, ww.stride, ww.pad)
-        oc.conv2d_grad_weight(v["X"], v["dY"], ww.R, ww.S, ww.stride, ww.pad)
-        el = time.perf_counter() - t0
-        if el >= seconds / 3 or n >= 32:
-            break
-        n *= 2
-    return (2 * ww.flops() / el / 1e12, oracle.max_threads(),
-            f"both derivatives of {ww.name} ({el:.1f} s)")
+        oc.conv2d_grad_input(v["dY"], v["Wt"], w.H, w.W, w.stride, w.pad)
+        oc.conv2d_grad_weight(v["X"], v["dY"], w.R, w.S, w.stride, w.pad)
+        el += time.perf_counter() - t0
+        flops += 2 * w.flops()
+        done.append(w.cid)
+    return (flops / el / 1e12, oracle.max_threads(),
+            f"both derivatives of {len(done)} layers of the set at batch 32, "
+            f"{flops / 1e9:.0f} GFLOP in {el:.1f} s")
 
 
 def run_conv(args):
