@@ -18,7 +18,7 @@
 namespace {
 
 constexpr int kMaxDevices = 64;
-constexpr int kMaxSlots = 48;
+constexpr int kMaxSlots = 64;
 
 // Device error word: bounded waits in the ACCEL kernels write a code here
 // instead of trapping. One copy per device (module globals are per context).
@@ -330,7 +330,8 @@ size_t mg_attn_fwd_decode_workspace_bytes(int B, int H, int Lq, int Lk, int D, i
   if (check_common(B, H, Lq, Lk, D, MG_MASK_NONE, 1.f, contract) != MG_OK) return 0;
   if (Lq > mg_decode_max_rows()) return 0;
   const MgProblem p = make_problem(B, H, Lq, Lk, D, MG_MASK_NONE, 1.f);
-  return (mg_decode_workspace_floats(p) * sizeof(float) + 255) & ~static_cast<size_t>(255);
+  return (mg_decode_workspace_floats(p, !is_strict(contract)) * sizeof(float) + 255) &
+         ~static_cast<size_t>(255);
 }
 
 int mg_attn_fwd_decode(const void *Q, const void *K, const void *V, void *O, float *LSE, int B,
@@ -351,12 +352,14 @@ int mg_attn_fwd_decode(const void *Q, const void *K, const void *V, void *O, flo
   const Range out[] = {rng(O, nq * 4), rng(LSE, static_cast<size_t>(B) * H * Lq * 4),
                        rng(workspace, need)};
   if ((rc = check_alias(in, 3, out, 3))) return rc;
-  const MgProblem p = make_problem(B, H, Lq, Lk, D, mask, scale);
+  const MgProblem p = make_problem(B, H, Lq, Lk, D, mask, scale, nullptr, contract);
+  unsigned int *err = device_error_word();
+  if (!err) return MG_ERR_CUDA;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   ProfScope ps(MGK_DECODE_FWD, st);
   return map_cuda(mg_launch_decode_fwd(Q, K, V, static_cast<float *>(O), LSE,
                                        static_cast<float *>(workspace), p,
-                                       contract & MG_CONTRACT_BASE_MASK, st));
+                                       contract & MG_CONTRACT_BASE_MASK, err, st));
 }
 
 size_t mg_attn_bwd_workspace_bytes_ex(int B, int H, int Lq, int Lk, int D, int contract) {

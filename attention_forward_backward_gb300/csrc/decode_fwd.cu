@@ -7,16 +7,18 @@
 // Training and Inference through Vulkan and Metal", Section 3.1) for Lq <= 8
 // query rows. With so few rows the work is one pass over K and V, bound by HBM,
 // and the generic kernels leave most SMs idle when there are few heads: splitting
-// the keys lets every SM stream its share. Arithmetic is f32 on the CUDA cores for
-// both contracts (bf16 inputs are widened on load) with K, V and Q held in
-// registers, never staged in shared memory; scores are in base 2 with
+// the keys lets every SM stream its share. This file holds the STRICT_F32 partial
+// kernel (f32 FFMA on the CUDA cores, K, V and Q in registers, never staged in
+// shared memory), the merge shared by both contracts, and the split policy; the
+// 16-bit contracts compute their partials on the tensor cores (decode_tc.cu).
+// Scores are in base 2 with
 // scale * log2(e) folded into Q, and every partial state is the exact
 // online-softmax state of its keys, so merging is exact up to rounding:
 //   m = max_s m_s,  l = sum_s l_s 2^(m_s - m),  O = sum_s O_s 2^(m_s - m) / l,
 //   LSE = ln 2 (m + log2 l);  a row with no allowed key gets O = 0, LSE = -inf.
 #include <math.h>
 
-#include <cuda_fp16.h>
+#include <algorithm>
 
 #include "internal.h"
 
@@ -27,15 +29,11 @@ constexpr float kLn2F = 0.6931471805599453f;
 constexpr int kMaxLq = 8;   // query rows per head handled here
 constexpr int kTile = 32;   // split lengths are whole multiples of this many keys
 constexpr int kThreads = 128;
+constexpr int kMaxSplits = 256;  // the split policies never exceed this
 
 __device__ __forceinline__ float load_in(const float *p, size_t i) { return p[i]; }
-__device__ __forceinline__ float load_in(const __nv_bfloat16 *p, size_t i) {
-  return __bfloat162float(p[i]);
-}
-__device__ __forceinline__ float load_in(const __half *p, size_t i) { return __half2float(p[i]); }
-
 // Eight consecutive input elements as raw registers (16-byte loads): fetched one
-// step ahead, widened to f32 registers when the step uses them.
+// step ahead, copied to the f32 registers the step uses.
 template <typename TIn> struct Raw8;
 template <> struct Raw8<float> {
   float4 a, b;
@@ -49,43 +47,6 @@ template <> struct Raw8<float> {
     dst[4] = b.x; dst[5] = b.y; dst[6] = b.z; dst[7] = b.w;
   }
 };
-template <> struct Raw8<__nv_bfloat16> {
-  uint4 u;
-  __device__ __forceinline__ void load(const __nv_bfloat16 *p) {
-    u = *reinterpret_cast<const uint4 *>(p);
-  }
-  __device__ __forceinline__ void zero() { u = make_uint4(0u, 0u, 0u, 0u); }
-  __device__ __forceinline__ void put(float *dst) const {
-    const unsigned w[4] = {u.x, u.y, u.z, u.w};
-#pragma unroll
-    for (int k = 0; k < 4; ++k) {  // bf16 -> f32 is a 16-bit shift
-      dst[2 * k] = __uint_as_float(w[k] << 16);
-      dst[2 * k + 1] = __uint_as_float(w[k] & 0xffff0000u);
-    }
-  }
-};
-
-template <> struct Raw8<__half> {
-  uint4 u;
-  __device__ __forceinline__ void load(const __half *p) { u = *reinterpret_cast<const uint4 *>(p); }
-  __device__ __forceinline__ void zero() { u = make_uint4(0u, 0u, 0u, 0u); }
-  __device__ __forceinline__ void put(float *dst) const {
-    const unsigned w[4] = {u.x, u.y, u.z, u.w};
-#pragma unroll
-    for (int k = 0; k < 4; ++k) {
-      const float2 f = __half22float2(*reinterpret_cast<const __half2 *>(&w[k]));
-      dst[2 * k] = f.x;
-      dst[2 * k + 1] = f.y;
-    }
-  }
-};
-
-__device__ __forceinline__ float warp_max(float v) {
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
-  return v;
-}
-
 // One CTA of four warps: head bh, keys [k_begin, k_end). Nothing is staged in
 // shared memory: a key row of D elements is spread over LPR = D / 8 lanes (eight
 // consecutive elements each, one 16-byte load for bf16, two for f32), so a warp
@@ -246,133 +207,185 @@ __global__ void __launch_bounds__(kThreads)
   }
 }
 
-// One CTA per (bh, q): merge the S partial records. Thread (slot, c4) adds the
-// records of splits slot, slot + SLOTS, ... for elements 4 c4 .. 4 c4 + 3; the
-// slots are summed in shared memory.
+// One CTA of D threads per (bh, q) merges the S partial records in two passes
+// (each a few memory round trips, not one per record): the threads read the
+// splits' (m, l) pairs and reduce m = max_s m_s and l = sum_s l_s 2^(m_s - m),
+// keeping the weights w_s = 2^(m_s - m) in shared memory; then thread d adds
+// O_s[d] w_s over the splits, sixteen records in flight. Launched as a
+// programmatic dependent of the partial kernel: it may be scheduled before the
+// partials finish and waits for them here.
 template <int D>
-__global__ void __launch_bounds__(kThreads)
+__global__ void __launch_bounds__(D)
     decode_merge_kernel(const float *__restrict__ part, float *__restrict__ O,
                         float *__restrict__ LSE, int Lq, int S) {
-  constexpr int TPR = D / 4;
-  constexpr int SLOTS = kThreads / TPR;
-  __shared__ float sRed[kThreads / 32];
-  __shared__ float sAcc[SLOTS][D];
-  __shared__ float sL[SLOTS];
-  const int bh = blockIdx.x / Lq, q = blockIdx.x % Lq;
-  const int tid = threadIdx.x, slot = tid / TPR, c4 = tid % TPR;
+  constexpr int NW = D / 32;
+  __shared__ float sW[kMaxSplits];
+  __shared__ float sRed[NW];
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+  const int bh = blockIdx.x / Lq, q = blockIdx.x % Lq, d = threadIdx.x;
+  const int lane = d & 31, wid = d >> 5;
   const size_t rstride = static_cast<size_t>(Lq) * (D + 4);
   const float *rec0 = part + static_cast<size_t>(bh) * S * rstride + q * (D + 4);
-
+  // pass 1: maximum over the splits (a split with no allowed key has m = -inf)
   float mx = -INFINITY;
-  for (int s = tid; s < S; s += kThreads) mx = fmaxf(mx, rec0[s * rstride + D]);
-  mx = warp_max(mx);
-  if ((tid & 31) == 0) sRed[tid >> 5] = mx;
+  for (int sp = d; sp < S; sp += D) {
+    const float m = rec0[sp * rstride + D];
+    sW[sp] = m;
+    mx = fmaxf(mx, m);
+  }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+  if (lane == 0) sRed[wid] = mx;
   __syncthreads();
   mx = sRed[0];
 #pragma unroll
-  for (int w = 1; w < kThreads / 32; ++w) mx = fmaxf(mx, sRed[w]);
-
-  float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-  float ls = 0.f;
-  if (mx != -INFINITY) {
-#pragma unroll 4
-    for (int s = slot; s < S; s += SLOTS) {
-      const float *r = rec0 + s * rstride;
-      const float w = exp2f(r[D] - mx);  // a split with no allowed key has m = -inf: w = 0
-      ls = fmaf(r[D + 1], w, ls);
-      const float4 v = *reinterpret_cast<const float4 *>(r + 4 * c4);
-      acc.x = fmaf(v.x, w, acc.x);
-      acc.y = fmaf(v.y, w, acc.y);
-      acc.z = fmaf(v.z, w, acc.z);
-      acc.w = fmaf(v.w, w, acc.w);
-    }
-  }
-  sAcc[slot][4 * c4] = acc.x;
-  sAcc[slot][4 * c4 + 1] = acc.y;
-  sAcc[slot][4 * c4 + 2] = acc.z;
-  sAcc[slot][4 * c4 + 3] = acc.w;
-  if (c4 == 0) sL[slot] = ls;
+  for (int w = 1; w < NW; ++w) mx = fmaxf(mx, sRed[w]);
   __syncthreads();
-  const size_t row = static_cast<size_t>(bh) * Lq + q;
-  float lsum = 0.f;
-#pragma unroll
-  for (int k = 0; k < SLOTS; ++k) lsum += sL[k];
-  for (int d = tid; d < D; d += kThreads) {
-    float t = 0.f;
-#pragma unroll
-    for (int k = 0; k < SLOTS; ++k) t += sAcc[k][d];
-    O[row * D + d] = lsum > 0.f ? t / lsum : 0.f;
+  float ls = 0.f;
+  for (int sp = d; sp < S; sp += D) {
+    const float w = mx == -INFINITY ? 0.f : exp2f(sW[sp] - mx);  // m_s = -inf: 0
+    sW[sp] = w;
+    ls = fmaf(rec0[sp * rstride + D + 1], w, ls);
   }
-  if (tid == 0) LSE[row] = lsum > 0.f ? (mx + log2f(lsum)) * kLn2F : -INFINITY;
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) ls += __shfl_xor_sync(0xffffffffu, ls, o);
+  if (lane == 0) sRed[wid] = ls;
+  __syncthreads();
+  ls = 0.f;
+#pragma unroll
+  for (int w = 0; w < NW; ++w) ls += sRed[w];
+  // pass 2: element d
+  float acc = 0.f;
+  for (int s0 = 0; s0 < S; s0 += 16) {
+    float v[16];
+#pragma unroll
+    for (int u = 0; u < 16; ++u)
+      v[u] = s0 + u < S ? rec0[static_cast<size_t>(s0 + u) * rstride + d] : 0.f;
+#pragma unroll
+    for (int u = 0; u < 16; ++u)
+      if (s0 + u < S) acc = fmaf(v[u], sW[s0 + u], acc);
+  }
+  const size_t row = static_cast<size_t>(bh) * Lq + q;
+  O[row * D + d] = ls > 0.f ? acc / ls : 0.f;
+  if (d == 0) LSE[row] = ls > 0.f ? (mx + log2f(ls)) * kLn2F : -INFINITY;
 }
 
 template <int D, int LQ, typename TIn>
-cudaError_t launch(const TIn *Q, const TIn *K, const TIn *V, float *O, float *LSE, float *part,
-                   const MgProblem &p, int S, int chunk, cudaStream_t st) {
+cudaError_t launch(const TIn *Q, const TIn *K, const TIn *V, float *part, const MgProblem &p,
+                   int S, int chunk, cudaStream_t st) {
   const int BH = p.B * p.H;
   decode_partial_kernel<D, LQ, TIn>
       <<<static_cast<unsigned>(static_cast<long long>(BH) * S), kThreads, 0, st>>>(
           Q, K, V, part, p.L, p.Lk, p.causal, p.off, S, chunk, p.scale * kLog2eF);
-  cudaError_t e = cudaGetLastError();
-  if (e != cudaSuccess) return e;
-  decode_merge_kernel<D><<<static_cast<unsigned>(static_cast<long long>(BH) * p.L), kThreads, 0,
-                           st>>>(part, O, LSE, p.L, S);
   return cudaGetLastError();
 }
 
 template <int D, typename TIn>
-cudaError_t launch_rows(const TIn *Q, const TIn *K, const TIn *V, float *O, float *LSE,
-                        float *part, const MgProblem &p, int S, int chunk, cudaStream_t st) {
-  if (p.L <= 1) return launch<D, 1, TIn>(Q, K, V, O, LSE, part, p, S, chunk, st);
-  if (p.L <= 2) return launch<D, 2, TIn>(Q, K, V, O, LSE, part, p, S, chunk, st);
-  if (p.L <= 4) return launch<D, 4, TIn>(Q, K, V, O, LSE, part, p, S, chunk, st);
-  return launch<D, 8, TIn>(Q, K, V, O, LSE, part, p, S, chunk, st);
+cudaError_t launch_rows(const TIn *Q, const TIn *K, const TIn *V, float *part, const MgProblem &p,
+                        int S, int chunk, cudaStream_t st) {
+  if (p.L <= 1) return launch<D, 1, TIn>(Q, K, V, part, p, S, chunk, st);
+  if (p.L <= 2) return launch<D, 2, TIn>(Q, K, V, part, p, S, chunk, st);
+  if (p.L <= 4) return launch<D, 4, TIn>(Q, K, V, part, p, S, chunk, st);
+  return launch<D, 8, TIn>(Q, K, V, part, p, S, chunk, st);
+}
+
+// The merge, launched with programmatic stream serialisation so that its launch
+// overlaps the end of the partial kernel (it waits for the partials itself).
+template <int D>
+cudaError_t merge(const float *part, float *O, float *LSE, const MgProblem &p, int S,
+                  cudaStream_t st) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(static_cast<unsigned>(static_cast<long long>(p.B) * p.H * p.L));
+  cfg.blockDim = dim3(D);
+  cfg.dynamicSmemBytes = 0;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, decode_merge_kernel<D>, part, O, LSE, p.L, S);
+}
+
+template <int D>
+cudaError_t partial_f32(const void *Q, const void *K, const void *V, float *part,
+                        const MgProblem &p, int S, int chunk, cudaStream_t st) {
+  return launch_rows<D, float>(static_cast<const float *>(Q), static_cast<const float *>(K),
+                               static_cast<const float *>(V), part, p, S, chunk, st);
 }
 
 }  // namespace
 
 int mg_decode_max_rows() { return kMaxLq; }
 
-// Splits of the key axis: about eight CTAs per SM of the current device (its SM
-// count is read once per device), at least 256 keys per split. Depends only on
-// the shape and the device, so the workspace query and the call agree.
-void mg_decode_split(const MgProblem &p, int *S, int *chunk) {
+// Splits of the key axis. Depends only on the shape, the kernel family and the
+// device (its SM count is read once per device), so the workspace query and the
+// call agree.
+// * CUDA-core kernel: about eight CTAs per SM, at least 256 keys per split,
+//   split lengths in whole 32-key steps.
+// * tensor-core kernel (one CTA per SM): the split count s minimising
+//   waves(s) * (c0 + Lk / s), waves(s) = ceil(B H s / SMs), with c0 = 256 keys
+//   standing for a CTA's fixed cost (set-up, pipeline fill, record); at least
+//   512 keys per split, split lengths in whole 128-key tiles.
+void mg_decode_split(const MgProblem &p, int *S, int *chunk, bool tc) {
   const long long BH = static_cast<long long>(p.B) * p.H;
-  const int want = static_cast<int>((8LL * mg_sm_count() + BH - 1) / BH);
-  const int maxs = (p.Lk + 255) / 256;
-  int s = want < 1 ? 1 : want;
-  if (s > maxs) s = maxs;
-  if (s > 256) s = 256;
-  const int c = ((p.Lk + s - 1) / s + kTile - 1) / kTile * kTile;
+  const int sms = mg_sm_count();
+  int s, step;
+  if (tc) {
+    step = 128;
+    const int maxs = std::max(1, std::min(kMaxSplits, (p.Lk + 511) / 512));
+    double best = 0.0;
+    s = 1;
+    for (int t = 1; t <= maxs; ++t) {
+      const long long waves = (BH * t + sms - 1) / sms;
+      const double cost = static_cast<double>(waves) * (256.0 + static_cast<double>(p.Lk) / t);
+      if (t == 1 || cost < best) {
+        best = cost;
+        s = t;
+      }
+    }
+  } else {
+    step = kTile;
+    const int want = static_cast<int>((8LL * sms + BH - 1) / BH);
+    const int maxs = (p.Lk + 255) / 256;
+    s = want < 1 ? 1 : want;
+    if (s > maxs) s = maxs;
+    if (s > kMaxSplits) s = kMaxSplits;
+  }
+  const int c = ((p.Lk + s - 1) / s + step - 1) / step * step;
   *S = (p.Lk + c - 1) / c;
   *chunk = c;
 }
 
-size_t mg_decode_workspace_floats(const MgProblem &p) {
+size_t mg_decode_workspace_floats(const MgProblem &p, bool tc) {
   int S, chunk;
-  mg_decode_split(p, &S, &chunk);
+  mg_decode_split(p, &S, &chunk, tc);
   return static_cast<size_t>(p.B) * p.H * S * p.L * (p.D + 4);
-}
-
-template <typename T>
-cudaError_t dispatch_d(const void *Q, const void *K, const void *V, float *O, float *LSE,
-                       float *part, const MgProblem &p, int S, int chunk, cudaStream_t st) {
-  const T *q = static_cast<const T *>(Q), *k = static_cast<const T *>(K),
-          *v = static_cast<const T *>(V);
-  switch (p.D) {
-    case 32: return launch_rows<32, T>(q, k, v, O, LSE, part, p, S, chunk, st);
-    case 64: return launch_rows<64, T>(q, k, v, O, LSE, part, p, S, chunk, st);
-    case 128: return launch_rows<128, T>(q, k, v, O, LSE, part, p, S, chunk, st);
-    default: return cudaErrorInvalidValue;
-  }
 }
 
 cudaError_t mg_launch_decode_fwd(const void *Q, const void *K, const void *V, float *O,
                                  float *LSE, float *part, const MgProblem &p, int in_type,
-                                 cudaStream_t st) {
+                                 unsigned int *err, cudaStream_t st) {
   int S, chunk;
-  mg_decode_split(p, &S, &chunk);
-  if (in_type == 1) return dispatch_d<__nv_bfloat16>(Q, K, V, O, LSE, part, p, S, chunk, st);
-  if (in_type == 2) return dispatch_d<__half>(Q, K, V, O, LSE, part, p, S, chunk, st);
-  return dispatch_d<float>(Q, K, V, O, LSE, part, p, S, chunk, st);
+  cudaError_t e;
+  if (in_type == 1 || in_type == 2) {
+    // 16-bit inputs: both products on the tensor cores
+    mg_decode_split(p, &S, &chunk, true);
+    e = mg_launch_decode_tc_partial(Q, K, V, part, p, S, chunk, err, st);
+  } else {
+    mg_decode_split(p, &S, &chunk, false);
+    switch (p.D) {
+      case 32: e = partial_f32<32>(Q, K, V, part, p, S, chunk, st); break;
+      case 64: e = partial_f32<64>(Q, K, V, part, p, S, chunk, st); break;
+      case 128: e = partial_f32<128>(Q, K, V, part, p, S, chunk, st); break;
+      default: return cudaErrorInvalidValue;
+    }
+  }
+  if (e != cudaSuccess) return e;
+  switch (p.D) {
+    case 32: return merge<32>(part, O, LSE, p, S, st);
+    case 64: return merge<64>(part, O, LSE, p, S, st);
+    case 128: return merge<128>(part, O, LSE, p, S, st);
+    default: return cudaErrorInvalidValue;
+  }
 }

@@ -112,12 +112,11 @@ uint64_t mg_wait_limit_ns();
 // Split-key forward for at most mg_decode_max_rows() query rows (decoding). The
 // partial records need mg_decode_workspace_floats() floats of scratch.
 int mg_decode_max_rows();
-void mg_decode_split(const MgProblem &p, int *S, int *chunk);
-size_t mg_decode_workspace_floats(const MgProblem &p);
-// in_type: 0 f32, 1 bf16, 2 f16 inputs (the contract's base value).
+void mg_decode_split(const MgProblem &p, int *S, int *chunk, bool tc);
+size_t mg_decode_workspace_floats(const MgProblem &p, bool tc);
 cudaError_t mg_launch_decode_fwd(const void *Q, const void *K, const void *V, float *O,
                                  float *LSE, float *part, const MgProblem &p, int in_type,
-                                 cudaStream_t st);
+                                 unsigned int *err, cudaStream_t st);
 
 // The argument checks every compute call starts with (sizes, mask, scale,
 // contract, head dim), in the same order: MG_OK or the mg_status_t to return.
@@ -154,3 +153,9 @@ cudaError_t mg_launch_conv_dgrad(const void *dY, const void *Wt, float *dX,
 // dW += the weight gradient from X and dY (f32; the caller zeroes dW first).
 cudaError_t mg_launch_conv_wgrad(const void *X, const void *dY, float *dW,
                                  const MgConvProblem &p, unsigned int *err, cudaStream_t st);
+
+// Partial records of the split-key forward with both products on the tensor
+// cores (16-bit inputs; the split from mg_decode_split(..., true)).
+cudaError_t mg_launch_decode_tc_partial(const void *Q, const void *K, const void *V, float *part,
+                                        const MgProblem &p, int S, int chunk, unsigned int *err,
+                                        cudaStream_t st);

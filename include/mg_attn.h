@@ -269,18 +269,22 @@ size_t mg_attn_fwd_decode_workspace_bytes(int B, int H, int Lq, int Lk, int D, i
  * schedule: the key axis is split over many CTAs, each of which keeps the
  * running max, sum and unnormalised output of its keys (the online softmax of
  * the tiled forward archetype, Section 3.3 of the paper), and a second kernel
- * merges the splits. The split count depends on (B, H, Lk) only.
- *   Q, O       [B][H][Lq][D] (Q f32 or bf16 by contract, O f32), Lq in [1, 8]
+ * merges the splits. The split count depends on (B, H, Lk), the contract
+ * family (f32 or 16-bit) and the device's SM count only.
+ *   Q, O       [B][H][Lq][D] (Q f32, bf16 or f16 by contract, O f32), Lq in [1, 8]
  *   K, V       [B][H][Lk][D]
  *   LSE        out [B][H][Lq] f32
  *   mask       mg_mask_t; rows with no allowed key get O = 0, LSE = -inf
  *   workspace  scratch of at least mg_attn_fwd_decode_workspace_bytes() bytes,
  *              16-byte aligned, not overlapping any tensor; contents on entry do
  *              not matter
- * Both contracts compute in f32 on the CUDA cores (bf16 inputs are widened on
- * load); the work is one pass over K and V and is bound by HBM, not by the
- * tensor cores. Lq > 8 returns MG_ERR_UNSUPPORTED (use mg_attn_fwd_ex). Other
- * preconditions, ownership and errors as mg_attn_fwd_ex.
+ * The work is one pass over K and V, bound by HBM. STRICT_F32 computes in f32
+ * on the CUDA cores (FFMA). The ACCEL contracts compute S = Q K^T and P V on the
+ * tensor cores: keys on the MMA's M axis, the query rows padded to N = 16, f32
+ * accumulation, P rounded to the 16-bit input type as the operand (as in
+ * mg_attn_fwd), the softmax in f32. Lq > 8 returns MG_ERR_UNSUPPORTED (use
+ * mg_attn_fwd_ex). Other preconditions, ownership and errors as mg_attn_fwd_ex;
+ * a bounded wait that gives up is reported by mg_get_device_error().
  */
 int mg_attn_fwd_decode(const void *Q, const void *K, const void *V, void *O, float *LSE,
                        int B, int H, int Lq, int Lk, int D, int mask, float scale,

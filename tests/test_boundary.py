@@ -223,13 +223,19 @@ def test_fwd_decode_rejects(lib, kw, code):
 def test_decode_workspace_bytes(lib):
     """One record of D + 4 floats per (head, key split, query row); the split
     count is at least one, at most one per 256 keys, and the size is a multiple
-    of 256 bytes. Worked cases: B=1, H=8, Lk=32768 asks for ceil(1216 / 8) = 152
-    splits, capped at 32768 / 256 = 128 splits of 256 keys: 8 * 128 * 1 * 132
-    floats = 540,672 bytes. B=1, H=8, Lk=100000 keeps 152 splits of
-    ceil(100000 / 152) = 658 -> 672 keys (whole 32-key tiles), which cover the
-    keys in 149 splits: 8 * 149 * 3 * 132 floats (Lq = 3) = 1,888,128 bytes,
-    rounded up to 1,888,256."""
-    assert lib.mg_attn_fwd_decode_workspace_bytes(1, 8, 1, 32768, 128, 1) == 540672
+    of 256 bytes. Worked cases with 152 SMs (the count assumed without a GPU):
+    STRICT_F32, B=1, H=8, Lk=32768 asks for ceil(1216 / 8) = 152 splits, capped
+    at 32768 / 256 = 128 splits of 256 keys: 8 * 128 * 1 * 132 floats = 540,672
+    bytes. B=1, H=8, Lk=100000 keeps 152 splits of ceil(100000 / 152) = 658 ->
+    672 keys (whole 32-key tiles), which cover the keys in 149 splits:
+    8 * 149 * 3 * 132 floats (Lq = 3) = 1,888,128 bytes, rounded up to 1,888,256.
+    The 16-bit contracts (tensor-core partials, one CTA per SM) take the split
+    count s minimising ceil(8 s / 152) * (256 + 32768 / s): s = 19 (one wave),
+    19 splits of 1792 keys (whole 128-key tiles): 8 * 19 * 132 floats = 80,256
+    bytes, rounded up to 80,384."""
+    assert lib.mg_attn_fwd_decode_workspace_bytes(1, 8, 1, 32768, 128, 0) == 540672
+    assert lib.mg_attn_fwd_decode_workspace_bytes(1, 8, 1, 32768, 128, 1) == 80384
+    assert lib.mg_attn_fwd_decode_workspace_bytes(1, 8, 1, 32768, 128, 2) == 80384
     assert lib.mg_attn_fwd_decode_workspace_bytes(1, 8, 3, 100000, 128, 0) == 1888256
     for (B, H, Lq, Lk, D) in [(1, 1, 1, 1, 32), (2, 3, 8, 5000, 64), (4, 32, 3, 100000, 128),
                               (64, 64, 1, 4096, 128)]:

@@ -77,3 +77,30 @@ def test_decode_rejects_nine_rows():
     with pytest.raises(mg.MgError) as ei:
         mg.mg_attn_fwd_decode(x, kv, kv.clone(), O, LSE, "none", 0.125, "strict", ws)
     assert ei.value.status == mg.MG_ERR_UNSUPPORTED
+
+
+@pytest.mark.parametrize("contract", ["accel", "strict"])
+@pytest.mark.parametrize("Lk", [127, 128, 129, 255, 257, 1793])
+def test_decode_tile_edges(Lk, contract):
+    """Key lengths at and around the tensor-core kernel's 128-key tile."""
+    _check(1, 2, 8, Lk, 128, "causal_bottom_right", contract, seed=1150 + Lk % 89)
+
+
+@pytest.mark.parametrize("contract", ["accel", "strict"])
+@pytest.mark.parametrize("mask", ["none", "causal_bottom_right"])
+def test_decode_large_logits(mask, contract):
+    """K scaled by 8 (logit standard deviation about 8 in base e): tile maxima
+    move by far more than the lazy-rescale threshold from tile to tile, so the
+    running reference and the accumulated output are rescaled many times."""
+    B, H, Lq, Lk, D = 2, 2, 8, 3000, 128
+    host = synth.cross_inputs(B, H, Lq, Lk, D, contract, seed_cfg=1160)
+    host.pop("dO")
+    base = synth.base_contract(contract)
+    kv = host["K"] if base == "strict" else host["K"]["values"]
+    host["K"] = synth.encode(np.ascontiguousarray(kv * np.float32(8.0)), contract)
+    dev, vals = device_inputs(host, contract)
+    scale = D ** -0.5
+    got = run_gpu_decode(dev, mask, scale, contract)
+    O, LSE = oracle.attn_fwd_ex(vals["Q"], vals["K"], vals["V"], mask, scale)
+    errs, bad = compare_ex(got, {"O": O, "LSE": LSE}, contract)
+    assert not bad, errs
