@@ -274,9 +274,17 @@ __global__ void __launch_bounds__(320, 1)
         for (int e = 0; e < 128; ++e)
           if (k0 + e > lim) r[e] = __float_as_uint(-INFINITY);
       }
-      float mx = __uint_as_float(r[0]);
+      // row maximum as eight independent chains (18 dependent steps, not 127)
+      float m8[8];
 #pragma unroll
-      for (int e = 1; e < 128; ++e) mx = fmaxf(mx, __uint_as_float(r[e]));
+      for (int i = 0; i < 8; ++i) m8[i] = __uint_as_float(r[i]);
+#pragma unroll
+      for (int e = 8; e < 128; e += 8) {
+#pragma unroll
+        for (int i = 0; i < 8; ++i) m8[i] = fmaxf(m8[i], __uint_as_float(r[e + i]));
+      }
+      const float mx = fmaxf(fmaxf(fmaxf(m8[0], m8[1]), fmaxf(m8[2], m8[3])),
+                             fmaxf(fmaxf(m8[4], m8[5]), fmaxf(m8[6], m8[7])));
       const float mx2 = mx * scale_log2;
       const bool need = mx2 > m_ref + 8.f;
       const bool warp_need = __any_sync(0xffffffffu, need);
@@ -285,14 +293,15 @@ __global__ void __launch_bounds__(320, 1)
       const float m_use = m_new == -INFINITY ? 0.f : m_new;
       // P = exp2(s * scale * log2e - m_new), packed to bf16 (masked scores are -inf -> 0)
       uint32_t pk[64];
-      float rs = 0.f;
+      float rs4[4] = {0.f, 0.f, 0.f, 0.f};  // row sum as four independent chains
 #pragma unroll
       for (int e = 0; e < 64; ++e) {
         const float p0 = ex2(fmaf(__uint_as_float(r[2 * e]), scale_log2, -m_use));
         const float p1 = ex2(fmaf(__uint_as_float(r[2 * e + 1]), scale_log2, -m_use));
-        rs += p0 + p1;
+        rs4[e & 3] += p0 + p1;
         pk[e] = pack16<F16>(p0, p1);
       }
+      const float rs = (rs4[0] + rs4[1]) + (rs4[2] + rs4[3]);
       if (warp_need) {
         const float alpha = m_new == -INFINITY ? 1.f : ex2(m_ref - m_new);
         if (j > 0) {
