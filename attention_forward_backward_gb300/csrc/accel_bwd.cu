@@ -34,11 +34,14 @@
 // At D = 64 dQ_j = dS K has columns and a staging tile of its own.
 //
 // MMA issue order (steady state, block j):
-//   dK(j), dQ(j), dP(j+1), dV(j+1), S(j+2)
+//   D = 128: dK(j), dQ(j), dP(j+1), dV(j+1), S(j+2)
+//   D = 64:  dK(j), dP(j+1), dQ(j), dV(j+1), S(j+2)
 // The softmax turns S(j+1) into P(j+1) while dK(j), dQ(j) and dP(j+1) run, and
 // dP(j+1) into dS(j+1) while dV(j+1) and S(j+2) run. S(j+2) overwrites P(j+1)
-// only after dV(j+1) has read it (issue order); at D = 128 dP(j+1) also waits
-// for the read-out of dQ(j) from the same columns.
+// only after dV(j+1) has read it (issue order); dP(j+1) overwrites dS^T(j) only
+// after dK(j) has read it. At D = 128 dP(j+1) also waits for the read-out of
+// dQ(j) from the same columns; at D = 64 it goes ahead of dQ(j), so that it is
+// done before the softmax warps need it.
 //
 // Warp roles: 0-3 dQ read-out, 4 TMA producer of K, V, Q (plus LSE and Dvec
 // staging), 5 MMA issuer, 6 TMA producer of dO, 8-15 two softmax warpgroups
@@ -386,11 +389,17 @@ __global__ void __launch_bounds__(512, 1)
       }
       for (int i = 0; ok && i < n; ++i) {
         if (!(ok = issue_dK(i))) break;
+        // D = 64: dQ has columns of its own, so dP(i+1) follows dK(i) (the last reader
+        // of dS^T(i) in dP^T's columns) at once and the softmax warps find it done
+        // when they reach dS(i+1). D = 128: dQ(i) is accumulated over dP^T's columns,
+        // so dP(i+1) waits until the dQ warps have read dQ(i) out.
+        if (!C::kDqInDp && i + 1 < n && !(ok = issue_dP(i + 1))) break;
         if (!(ok = issue_dQ(i))) break;
         if (i + 1 < n) {
-          // D = 128: dP^T's columns hold dQ(i) until the dQ warps have read it
-          if (C::kDqInDp && !(ok = mbar_wait(bar(C::B_DQEMPTY), i & 1, ab))) break;
-          if (!(ok = issue_dP(i + 1))) break;
+          if (C::kDqInDp) {
+            if (!(ok = mbar_wait(bar(C::B_DQEMPTY), i & 1, ab))) break;
+            if (!(ok = issue_dP(i + 1))) break;
+          }
           if (!(ok = issue_dV(i + 1))) break;
           if (i + 2 < n && !(ok = issue_S(i + 2))) break;
         }
