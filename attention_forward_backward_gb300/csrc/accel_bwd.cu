@@ -137,6 +137,7 @@ __device__ __forceinline__ void st_shared_v4(uint32_t addr, uint32_t a, uint32_t
                : "memory");
 }
 
+
 __device__ __forceinline__ void st_shared_f32(uint32_t addr, float v) {
   asm volatile("st.shared.f32 [%0], %1;" ::"r"(addr), "f"(v) : "memory");
 }
@@ -420,6 +421,16 @@ __global__ void __launch_bounds__(512, 1)
         tc_fence_after();
         const int q0 = (qb0 + j) * C::BQ;
         const uint32_t stage = sbase + C::OFF_DO + (j % C::NQS) * C::Q_TILE;
+        // this thread's element of query row q of the staged half sits at
+        // rowa[q mod 8] + 1024 (q / 8): the eight swizzled offsets once per block,
+        // so that each element costs one multiply and one store
+        uint32_t rowa[8];
+        {
+          const uint32_t sg = stage + (t >> 5) * C::DQ_BOX + ((t & 3) << 2);
+          const int unit = (t & 31) >> 2;
+#pragma unroll
+          for (int b = 0; b < 8; ++b) rowa[b] = sg + b * 128 + ((unit ^ b) << 4);
+        }
 #pragma unroll
         for (int h = 0; h < 2; ++h) {
           uint32_t r[64];
@@ -438,7 +449,7 @@ __global__ void __launch_bounds__(512, 1)
           }
 #pragma unroll
           for (int q = 0; q < 64; ++q)
-            st_shared_f32(stage + dq_stage_off(q, t, C::DQ_BOX), __uint_as_float(r[q]) * scale);
+            st_shared_f32(rowa[q & 7] + (q >> 3) * 1024, __uint_as_float(r[q]) * scale);
           fence_proxy_async_smem();
           __syncwarp();
           if (lane == 0) {
