@@ -274,14 +274,26 @@ __global__ void __launch_bounds__(320, 1)
         for (int e = 0; e < 128; ++e)
           if (k0 + e > lim) r[e] = __float_as_uint(-INFINITY);
       }
-      // row maximum as eight independent chains (18 dependent steps, not 127)
+      // row maximum as eight independent chains (three-input maxima at D = 128:
+      // about 68 instructions on a 10-step dependent path, not 127 on a 127-step one)
       float m8[8];
+      if constexpr (DP == 128) {
 #pragma unroll
-      for (int i = 0; i < 8; ++i) m8[i] = __uint_as_float(r[i]);
+        for (int i = 0; i < 8; ++i) m8[i] = fmaxf(__uint_as_float(r[i]), __uint_as_float(r[8 + i]));
 #pragma unroll
-      for (int e = 8; e < 128; e += 8) {
+        for (int e = 16; e < 128; e += 16) {
 #pragma unroll
-        for (int i = 0; i < 8; ++i) m8[i] = fmaxf(m8[i], __uint_as_float(r[e + i]));
+          for (int i = 0; i < 8; ++i)
+            m8[i] = fmax3(m8[i], __uint_as_float(r[e + i]), __uint_as_float(r[e + 8 + i]));
+        }
+      } else {
+#pragma unroll
+        for (int i = 0; i < 8; ++i) m8[i] = __uint_as_float(r[i]);
+#pragma unroll
+        for (int e = 8; e < 128; e += 8) {
+#pragma unroll
+          for (int i = 0; i < 8; ++i) m8[i] = fmaxf(m8[i], __uint_as_float(r[e + i]));
+        }
       }
       const float mx = fmaxf(fmaxf(fmaxf(m8[0], m8[1]), fmaxf(m8[2], m8[3])),
                              fmaxf(fmaxf(m8[4], m8[5]), fmaxf(m8[6], m8[7])));
@@ -291,17 +303,36 @@ __global__ void __launch_bounds__(320, 1)
       const float m_new = warp_need ? fmaxf(m_ref, mx2) : m_ref;
       // a row that has seen no allowed key yet keeps m = -inf; its P is 0
       const float m_use = m_new == -INFINITY ? 0.f : m_new;
-      // P = exp2(s * scale * log2e - m_new), packed to bf16 (masked scores are -inf -> 0)
+      // P = exp2(s * scale * log2e - m_new), packed to 16 bits (masked scores are
+      // -inf -> 0). At D = 128 in pairs: one packed FMA per two exponents' arguments
+      // and one packed add per two terms of the row sum (measured 3% faster there;
+      // at D = 64 the pairs cost registers and the scalar form is kept)
       uint32_t pk[64];
-      float rs4[4] = {0.f, 0.f, 0.f, 0.f};  // row sum as four independent chains
+      float rs;
+      if constexpr (DP == 128) {
+        const uint64_t sc2 = f2pack(scale_log2, scale_log2), nm2 = f2pack(-m_use, -m_use);
+        uint64_t rs2[4] = {0ull, 0ull, 0ull, 0ull};
 #pragma unroll
-      for (int e = 0; e < 64; ++e) {
-        const float p0 = ex2(fmaf(__uint_as_float(r[2 * e]), scale_log2, -m_use));
-        const float p1 = ex2(fmaf(__uint_as_float(r[2 * e + 1]), scale_log2, -m_use));
-        rs4[e & 3] += p0 + p1;
-        pk[e] = pack16<F16>(p0, p1);
+        for (int e = 0; e < 64; ++e) {
+          const float2 t = f2unpack(
+              f2fma(f2pack(__uint_as_float(r[2 * e]), __uint_as_float(r[2 * e + 1])), sc2, nm2));
+          const float p0 = ex2(t.x), p1 = ex2(t.y);
+          rs2[e & 3] = f2add(rs2[e & 3], f2pack(p0, p1));
+          pk[e] = pack16<F16>(p0, p1);
+        }
+        const float2 ra = f2unpack(f2add(rs2[0], rs2[1])), rb = f2unpack(f2add(rs2[2], rs2[3]));
+        rs = (ra.x + ra.y) + (rb.x + rb.y);
+      } else {
+        float rs4[4] = {0.f, 0.f, 0.f, 0.f};  // row sum as four independent chains
+#pragma unroll
+        for (int e = 0; e < 64; ++e) {
+          const float p0 = ex2(fmaf(__uint_as_float(r[2 * e]), scale_log2, -m_use));
+          const float p1 = ex2(fmaf(__uint_as_float(r[2 * e + 1]), scale_log2, -m_use));
+          rs4[e & 3] += p0 + p1;
+          pk[e] = pack16<F16>(p0, p1);
+        }
+        rs = (rs4[0] + rs4[1]) + (rs4[2] + rs4[3]);
       }
-      const float rs = (rs4[0] + rs4[1]) + (rs4[2] + rs4[3]);
       if (warp_need) {
         const float alpha = m_new == -INFINITY ? 1.f : ex2(m_ref - m_new);
         if (j > 0) {
