@@ -253,8 +253,9 @@ __global__ void __launch_bounds__(512, 1)
         break;
 #pragma unroll
       for (int u = 0; u < C::BQ / 32; ++u) {
-        // +inf also for a row with an empty softmax (LSE = -inf): its P is 0
-        sLse[st * C::BQ + 32 * u + lane] = lse_r[u] == -INFINITY ? INFINITY : lse_r[u] * kLog2e;
+        // staged negated (-LSE log2 e), -inf for a row with an empty softmax (LSE =
+        // -inf): its P is 0
+        sLse[st * C::BQ + 32 * u + lane] = lse_r[u] == -INFINITY ? -INFINITY : -lse_r[u] * kLog2e;
         sDv[st * C::BQ + 32 * u + lane] = dv_r[u];
       }
       __syncwarp();
@@ -536,13 +537,21 @@ __global__ void __launch_bounds__(512, 1)
         tmem_ld32(tS, *reinterpret_cast<uint32_t(*)[32]>(r));
         tmem_ld32(tS + 32, *reinterpret_cast<uint32_t(*)[32]>(r + 32));
         tmem_wait_ld();
+        // P = exp2(s * scale * log2e - LSE log2e): the arguments of two exponents per
+        // packed FMA (sm_100+ f32x2) against the negated staged LSE
+        const uint64_t sc2 = f2pack(scale_log2, scale_log2);
 #pragma unroll
         for (int e = 0; e < C::QPW; e += 4) {
           const float4 l4 = *reinterpret_cast<const float4 *>(lse + e);
-          const float lv[4] = {l4.x, l4.y, l4.z, l4.w};
+          const float2 t01 = f2unpack(f2fma(
+              f2pack(__uint_as_float(r[e]), __uint_as_float(r[e + 1])), sc2, f2pack(l4.x, l4.y)));
+          const float2 t23 = f2unpack(f2fma(
+              f2pack(__uint_as_float(r[e + 2]), __uint_as_float(r[e + 3])), sc2,
+              f2pack(l4.z, l4.w)));
+          const float tv[4] = {t01.x, t01.y, t23.x, t23.y};
 #pragma unroll
           for (int u = 0; u < 4; ++u) {
-            float x = ex2(fmaf(__uint_as_float(r[e + u]), scale_log2, -lv[u]));
+            float x = ex2(tv[u]);
             if (need_mask && e + u < lim0) x = 0.f;
             p[e + u] = x;
           }
@@ -572,12 +581,19 @@ __global__ void __launch_bounds__(512, 1)
 #pragma unroll
         for (int e = 0; e < 16; e += 2) {
           const float4 d4 = *reinterpret_cast<const float4 *>(dvq + 32 * c + 2 * e);
-          const float a0 = p[32 * c + 2 * e] * (__uint_as_float(r[2 * e]) - d4.x);
-          const float a1 = p[32 * c + 2 * e + 1] * (__uint_as_float(r[2 * e + 1]) - d4.y);
-          const float a2 = p[32 * c + 2 * e + 2] * (__uint_as_float(r[2 * e + 2]) - d4.z);
-          const float a3 = p[32 * c + 2 * e + 3] * (__uint_as_float(r[2 * e + 3]) - d4.w);
-          pk[e] = pack16<F16>(a0, a1);
-          pk[e + 1] = pack16<F16>(a2, a3);
+          const int q = 32 * c + 2 * e;
+          // dS = P (dP - Dvec) in pairs: one packed subtract and one packed multiply
+          // per two elements (sm_100+ f32x2)
+          const float2 a01 = f2unpack(f2mul(
+              f2pack(p[q], p[q + 1]),
+              f2sub(f2pack(__uint_as_float(r[2 * e]), __uint_as_float(r[2 * e + 1])),
+                    f2pack(d4.x, d4.y))));
+          const float2 a23 = f2unpack(f2mul(
+              f2pack(p[q + 2], p[q + 3]),
+              f2sub(f2pack(__uint_as_float(r[2 * e + 2]), __uint_as_float(r[2 * e + 3])),
+                    f2pack(d4.z, d4.w))));
+          pk[e] = pack16<F16>(a01.x, a01.y);
+          pk[e + 1] = pack16<F16>(a23.x, a23.y);
         }
         tmem_st16(tDP + 16 * c, pk);
         // dS^T row kr, queries ql .. ql+31 into the swizzled smem tile
