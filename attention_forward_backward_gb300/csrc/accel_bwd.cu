@@ -16,16 +16,17 @@
 //   P^T  = exp2(S^T scale log2e - LSE_j log2e), masked        (softmax warps)
 //   dV  += P^T dO_j           (A = P^T from TMEM, bf16)
 //   dS^T = P^T (dP^T - Dvec_j)                                (softmax warps)
-//   dK  += dS^T Q_j           (A = dS^T from TMEM, bf16)
-//   dQ_j = dS K               (dS^T also staged in shared memory)
+//   dK  += dS^T Q_j           (A = dS^T: from TMEM at D = 64, from the
+//                              shared-memory staging tile at D = 128; bf16)
+//   dQ_j = dS K               (dS^T staged in shared memory)
 // Every product is a 128 x 128 (D = 128) or 128 x 64 (D = 64) MMA group, so one
 // issuing thread keeps up with the tensor core and each byte an operand moves
 // through shared memory feeds twice the flops of 64-row query blocks.
 //
 // Tensor memory (512 columns) holds dV, dK, S^T and dP^T. At D = 128 that is
 // all of it, so dQ_j^T = K^T dS_j^T is accumulated over the dP^T columns once
-// dK_j has read dS_j^T from them (MMAs of one thread run in issue order), and
-// dP_{j+1} waits until the dQ warps have read dQ_j^T out. Those warps stage it
+// the softmax has read dP_j from them, and dP_{j+1} waits until the dQ warps
+// have read dQ_j^T out. Those warps stage it
 // in dO_j's ring stage (dead once dP_j and dV_j, which precede dQ_j, are done),
 // 64 query rows at a time, each warp one 32-column box of d, and add it into
 // global dQ with TMA tensor add-reductions; the stage returns to the dO
@@ -34,14 +35,16 @@
 // At D = 64 dQ_j = dS K has columns and a staging tile of its own.
 //
 // MMA issue order (steady state, block j):
-//   D = 128: dK(j), dQ(j), dP(j+1), dV(j+1), S(j+2)
+//   D = 128: dQ(j), dK(j), dP(j+1), dV(j+1), S(j+2)
 //   D = 64:  dK(j), dP(j+1), dQ(j), dV(j+1), S(j+2)
-// The softmax turns S(j+1) into P(j+1) while dK(j), dQ(j) and dP(j+1) run, and
+// The softmax turns S(j+1) into P(j+1) while the products of block j run, and
 // dP(j+1) into dS(j+1) while dV(j+1) and S(j+2) run. S(j+2) overwrites P(j+1)
-// only after dV(j+1) has read it (issue order); dP(j+1) overwrites dS^T(j) only
-// after dK(j) has read it. At D = 128 dP(j+1) also waits for the read-out of
-// dQ(j) from the same columns; at D = 64 it goes ahead of dQ(j), so that it is
-// done before the softmax warps need it.
+// only after dV(j+1) has read it (issue order). At D = 128 dK(j) reads dS^T(j)
+// from the shared-memory staging tile (dQ's operand too), so dQ(j) goes first
+// into dP^T's columns, dK(j) runs while the dQ warps read dQ(j) out, and dP(j+1)
+// waits for that read-out; at D = 64 dK(j) reads dS^T(j) from dP^T's columns and
+// dP(j+1) follows it at once, ahead of dQ(j), so that it is done before the
+// softmax warps need it.
 //
 // Warp roles: 0-3 dQ read-out, 4 TMA producer of K, V, Q (plus LSE and Dvec
 // staging), 5 MMA issuer, 6 TMA producer of dO, 8-15 two softmax warpgroups
@@ -355,15 +358,32 @@ __global__ void __launch_bounds__(512, 1)
         if (!C::kDqInDp) mma_commit(bar(C::B_DOFREE + j % C::NQS));
         return true;
       };
+      // dK += dS^T Q_j. D = 64: A = dS^T from dP^T's columns (bf16, TMEM). D = 128:
+      // A = dS^T from the shared-memory staging tile (K-major: key rows, 64-query
+      // chunks), so that dQ(j) may go first and overwrite dP^T's columns at once.
+      const uint64_t dDSk = sdesc_sw128(sb + C::OFF_DS, 0, 1024);
       auto issue_dK = [&](int j) -> bool {
-        if (!mbar_wait(bar(C::B_DSREADY), j & 1, ab)) return false;
+        if (!C::kDqInDp && !mbar_wait(bar(C::B_DSREADY), j & 1, ab)) return false;
         tc_fence_after();
-        issue_acc(tmem + C::T_DP, sdesc_add(dQmn, (j % C::NQS) * C::Q_TILE), tmem + C::T_DK,
-                  j == 0);
+        if constexpr (C::kDqInDp) {
+          const uint64_t dA = opaque_u64(dDSk);
+          const uint64_t dY = opaque_u64(sdesc_add(dQmn, (j % C::NQS) * C::Q_TILE));
+#pragma unroll
+          for (int kk = 0; kk < C::BQ / 16; ++kk)
+            mma_ss(tmem + C::T_DK, sdesc_add(dA, (kk >> 2) * C::DS_CHUNK + (kk & 3) * 32),
+                   sdesc_add(dY, kk * 2048), idKV, (j > 0 || kk > 0) ? 1u : 0u);
+          // dQ(j) and dK(j) have read the staging tile
+          mma_commit(bar(C::B_DSMFREE));
+        } else {
+          issue_acc(tmem + C::T_DP, sdesc_add(dQmn, (j % C::NQS) * C::Q_TILE), tmem + C::T_DK,
+                    j == 0);
+        }
         mma_commit(bar(C::B_QFREE + j % C::NQS));
         return true;
       };
       auto issue_dQ = [&](int j) -> bool {
+        // D = 128: dQ(j) is the first product after dS(j)
+        if (C::kDqInDp && !mbar_wait(bar(C::B_DSREADY), j & 1, ab)) return false;
         // D = 64: dQ has columns of its own; wait until dQ(j-1) has been read out
         if (!C::kDqInDp && j > 0 && !mbar_wait(bar(C::B_DQEMPTY), (j - 1) & 1, ab)) return false;
         tc_fence_after();
@@ -382,7 +402,7 @@ __global__ void __launch_bounds__(512, 1)
           }
         }
         mma_commit(bar(C::B_DQFULL));
-        mma_commit(bar(C::B_DSMFREE));
+        if (!C::kDqInDp) mma_commit(bar(C::B_DSMFREE));  // D = 128: after dK(j)
         return true;
       };
       if (ok && n > 0) {
@@ -390,18 +410,25 @@ __global__ void __launch_bounds__(512, 1)
         if (ok && n > 1) ok = issue_S(1);
       }
       for (int i = 0; ok && i < n; ++i) {
-        if (!(ok = issue_dK(i))) break;
-        // D = 64: dQ has columns of its own, so dP(i+1) follows dK(i) (the last reader
-        // of dS^T(i) in dP^T's columns) at once and the softmax warps find it done
-        // when they reach dS(i+1). D = 128: dQ(i) is accumulated over dP^T's columns,
-        // so dP(i+1) waits until the dQ warps have read dQ(i) out.
-        if (!C::kDqInDp && i + 1 < n && !(ok = issue_dP(i + 1))) break;
-        if (!(ok = issue_dQ(i))) break;
-        if (i + 1 < n) {
-          if (C::kDqInDp) {
+        if constexpr (C::kDqInDp) {
+          // D = 128: dQ(i) into dP^T's columns as soon as dS(i) is staged, dK(i) (from
+          // the staging tile) while the dQ warps read dQ(i) out, then dP(i+1) into
+          // the freed columns
+          if (!(ok = issue_dQ(i))) break;
+          if (!(ok = issue_dK(i))) break;
+          if (i + 1 < n) {
             if (!(ok = mbar_wait(bar(C::B_DQEMPTY), i & 1, ab))) break;
             if (!(ok = issue_dP(i + 1))) break;
           }
+        } else {
+          // D = 64: dQ has columns of its own, so dP(i+1) follows dK(i) (the last
+          // reader of dS^T(i) in dP^T's columns) at once and the softmax warps find it
+          // done when they reach dS(i+1)
+          if (!(ok = issue_dK(i))) break;
+          if (i + 1 < n && !(ok = issue_dP(i + 1))) break;
+          if (!(ok = issue_dQ(i))) break;
+        }
+        if (i + 1 < n) {
           if (!(ok = issue_dV(i + 1))) break;
           if (i + 2 < n && !(ok = issue_S(i + 2))) break;
         }
@@ -569,7 +596,8 @@ __global__ void __launch_bounds__(512, 1)
       if (lane == 0) mbar_arrive(bar(C::B_PREADY));
 
       if (!(ok = mbar_wait_warp(bar(C::B_DPFULL), j & 1, ab))) break;
-      // the dS^T staging tile is free once dQ(j - 1) has completed
+      // the dS^T staging tile is free once its readers of block j - 1 have completed
+      // (dQ(j - 1), and at D = 128 dK(j - 1))
       if (j > 0 && !(ok = mbar_wait_warp(bar(C::B_DSMFREE), (j - 1) & 1, ab))) break;
       tc_fence_after();
 #pragma unroll
@@ -595,7 +623,8 @@ __global__ void __launch_bounds__(512, 1)
           pk[e] = pack16<F16>(a01.x, a01.y);
           pk[e + 1] = pack16<F16>(a23.x, a23.y);
         }
-        tmem_st16(tDP + 16 * c, pk);
+        // D = 64: dK reads dS^T from dP^T's columns; D = 128: from the staging tile only
+        if constexpr (!C::kDqInDp) tmem_st16(tDP + 16 * c, pk);
         // dS^T row kr, queries ql .. ql+31 into the swizzled smem tile
         const int ql = g * C::QPW + 32 * c;
         const uint32_t chunk = sDS + (ql >> 6) * C::DS_CHUNK + kr * 128;
