@@ -41,6 +41,7 @@
 // tensor map whose row and column strides are doubled). Partial sums are added
 // into dW (zeroed first) with TMA f32 add-reductions.
 #include <stdint.h>
+#include <stdlib.h>
 
 #include <algorithm>
 
@@ -55,23 +56,26 @@ using namespace mg_tc;
 template <int BN>
 struct ConvCfg {
   static constexpr int BM = 128;                  // accumulator rows (MMA M)
-  static constexpr int NST = BN == 128 ? 4 : 6;   // ring stages, continuous across work items
   static constexpr int A_BYTES = BM * 128;        // 128 rows x 64 elements
   static constexpr int B_BYTES = BN * 128;        // BN/64 boxes of 64 rows x 128 bytes
   static constexpr int STAGE = A_BYTES + B_BYTES;
-  // accumulator staging for the TMA stores: BN/32 chunks of 128 rows x 32 f32
-  // (128-byte rows, 128-byte swizzle)
+  // ring stages, continuous across work items: as many as fit beside the staging
+  // ring (24, 32 or 48 KB a stage)
+  static constexpr int NST = BN == 256 ? 4 : (BN == 128 ? 6 : 8);
+  // accumulator read-back staging: a ring of two 16 KB buffers, each one 32-column
+  // chunk (dX: 128 pixel rows x 32 f32; dW: four warps' 32 rows x 32 f32, 4 KB a
+  // warp), 128-byte rows with 128-byte swizzle
   static constexpr int OFF_STG = NST * STAGE;
   static constexpr int STG_CHUNK = BM * 128;
-  static constexpr int OFF_BAR = OFF_STG + (BN / 32) * STG_CHUNK;
+  static constexpr int OFF_BAR = OFF_STG + 2 * STG_CHUNK;
   static constexpr int B_FULL = 0;                // NST: stage loaded
   static constexpr int B_EMPTY = NST;             // NST: stage consumed by its MMAs
   static constexpr int B_AFULL = 2 * NST;         // 2: accumulator buffer complete
   static constexpr int B_AEMPTY = 2 * NST + 2;    // 2: accumulator buffer read out (4 warps)
   static constexpr int B_DRAIN = 2 * NST + 4;
-  static constexpr int B_SFULL = 2 * NST + 5;     // staging written (4 warps)
-  static constexpr int B_SFREE = 2 * NST + 6;     // staging read by the TMA stores
-  static constexpr int NBAR = 2 * NST + 7;
+  static constexpr int B_SFULL = 2 * NST + 5;     // 2: staging buffer written (4 warps, dX)
+  static constexpr int B_SFREE = 2 * NST + 7;     // 2: staging buffer read by its TMA store
+  static constexpr int NBAR = 2 * NST + 9;
   static constexpr int OFF_MISC = OFF_BAR + NBAR * 8;
   static constexpr int SMEM_BYTES = OFF_MISC + 16 + 1024;
   static constexpr int NTHREADS = 192;            // warps 0-3 read-back, 4 TMA, 5 MMA
@@ -123,7 +127,10 @@ __device__ __forceinline__ uint32_t conv_setup(uint8_t *smem, uint32_t sbase, in
   if (threadIdx.x == 128) {
     for (int i = 0; i < C::NBAR; ++i)
       mbar_init(sbase + C::OFF_BAR + 8u * i,
-                (i == C::B_AEMPTY || i == C::B_AEMPTY + 1 || i == C::B_SFULL) ? 4u : 1u);
+                (i == C::B_AEMPTY || i == C::B_AEMPTY + 1 || i == C::B_SFULL ||
+                 i == C::B_SFULL + 1)
+                    ? 4u
+                    : 1u);
     *reinterpret_cast<volatile int *>(smem + C::OFF_MISC + 4) = 0;
     fence_barrier_init();
   }
@@ -313,63 +320,68 @@ __global__ void __launch_bounds__(192, 1)
     __syncwarp();
   } else {
     // ------------------------------------------------------------ read-back (warps 0-3)
-    // Accumulator rows are the tile's pixels in box order: each thread stages its
-    // row in shared memory, then one thread stores the whole pixel box per 32
-    // channels with TMA (a phase view of dX: elements past the image are not
-    // written), or adds it into the zeroed dX when the steps are split.
+    // Accumulator rows are the tile's pixels in box order. Per 32-channel chunk,
+    // each thread stages its row in one of two shared-memory buffers and one
+    // thread stores the pixel box with TMA (a phase view of dX: elements past the
+    // image are not written), or adds it into the zeroed dX when the steps are
+    // split. A buffer is refilled once the store two chunks back has read it; gc
+    // counts the chunks staged so far (the same sequence in every thread).
     const int m = 32 * warp + lane;
     const uint32_t lane_off = static_cast<uint32_t>(32 * warp) << 16;
-    const uint32_t stg = sbase + C::OFF_STG;
-    int it = 0;
-    for (int item = blockIdx.x; item < a.items; item += gridDim.x, ++it) {
+    int it = 0, gc = 0;
+    bool ok = true;
+    for (int item = blockIdx.x; ok && item < a.items; item += gridDim.x, ++it) {
       const DgradItem d = dgrad_item(a, item, BN);
       bool any = false;
       for (DgradSteps x(d); x.s < d.se && !any; x.next(d)) any = x.live(a, d);
       const bool store = any || a.G == 1;  // no live step: zeros, or nothing to add
       const int buf = it & 1;
-      if (!mbar_wait_warp(bar(C::B_AFULL + buf), (it >> 1) & 1, ab)) break;
+      if (!(ok = mbar_wait_warp(bar(C::B_AFULL + buf), (it >> 1) & 1, ab))) break;
       tc_fence_after();
-      if (it > 0 && !mbar_wait_warp(bar(C::B_SFREE), (it - 1) & 1, ab)) break;
-      if (store) {
+      const int ph = d.ph * a.st + d.pw;
+      const CUtensorMap *mo = ph == 0 ? &tmO0 : (ph == 1 ? &tmO1 : (ph == 2 ? &tmO2 : &tmO3));
+      const int nch = store ? min(BN / 32, (a.C - d.c0 + 31) / 32) : 0;
+      for (int cc = 0; cc < nch; ++cc, ++gc) {
+        uint32_t r[32];
+        if (any) {
+          tmem_ld32(tmem + lane_off + buf * BN + 32 * cc, r);
+          tmem_wait_ld();
+        } else {
 #pragma unroll
-        for (int cc = 0; cc < BN / 32; ++cc) {
-          uint32_t r[32];
-          if (any) {
-            tmem_ld32(tmem + lane_off + buf * BN + 32 * cc, r);
-            tmem_wait_ld();
-          } else {
-#pragma unroll
-            for (int e = 0; e < 32; ++e) r[e] = 0u;  // no tap reaches these pixels
-          }
-          stage_row(stg + cc * C::STG_CHUNK + m * 128, m, r);
+          for (int e = 0; e < 32; ++e) r[e] = 0u;  // no tap reaches these pixels
         }
-      }
-      tc_fence_before();
-      fence_proxy_async_smem();
-      __syncwarp();
-      if (lane == 0) {
-        mbar_arrive(bar(C::B_AEMPTY + buf));
-        mbar_arrive(bar(C::B_SFULL));
-      }
-      if (warp == 0) {
-        if (!mbar_wait_warp(bar(C::B_SFULL), it & 1, ab)) break;
-        if (lane == 0) {
-          if (store) {
-            const int ph = d.ph * a.st + d.pw;
-            const CUtensorMap *mo =
-                ph == 0 ? &tmO0 : (ph == 1 ? &tmO1 : (ph == 2 ? &tmO2 : &tmO3));
-            for (int cc = 0; cc < BN / 32 && d.c0 + 32 * cc < a.C; ++cc) {
-              if (a.G == 1)
-                tma_store_4d(mo, stg + cc * C::STG_CHUNK, d.c0 + 32 * cc, d.j0, d.i0, d.n0);
-              else
-                tma_reduce_add_4d(mo, stg + cc * C::STG_CHUNK, d.c0 + 32 * cc, d.j0, d.i0, d.n0);
-            }
-            bulk_commit_group();
-            bulk_wait_group_read0();
-          }
-          mbar_arrive(bar(C::B_SFREE));
+        if (cc == nch - 1) {  // the accumulator buffer is read out
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(bar(C::B_AEMPTY + buf));
         }
+        const int sb = gc & 1;
+        const uint32_t sa = sbase + C::OFF_STG + sb * C::STG_CHUNK;
+        if (gc >= 2 && !(ok = mbar_wait_warp(bar(C::B_SFREE + sb), ((gc >> 1) - 1) & 1, ab)))
+          break;
+        stage_row(sa + m * 128, m, r);
+        fence_proxy_async_smem();
         __syncwarp();
+        if (lane == 0) mbar_arrive(bar(C::B_SFULL + sb));
+        if (warp == 0) {
+          if (!(ok = mbar_wait_warp(bar(C::B_SFULL + sb), (gc >> 1) & 1, ab))) break;
+          if (lane == 0) {
+            if (a.G == 1)
+              tma_store_4d(mo, sa, d.c0 + 32 * cc, d.j0, d.i0, d.n0);
+            else
+              tma_reduce_add_4d(mo, sa, d.c0 + 32 * cc, d.j0, d.i0, d.n0);
+            bulk_commit_group();
+            // the previous chunk's store has read the other buffer
+            bulk_wait_group_read1();
+            if (gc >= 1) mbar_arrive(bar(C::B_SFREE + (sb ^ 1)));
+          }
+          __syncwarp();
+        }
+      }
+      if (ok && nch == 0) {  // nothing to store: the accumulator is free at once
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(bar(C::B_AEMPTY + buf));
       }
     }
     if (threadIdx.x == 0) bulk_wait_group0();
@@ -531,12 +543,14 @@ __global__ void __launch_bounds__(192, 1)
     __syncwarp();
   } else {
     // ------------------------------------------------------------ read-back: add into dW
-    // Warp w owns accumulator rows k0 + 32w .. k0 + 32w + 31: it stages them in
-    // its own part of shared memory and adds them into dW with TMA reductions
-    // (a [K][R*S][C] view: rows past K and channels past C are not written).
+    // Warp w owns accumulator rows k0 + 32w .. k0 + 32w + 31: per 32-channel chunk
+    // it stages them in one of its two 4 KB buffers and adds them into dW with a
+    // TMA reduction (a [K][R*S][C] view: rows past K and channels past C are not
+    // written); a buffer is refilled once the reduction two chunks back has read
+    // it (the warp's own bulk groups).
     const uint32_t lane_off = static_cast<uint32_t>(32 * warp) << 16;
-    const uint32_t stg = sbase + C::OFF_STG + warp * 32 * 128;
-    int it = 0;
+    const uint32_t stg = sbase + C::OFF_STG + warp * 2 * 32 * 128;
+    int it = 0, gc = 0;
     for (int item = blockIdx.x; item < a.items; item += gridDim.x, ++it) {
       const WgradItem w = wgrad_item(a, item, BN);
       bool any = false;
@@ -544,30 +558,26 @@ __global__ void __launch_bounds__(192, 1)
       const int buf = it & 1;
       if (!mbar_wait_warp(bar(C::B_AFULL + buf), (it >> 1) & 1, ab)) break;
       tc_fence_after();
-      if (any) {
-        // this warp's previous reductions have finished reading its staging rows
-        if (lane == 0) bulk_wait_group_read0();
+      const int nch =
+          any && w.k0 + 32 * warp < a.K ? min(BN / 32, (a.C - w.c0 + 31) / 32) : 0;
+      for (int cc = 0; cc < nch; ++cc, ++gc) {
+        uint32_t v[32];
+        tmem_ld32(tmem + lane_off + buf * BN + 32 * cc, v);
+        tmem_wait_ld();
+        const uint32_t sa = stg + (gc & 1) * 32 * 128;
+        if (lane == 0) bulk_wait_group_read1();
         __syncwarp();
-#pragma unroll
-        for (int cc = 0; cc < BN / 32; ++cc) {
-          uint32_t v[32];
-          tmem_ld32(tmem + lane_off + buf * BN + 32 * cc, v);
-          tmem_wait_ld();
-          stage_row(stg + cc * C::STG_CHUNK + lane * 128, lane, v);
-        }
-      }
-      tc_fence_before();
-      fence_proxy_async_smem();
-      __syncwarp();
-      if (lane == 0) {
-        mbar_arrive(bar(C::B_AEMPTY + buf));
-        if (any && w.k0 + 32 * warp < a.K) {
-          for (int cc = 0; cc < BN / 32 && w.c0 + 32 * cc < a.C; ++cc)
-            tma_reduce_add_3d(&tmdW, stg + cc * C::STG_CHUNK, w.c0 + 32 * cc, w.r * a.S + w.sx,
-                              w.k0 + 32 * warp);
+        stage_row(sa + lane * 128, lane, v);
+        fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0) {
+          tma_reduce_add_3d(&tmdW, sa, w.c0 + 32 * cc, w.r * a.S + w.sx, w.k0 + 32 * warp);
           bulk_commit_group();
         }
       }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(bar(C::B_AEMPTY + buf));
     }
     if (lane == 0) bulk_wait_group0();
   }
@@ -595,6 +605,45 @@ void pixel_box(int N, int Hg, int Wg, int rows, bool exact, int &BW, int &BH, in
   }
 }
 
+// Input-gradient tiling: the pixel box, the prefix sums of the tiles of each
+// stride phase, their total, and the fewest reduction steps of a phase with pixels.
+struct DgradGeom {
+  int BW, BH, BNi;
+  int tile_end[4];
+  long long tiles;
+  int tmin;
+};
+
+DgradGeom dgrad_geom(const MgConvProblem &p) {
+  DgradGeom g{};
+  const int st = p.stride;
+  pixel_box(p.N, (p.H + st - 1) / st, (p.W + st - 1) / st, 128, false, g.BW, g.BH, g.BNi);
+  g.tmin = 1 << 30;
+  for (int ph = 0; ph < st * st; ++ph) {
+    const int hp = (p.H - ph / st + st - 1) / st, wp = (p.W - ph % st + st - 1) / st;
+    const long long n = hp > 0 && wp > 0
+                            ? static_cast<long long>((hp + g.BH - 1) / g.BH) *
+                                  ((wp + g.BW - 1) / g.BW) * ((p.N + g.BNi - 1) / g.BNi)
+                            : 0;
+    if (n > 0) {
+      const int r0 = (ph / st + p.pad) % st, s0 = (ph % st + p.pad) % st;
+      const int nr = r0 < p.R ? (p.R - r0 + st - 1) / st : 0;
+      const int ns = s0 < p.S ? (p.S - s0 + st - 1) / st : 0;
+      g.tmin = std::min(g.tmin, nr * ns * ((p.K + 63) / 64));
+    }
+    g.tiles += n;
+    g.tile_end[ph] = static_cast<int>(std::min<long long>(g.tiles, 0x7fffffffLL));
+  }
+  return g;
+}
+
+// The reduction steps of each tile are split into groups (partial sums added into
+// a zeroed dX) when there are at most half as many work items as SMs and at least
+// 8 steps a tile.
+bool dgrad_split(const DgradGeom &g, int C, int BN, int sms) {
+  return 2 * g.tiles * ((C + BN - 1) / BN) <= sms && g.tmin >= 8;
+}
+
 template <int BN, bool F16>
 cudaError_t launch_dgrad(const void *dY, const void *Wt, float *dX, const MgConvProblem &p,
                          unsigned int *err, cudaStream_t s) {
@@ -605,7 +654,10 @@ cudaError_t launch_dgrad(const void *dY, const void *Wt, float *dX, const MgConv
   DgradArgs a{};
   a.N = p.N; a.H = p.H; a.W = p.W; a.C = p.C; a.K = p.K; a.R = p.R; a.S = p.S;
   a.st = st; a.pad = p.pad; a.P = p.P; a.Q = p.Q;
-  pixel_box(p.N, (p.H + st - 1) / st, (p.W + st - 1) / st, 128, false, a.BW, a.BH, a.BNi);
+  const DgradGeom geo = dgrad_geom(p);
+  a.BW = geo.BW;
+  a.BH = geo.BH;
+  a.BNi = geo.BNi;
   {
     const long long dims[4] = {K, p.Q, p.P, p.N};
     const long long str[3] = {K * 2, static_cast<long long>(p.Q) * K * 2,
@@ -623,32 +675,15 @@ cudaError_t launch_dgrad(const void *dY, const void *Wt, float *dX, const MgConv
     if (e != cudaSuccess) return e;
   }
   a.nphase = st * st;
-  long long tiles = 0;
-  int tmin = 1 << 30;  // fewest reduction steps of a phase that has pixels
-  for (int ph = 0; ph < a.nphase; ++ph) {
-    const int hp = (p.H - ph / st + st - 1) / st, wp = (p.W - ph % st + st - 1) / st;
-    const long long n = hp > 0 && wp > 0
-                            ? static_cast<long long>((hp + a.BH - 1) / a.BH) *
-                                  ((wp + a.BW - 1) / a.BW) * ((p.N + a.BNi - 1) / a.BNi)
-                            : 0;
-    if (n > 0) {
-      const int r0 = (ph / st + p.pad) % st, s0 = (ph % st + p.pad) % st;
-      const int nr = r0 < p.R ? (p.R - r0 + st - 1) / st : 0;
-      const int ns = s0 < p.S ? (p.S - s0 + st - 1) / st : 0;
-      tmin = std::min(tmin, nr * ns * ((p.K + 63) / 64));
-    }
-    tiles += n;
-    a.tile_end[ph] = static_cast<int>(tiles);
-  }
+  for (int ph = 0; ph < 4; ++ph) a.tile_end[ph] = geo.tile_end[ph];
   a.CB = (p.C + BN - 1) / BN;
-  // At most half as many work items as SMs: split each tile's reduction steps
-  // into G groups (at least 4 steps each; G * work <= SMs, one wave) whose
-  // partial sums are added into a zeroed dX.
-  const long long work = tiles * a.CB;
+  // Split each tile's reduction steps into G groups (at least 4 steps each;
+  // G * work <= SMs, one wave) whose partial sums are added into a zeroed dX.
+  const long long work = geo.tiles * a.CB;
   const int sms = mg_sm_count();
   a.G = 1;
-  if (2 * work <= sms && tmin >= 8)
-    a.G = static_cast<int>(std::min<long long>({sms / work, tmin / 4, 8}));
+  if (dgrad_split(geo, p.C, BN, sms))
+    a.G = static_cast<int>(std::min<long long>({sms / work, geo.tmin / 4, 8}));
   if (work * a.G > 0x7fffffffLL || work < 1) return cudaErrorInvalidValue;
   a.items = static_cast<int>(work * a.G);
   a.dX = dX;
@@ -673,7 +708,7 @@ cudaError_t launch_dgrad(const void *dY, const void *Wt, float *dX, const MgConv
   }
   auto kern = conv_dgrad_kernel<BN, F16>;
   cudaError_t e = mg_set_smem_attr(reinterpret_cast<const void *>(kern), C::SMEM_BYTES,
-                                   32 + (BN == 128 ? 1 : 0) + (F16 ? 2 : 0));
+                                   32 + 2 * (BN / 128) + (F16 ? 1 : 0));
   if (e != cudaSuccess) return e;
   const int grid = std::min(a.items, sms);
   kern<<<grid, C::NTHREADS, C::SMEM_BYTES, s>>>(tdy, tw, to[0], to[1], to[2], to[3], a);
@@ -738,7 +773,7 @@ cudaError_t launch_wgrad(const void *X, const void *dY, float *dW, const MgConvP
   }
   auto kern = conv_wgrad_kernel<BN, F16>;
   cudaError_t e = mg_set_smem_attr(reinterpret_cast<const void *>(kern), C::SMEM_BYTES,
-                                   36 + (BN == 128 ? 1 : 0) + (F16 ? 2 : 0));
+                                   40 + 2 * (BN / 128) + (F16 ? 1 : 0));
   if (e != cudaSuccess) return e;
   const int grid = std::min(a.items, sms);
   kern<<<grid, C::NTHREADS, C::SMEM_BYTES, s>>>(tdy, tx[0], tx[1], tx[2], tx[3], tdw, a);
@@ -747,20 +782,48 @@ cudaError_t launch_wgrad(const void *X, const void *dY, float *dW, const MgConvP
 
 }  // namespace
 
+// Accumulator width N (columns of C per work item): 64 for C <= 64, 256 for
+// C >= 256 (half the operand bytes per FLOP of N = 128 through shared memory,
+// which an M = 128 product with both operands in shared memory saturates), else
+// 128. MG_CONV_MAX_N=128 or 64 caps it.
+int conv_bn(int C) {
+  static const int cap = [] {
+    const char *v = getenv("MG_CONV_MAX_N");
+    const int c = v ? atoi(v) : 256;
+    return c >= 256 ? 256 : (c >= 128 ? 128 : 64);
+  }();
+  const int bn = C >= 256 ? 256 : (C > 64 ? 128 : 64);
+  return std::min(bn, cap);
+}
+
 cudaError_t mg_launch_conv_dgrad(const void *dY, const void *Wt, float *dX,
                                  const MgConvProblem &p, unsigned int *err, cudaStream_t s) {
-  const bool wide = p.C > 64;
-  if (p.f16) return wide ? launch_dgrad<128, true>(dY, Wt, dX, p, err, s)
-                         : launch_dgrad<64, true>(dY, Wt, dX, p, err, s);
-  return wide ? launch_dgrad<128, false>(dY, Wt, dX, p, err, s)
-              : launch_dgrad<64, false>(dY, Wt, dX, p, err, s);
+  int bn = conv_bn(p.C);
+  if (bn == 256) {
+    // 128-wide tiles where 256-wide ones would need the split reduction (a zeroed
+    // dX and added partial sums) that 128-wide ones do without
+    const DgradGeom g = dgrad_geom(p);
+    const int sms = mg_sm_count();
+    if (dgrad_split(g, p.C, 256, sms) && !dgrad_split(g, p.C, 128, sms)) bn = 128;
+  }
+  switch (bn * 2 + (p.f16 ? 1 : 0)) {
+    case 513: return launch_dgrad<256, true>(dY, Wt, dX, p, err, s);
+    case 512: return launch_dgrad<256, false>(dY, Wt, dX, p, err, s);
+    case 257: return launch_dgrad<128, true>(dY, Wt, dX, p, err, s);
+    case 256: return launch_dgrad<128, false>(dY, Wt, dX, p, err, s);
+    case 129: return launch_dgrad<64, true>(dY, Wt, dX, p, err, s);
+    default: return launch_dgrad<64, false>(dY, Wt, dX, p, err, s);
+  }
 }
 
 cudaError_t mg_launch_conv_wgrad(const void *X, const void *dY, float *dW,
                                  const MgConvProblem &p, unsigned int *err, cudaStream_t s) {
-  const bool wide = p.C > 64;
-  if (p.f16) return wide ? launch_wgrad<128, true>(X, dY, dW, p, err, s)
-                         : launch_wgrad<64, true>(X, dY, dW, p, err, s);
-  return wide ? launch_wgrad<128, false>(X, dY, dW, p, err, s)
-              : launch_wgrad<64, false>(X, dY, dW, p, err, s);
+  switch (conv_bn(p.C) * 2 + (p.f16 ? 1 : 0)) {
+    case 513: return launch_wgrad<256, true>(X, dY, dW, p, err, s);
+    case 512: return launch_wgrad<256, false>(X, dY, dW, p, err, s);
+    case 257: return launch_wgrad<128, true>(X, dY, dW, p, err, s);
+    case 256: return launch_wgrad<128, false>(X, dY, dW, p, err, s);
+    case 129: return launch_wgrad<64, true>(X, dY, dW, p, err, s);
+    default: return launch_wgrad<64, false>(X, dY, dW, p, err, s);
+  }
 }

@@ -96,6 +96,9 @@ EDGE = [
     (1, 2, 2, 8, 8, 2, 2, 2, 0),        # one output pixel
     (4, 3, 3, 64, 64, 3, 3, 2, 0),      # stride 2 without padding
     (5, 11, 13, 128, 256, 3, 3, 2, 1),  # several images per box at both strides
+    (2, 9, 7, 320, 72, 3, 3, 1, 1),     # 256-wide tiles of C, the second one ragged
+    (1, 5, 6, 264, 136, 3, 3, 2, 1),    # 256-wide tiles, 8 channels in the last chunk, stride 2
+    (3, 7, 7, 512, 40, 1, 1, 1, 0),     # 256-wide tiles, one reduction step of K
 ]
 
 
