@@ -783,9 +783,9 @@ cudaError_t launch_wgrad(const void *X, const void *dY, float *dW, const MgConvP
 }  // namespace
 
 // Accumulator width N (columns of C per work item): 64 for C <= 64, 256 for
-// C >= 256 (half the operand bytes per FLOP of N = 128 through shared memory,
-// which an M = 128 product with both operands in shared memory saturates), else
-// 128. MG_CONV_MAX_N=128 or 64 caps it.
+// C >= 256 (a quarter fewer operand bytes per FLOP through shared memory than
+// N = 128, which an M = 128 product with both operands there would saturate at
+// the full tensor rate), else 128. MG_CONV_MAX_N=128 or 64 caps it.
 int conv_bn(int C) {
   static const int cap = [] {
     const char *v = getenv("MG_CONV_MAX_N");

@@ -310,15 +310,21 @@ int mg_attn_fwd_decode(const void *Q, const void *K, const void *V, void *O, flo
  * tcgen05 tensor cores with f32 accumulation; dX and dW are f32 and are
  * overwritten. Only the order of the f32 additions differs from exact
  * arithmetic on the 16-bit inputs; dW adds per-CTA partial sums with f32
- * atomics, so it is not bitwise reproducible across runs.
+ * atomics, so it is not bitwise reproducible across runs (nor is dX when there
+ * are too few output tiles to fill the GPU and each tile's reduction is split).
  * Preconditions checked: pointers non-NULL, 16-byte aligned, outputs not
  * overlapping inputs; N, H, W, C, K, R, S >= 1; H, W <= 65535; R, S, pad in
  * [0, 64] with H + 2 pad >= R and W + 2 pad >= S; every tensor below 2^31
  * elements (else MG_ERR_INVALID_ARG); stride 1 or 2, C and K multiples of 8,
  * ceil(K/128) * ceil(C/64) <= 65535, contract ACCEL_BF16 or ACCEL_F16 without
  * flags (else MG_ERR_UNSUPPORTED: STRICT_F32 has no convolution derivatives).
- * Asynchronous on `stream`; no allocation. Kernel names in the profile:
- * "conv_dgrad", "conv_wgrad".
+ * Asynchronous on `stream`; no allocation and no synchronising call, so a
+ * sequence of these calls can be captured in a CUDA graph (the host cost of one
+ * call, argument checks, tensor-map encoding and the launch, is comparable to the
+ * kernel time of small layers). The environment variable MG_CONV_MAX_N=128 or 64
+ * (read once per process) caps the accumulator width, which is otherwise 256
+ * channels of C for C >= 256. Kernel names in the profile: "conv_dgrad",
+ * "conv_wgrad".
  */
 int mg_conv2d_grad_input(const void *dY, const void *Wt, float *dX, int N, int H, int W, int C,
                          int K, int R, int S, int stride, int pad, int contract, void *stream);
