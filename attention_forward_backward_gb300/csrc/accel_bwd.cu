@@ -153,6 +153,18 @@ __device__ __forceinline__ uint32_t dq_stage_off(int row, int col, int box_bytes
                                ((col & 3) << 2));
 }
 
+// The kernel's bounded waits: at D = 128 the variant that polls the abort flag and
+// the clock less often (measured 1.3% faster there, slower at D = 64).
+template <int DP>
+__device__ __forceinline__ bool bwait(uint32_t bar, uint32_t parity, const Abort &ab) {
+  if constexpr (DP == 128) return mbar_wait_poll(bar, parity, ab);
+  else return mbar_wait(bar, parity, ab);
+}
+template <int DP>
+__device__ __forceinline__ bool bwait_warp(uint32_t bar, uint32_t parity, const Abort &ab) {
+  return __all_sync(0xffffffffu, bwait<DP>(bar, parity, ab));
+}
+
 template <int DP, bool F16>
 __global__ void __launch_bounds__(512, 1)
     accel_dkdv_kernel(const __grid_constant__ CUtensorMap tmQ,
@@ -252,7 +264,7 @@ __global__ void __launch_bounds__(512, 1)
         lse_r[u] = v ? LSE[static_cast<size_t>(bh) * L + qg] : -INFINITY;
         dv_r[u] = v ? Dvec[static_cast<size_t>(bh) * L + qg] : 0.f;
       }
-      if (j >= C::NQS && !mbar_wait_warp(bar(C::B_QFREE + st), ((j / C::NQS) - 1) & 1, ab))
+      if (j >= C::NQS && !bwait_warp<DP>(bar(C::B_QFREE + st), ((j / C::NQS) - 1) & 1, ab))
         break;
 #pragma unroll
       for (int u = 0; u < C::BQ / 32; ++u) {
@@ -281,7 +293,7 @@ __global__ void __launch_bounds__(512, 1)
       int issued = 0;
       for (int j = 0; j < n; ++j) {
         const int st = j % C::NQS;
-        if (j >= C::NQS && !mbar_wait(bar(C::B_DOFREE + st), ((j / C::NQS) - 1) & 1, ab)) break;
+        if (j >= C::NQS && !bwait<DP>(bar(C::B_DOFREE + st), ((j / C::NQS) - 1) & 1, ab)) break;
         const int q0 = (qb0 + j) * C::BQ;
         mbar_arrive_expect_tx(bar(C::B_DOFULL + st), C::Q_TILE);
         for (int c = 0; c < C::NCHUNK; ++c)
@@ -299,7 +311,7 @@ __global__ void __launch_bounds__(512, 1)
       constexpr uint32_t idKV = idesc_16_f32(128, DP, false, true, F16);
       constexpr uint32_t idDQ =
           C::kDqInDp ? idesc_16_f32(128, C::BQ, true, true, F16) : idesc_16_f32(128, DP, true, true, F16);
-      bool ok = mbar_wait(bar(C::B_KVFULL), 0, ab);
+      bool ok = bwait<DP>(bar(C::B_KVFULL), 0, ab);
       // base descriptors; each MMA adds a compile-time byte offset
       const uint32_t sb = opaque_u32(sbase);
       const uint64_t dK0 = sdesc_sw128(sb + C::OFF_K, 0, 1024);
@@ -333,23 +345,23 @@ __global__ void __launch_bounds__(512, 1)
         }
       };
       auto issue_S = [&](int j) -> bool {
-        if (!mbar_wait(bar(C::B_QFULL + j % C::NQS), (j / C::NQS) & 1, ab)) return false;
+        if (!bwait<DP>(bar(C::B_QFULL + j % C::NQS), (j / C::NQS) & 1, ab)) return false;
         tc_fence_after();
         issue_T(dK0, sdesc_add(dQ0, (j % C::NQS) * C::Q_TILE), tmem + C::T_S);
         mma_commit(bar(C::B_SFULL));
         return true;
       };
       auto issue_dP = [&](int j) -> bool {
-        if (!mbar_wait(bar(C::B_DOFULL + j % C::NQS), (j / C::NQS) & 1, ab)) return false;
+        if (!bwait<DP>(bar(C::B_DOFULL + j % C::NQS), (j / C::NQS) & 1, ab)) return false;
         tc_fence_after();
         issue_T(dV0, sdesc_add(dO0, (j % C::NQS) * C::Q_TILE), tmem + C::T_DP);
         mma_commit(bar(C::B_DPFULL));
         return true;
       };
       auto issue_dV = [&](int j) -> bool {
-        if (!mbar_wait(bar(C::B_PREADY), j & 1, ab)) return false;
+        if (!bwait<DP>(bar(C::B_PREADY), j & 1, ab)) return false;
         // dO_j has landed (dP(j) waited for it; the wait is kept for clarity)
-        if (!mbar_wait(bar(C::B_DOFULL + j % C::NQS), (j / C::NQS) & 1, ab)) return false;
+        if (!bwait<DP>(bar(C::B_DOFULL + j % C::NQS), (j / C::NQS) & 1, ab)) return false;
         tc_fence_after();
         issue_acc(tmem + C::T_S, sdesc_add(dOmn, (j % C::NQS) * C::Q_TILE), tmem + C::T_DV,
                   j == 0);
@@ -363,7 +375,7 @@ __global__ void __launch_bounds__(512, 1)
       // chunks), so that dQ(j) may go first and overwrite dP^T's columns at once.
       const uint64_t dDSk = sdesc_sw128(sb + C::OFF_DS, 0, 1024);
       auto issue_dK = [&](int j) -> bool {
-        if (!C::kDqInDp && !mbar_wait(bar(C::B_DSREADY), j & 1, ab)) return false;
+        if (!C::kDqInDp && !bwait<DP>(bar(C::B_DSREADY), j & 1, ab)) return false;
         tc_fence_after();
         if constexpr (C::kDqInDp) {
           const uint64_t dA = opaque_u64(dDSk);
@@ -383,9 +395,9 @@ __global__ void __launch_bounds__(512, 1)
       };
       auto issue_dQ = [&](int j) -> bool {
         // D = 128: dQ(j) is the first product after dS(j)
-        if (C::kDqInDp && !mbar_wait(bar(C::B_DSREADY), j & 1, ab)) return false;
+        if (C::kDqInDp && !bwait<DP>(bar(C::B_DSREADY), j & 1, ab)) return false;
         // D = 64: dQ has columns of its own; wait until dQ(j-1) has been read out
-        if (!C::kDqInDp && j > 0 && !mbar_wait(bar(C::B_DQEMPTY), (j - 1) & 1, ab)) return false;
+        if (!C::kDqInDp && j > 0 && !bwait<DP>(bar(C::B_DQEMPTY), (j - 1) & 1, ab)) return false;
         tc_fence_after();
         const uint64_t dDS = opaque_u64(dDSmn);
         const uint64_t dKq = opaque_u64(dKmn);
@@ -417,7 +429,7 @@ __global__ void __launch_bounds__(512, 1)
           if (!(ok = issue_dQ(i))) break;
           if (!(ok = issue_dK(i))) break;
           if (i + 1 < n) {
-            if (!(ok = mbar_wait(bar(C::B_DQEMPTY), i & 1, ab))) break;
+            if (!(ok = bwait<DP>(bar(C::B_DQEMPTY), i & 1, ab))) break;
             if (!(ok = issue_dP(i + 1))) break;
           }
         } else {
@@ -445,7 +457,7 @@ __global__ void __launch_bounds__(512, 1)
       // thread t = d: dQ^T[d][q] for the block's 128 query rows, in two halves
       // of 64 rows; warp w stages and reduces box w (d = 32w .. 32w+31)
       for (int j = 0; j < n; ++j) {
-        if (!mbar_wait_warp(bar(C::B_DQFULL), j & 1, ab)) break;
+        if (!bwait_warp<DP>(bar(C::B_DQFULL), j & 1, ab)) break;
         tc_fence_after();
         const int q0 = (qb0 + j) * C::BQ;
         const uint32_t stage = sbase + C::OFF_DO + (j % C::NQS) * C::Q_TILE;
@@ -499,7 +511,7 @@ __global__ void __launch_bounds__(512, 1)
       // the four warps never wait on one another.
       const uint32_t stage = sbase + C::OFF_DQ;
       for (int j = 0; j < n; ++j) {
-        if (!mbar_wait_warp(bar(C::B_DQFULL), j & 1, ab)) break;
+        if (!bwait_warp<DP>(bar(C::B_DQFULL), j & 1, ab)) break;
         tc_fence_after();
         uint32_t r[DP];
 #pragma unroll
@@ -546,8 +558,8 @@ __global__ void __launch_bounds__(512, 1)
     for (int j = 0; j < n; ++j) {
       const int st = j % C::NQS;
       const int q0 = (qb0 + j) * C::BQ;
-      if (!(ok = mbar_wait_warp(bar(C::B_QFULL + st), (j / C::NQS) & 1, ab))) break;
-      if (!(ok = mbar_wait_warp(bar(C::B_SFULL), j & 1, ab))) break;
+      if (!(ok = bwait_warp<DP>(bar(C::B_QFULL + st), (j / C::NQS) & 1, ab))) break;
+      if (!(ok = bwait_warp<DP>(bar(C::B_SFULL), j & 1, ab))) break;
       tc_fence_after();
       // query column e of this warpgroup's slice is masked iff e < lim0 (e is q - q0 - g QPW)
       const int lim0 = qmin == INT_MIN ? INT_MIN
@@ -595,10 +607,10 @@ __global__ void __launch_bounds__(512, 1)
       __syncwarp();
       if (lane == 0) mbar_arrive(bar(C::B_PREADY));
 
-      if (!(ok = mbar_wait_warp(bar(C::B_DPFULL), j & 1, ab))) break;
+      if (!(ok = bwait_warp<DP>(bar(C::B_DPFULL), j & 1, ab))) break;
       // the dS^T staging tile is free once its readers of block j - 1 have completed
       // (dQ(j - 1), and at D = 128 dK(j - 1))
-      if (j > 0 && !(ok = mbar_wait_warp(bar(C::B_DSMFREE), (j - 1) & 1, ab))) break;
+      if (j > 0 && !(ok = bwait_warp<DP>(bar(C::B_DSMFREE), (j - 1) & 1, ab))) break;
       tc_fence_after();
 #pragma unroll
       for (int c = 0; c < C::QPW / 32; ++c) {
@@ -645,7 +657,7 @@ __global__ void __launch_bounds__(512, 1)
       }
     }
     // dK (scaled) and dV of this key block
-    if (ok && n > 0) ok = mbar_wait_warp(bar(C::B_ACCDONE), 0, ab);
+    if (ok && n > 0) ok = bwait_warp<DP>(bar(C::B_ACCDONE), 0, ab);
     if (ok && n == 0 && kg < Lk_rows) {
       // no query sees this key block: dK = dV = 0 (warpgroup g writes its half)
       const size_t row = (static_cast<size_t>(bh) * Lk_rows + kg) * D;
