@@ -46,7 +46,7 @@ L2_FLUSH_BYTES = 512 << 20  # > 129 MB L2
 # profiles/ (taken on half of the heads and scaled by 2; per-head traffic is
 # identical). Remove an entry when its kernel changes.
 NCU_TRAFFIC_BYTES = {
-    ("accel_dkdv_dq", 5): 2 * (405.7408e6 + 350.30272e6),
+    ("accel_dkdv_dq", 5): 2 * (404.838144e6 + 349.18912e6),
     ("accel_fwd", 5): 2 * (203.519232e6 + 101.042688e6),
 }
 
